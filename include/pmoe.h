@@ -1,0 +1,182 @@
+/*
+ * pmoe.h -- C ABI of the paged fused-MoE layer forward for GB300 (sm_103a).
+ *
+ * The operation (Rimuru, paper-daily.com/en, section "Expert weights are scattered across
+ * pages. How does the kernel read them?"): a fused MoE layer whose expert weights are not
+ * stored contiguously.  Cached experts sit in pages of one shared page pool, experts copied in
+ * for this step sit in a slot of one of two alternating load buffers, and the kernel takes, per
+ * expert, where it is -- a page number or a buffer slot.  Gate (W1) and up (W3) projections of
+ * an expert occupy one page each and the kernel picks the page by whether the output column n
+ * is in the first or the second half; the element address is
+ *
+ *     addr_e(n, t) = B_P + p_e(n) * f * d + (n mod f) * d + t
+ *
+ * so the page lookup happens once per output tile and reads inside a page use fixed strides.
+ * No contiguous copy of any expert is made.  Section "The adjuster": an expert takes three
+ * pages, W1 (gate), W3 (up) and W2 (down projection).
+ *
+ * Conventions shared by every call below
+ *   bf16       IEEE bfloat16 bit patterns (uint16 storage).
+ *   page       f*d bf16 elements.  W1/W3 pages are [f rows][d cols] row-major (row n = output
+ *              column n of the gate / up projection).  A W2 page is [d rows][f cols] row-major.
+ *   pool       `num_pages` consecutive pages starting at `page_pool` (device memory).
+ *   load buf   load_buf[b] holds `slots_per_buffer` slots; slot s holds the expert's W1, W3, W2
+ *              pages back to back, matrix j at element offset (3*s + j) * f * d.
+ *   page_table int32 [E + S][3] (device): pages of W1, W3, W2 for each routed expert e < E and
+ *              each shared-expert chunk E + s (s < S; always pool-resident).
+ *   buf_slot   int32 [E] (device): -1 = pool-resident (use page_table[e]); otherwise
+ *              b * slots_per_buffer + s = slot s of load buffer b (b in {0, 1}).
+ *   shared     the shared expert of intermediate size S*f is split into S chunks of width f;
+ *              chunk s is the expert E + s with weight 1 on every token.
+ *   ownership  the caller owns every buffer: pool, load buffers, tables, activations, outputs,
+ *              workspace, pinned host memory, streams and events.  The library allocates only
+ *              in pmoe_plan_create (the plan object and one device error word) and frees it in
+ *              pmoe_plan_destroy.  Forward calls allocate nothing and never synchronise the host.
+ *   errors     argument checks are synchronous and return a status.  Table contents are checked
+ *              on the device: an out-of-range page or slot of an expert that the routing
+ *              activates sets the plan's device error word (read it with pmoe_get_device_error)
+ *              and the tiles of that expert are skipped; the output is then undefined.  No call
+ *              traps, asserts or spins on the device.
+ *   streams    every device step of a call is enqueued on the stream given; cudaStream_t and
+ *              cudaEvent_t values are passed as pmoe_stream_t / pmoe_event_t.
+ */
+#ifndef PMOE_H
+#define PMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pmoe_stream_t; /* = cudaStream_t */
+typedef struct CUevent_st* pmoe_event_t;   /* = cudaEvent_t */
+
+typedef enum {
+    PMOE_OK = 0,
+    PMOE_ERR_INVALID_ARG = 1, /* a size, pointer or flag is out of range */
+    PMOE_ERR_PAGE_OOB = 2,    /* device error word: a page index outside [0, num_pages) */
+    PMOE_ERR_SLOT_OOB = 3,    /* device error word: a buffer slot outside [0, 2*slots) */
+    PMOE_ERR_UNSUPPORTED = 4, /* shape the kernels do not cover (see pmoe_plan_create) */
+    PMOE_ERR_CUDA = 5,        /* a CUDA runtime call failed; pmoe_last_error() has the text */
+    PMOE_ERR_TIMEOUT = 6,     /* pmoe_wait_event gave up */
+    PMOE_ERR_WORKSPACE = 7    /* workspace too small for this call */
+} pmoe_status;
+
+/* One MoE layer's shape. */
+typedef struct {
+    int32_t d;                 /* hidden size; multiple of 64 */
+    int32_t f;                 /* per-expert intermediate size; multiple of 128 */
+    int32_t num_experts;       /* E routed experts, 1..1024 */
+    int32_t top_k;             /* k, 1..min(E, 16) */
+    int32_t renormalize;       /* 1: divide the k routing weights by their sum */
+    int32_t num_shared_chunks; /* S >= 0; shared intermediate size S*f; E + S <= 1024 */
+    int32_t slots_per_buffer;  /* expert_offload_limit: slots in each of the two load buffers */
+} pmoe_layer_desc;
+
+typedef struct pmoe_plan* pmoe_plan_t;
+
+/* Kernel families a forward call may use (pmoe_plan_set_path). */
+typedef enum {
+    PMOE_PATH_AUTO = 0,   /* choose by token count */
+    PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
+    PMOE_PATH_TC = 2      /* tcgen05 tensor-core grouped GEMMs (large token counts) */
+} pmoe_path;
+
+/* Text of a status; never NULL. */
+const char* pmoe_status_string(pmoe_status s);
+/* Last error message of the calling thread (empty string if none). */
+const char* pmoe_last_error(void);
+
+/* Create a plan for one layer over a page pool and two load buffers (device pointers, each
+ * 16-byte aligned; load buffers may be NULL when slots_per_buffer == 0).  Builds the TMA tensor
+ * maps that view the pool as rows [num_pages*f, d] (W1/W3 pages) and [num_pages*d, f] (W2
+ * pages), and each load buffer likewise, on the current device; allocates the device error
+ * word.  The pool and the buffers must outlive the plan.  *out receives the plan. */
+pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool, int64_t num_pages,
+                             const void* load_buf0, const void* load_buf1, pmoe_plan_t* out);
+pmoe_status pmoe_plan_destroy(pmoe_plan_t plan);
+/* Force a kernel family (tests, benchmarks); PMOE_PATH_AUTO restores the default. */
+pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path);
+
+/* Measurement hook: while set, each forward call records events[i] on its stream right before
+ * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
+ * recorded), so elapsed times between consecutive events are per-kernel durations.  The kernel
+ * order is: routing, sort-and-pad, [row gather,] gate/up GEMM, down GEMM, combine.  The caller
+ * owns the events; n = 0 (or events = NULL) turns the hook off.  At most 16 events. */
+pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* events, int32_t n);
+
+/* Bytes of device workspace a forward call with up to max_tokens tokens needs (256-aligned
+ * start required).  0 on invalid arguments. */
+size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens);
+
+/* The layer forward.
+ *   hidden        bf16 [T][d] (device)
+ *   router_logits fp32 [T][E] (device); finite values
+ *   top_k         must equal desc->top_k (the pages' signature carries it per call)
+ *   page_table    int32 [E+S][3], buf_slot int32 [E] (device; see the conventions above)
+ *   out           bf16 [T][d] (device); must not alias any input
+ *   workspace     >= pmoe_workspace_size(desc, T) bytes of device memory, 256-byte aligned
+ * Steps, all on `stream`: top-k softmax routing; stable sort of (token, slot) pairs by expert
+ * with padding to the GEMM block size; page resolution and validation; gate/up GEMM with the
+ * SiLU-and-mul epilogue; down GEMM; weighted top-k combine plus the shared expert.
+ * out[t] = bf16( sum_j w[t,j] * y_{t,ids[t,j]} + sum_s y_{t,E+s} ), summed in that order. */
+pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
+                              const float* router_logits, int32_t top_k, const int32_t* page_table,
+                              const int32_t* buf_slot, void* out, void* workspace,
+                              size_t workspace_bytes, pmoe_stream_t stream);
+
+/* The contiguous twin of moe_paged_forward: the same kernels with the page lookup replaced by
+ * fixed addressing, for a plan whose pool holds expert e's W1, W3, W2 as pages 3e, 3e+1, 3e+2
+ * (shared chunk s as expert E+s).  It exists to measure the cost of the page lookup against
+ * a kernel that reads contiguous weights with identical inputs and routing. */
+pmoe_status moe_contig_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
+                               const float* router_logits, int32_t top_k, void* out,
+                               void* workspace, size_t workspace_bytes, pmoe_stream_t stream);
+
+/* Double-buffered expert prefetch (Rimuru, section "Expert weights are scattered across
+ * pages...": two load buffers alternate, one feeds this layer while the other receives the
+ * next layer's experts; section "The adjuster...": finish copying before the table points at
+ * the new location).  On copy_stream: wait for `buf_free` (the last reader of buffer `buf` is
+ * done; may be NULL), then copy n experts from pinned host memory -- host_experts[i] holds
+ * 3*f*d bf16 (W1, W3, W2 back to back) -- into slots slots[i] of load buffer `buf` with one
+ * cudaMemcpyAsync each, then record `copy_done` (may be NULL).  n must be <= slots_per_buffer
+ * and every slot in [0, slots_per_buffer); host_experts and slots are host arrays. */
+pmoe_status pmoe_prefetch_async(pmoe_plan_t plan, int32_t buf, int32_t n,
+                                const void* const* host_experts, const int32_t* slots,
+                                pmoe_stream_t copy_stream, pmoe_event_t buf_free,
+                                pmoe_event_t copy_done);
+
+/* Host-side wait on an event with a timeout (polls cudaEventQuery; never a device spin).
+ * PMOE_OK when the event completed, PMOE_ERR_TIMEOUT after timeout_ms milliseconds. */
+pmoe_status pmoe_wait_event(pmoe_event_t ev, int32_t timeout_ms);
+
+/* Read (and, if clear != 0, reset to 0) the plan's device error word: 0 or a pmoe_status code
+ * raised by a kernel.  Synchronises with `stream` (NULL = legacy default stream). */
+pmoe_status pmoe_get_device_error(pmoe_plan_t plan, int32_t clear, int32_t* code,
+                                  pmoe_stream_t stream);
+
+/* ---- single steps, for tests ------------------------------------------------------------ */
+
+/* Top-k softmax routing: logits fp32 [T][E] -> ids int32 [T][k], weights fp32 [T][k]; top-k on
+ * the logits with ties to the lower expert id, softmax over all E, optional renormalisation.
+ * Device pointers. */
+pmoe_status pmoe_route(const float* router_logits, int32_t T, int32_t E, int32_t top_k,
+                       int32_t renormalize, int32_t* ids, float* weights, pmoe_stream_t stream);
+
+/* Stable sort-and-pad of the T*(k+S) pairs by expert.  Routed pair i = t*k + j goes to expert
+ * ids[i]; shared pair T*k + s*T + t goes to expert E + s.  Experts in ascending id, pairs in
+ * ascending index within an expert; an expert with c > 0 pairs owns ceil(c/block_m) blocks,
+ * pads hold T*(k+S).  Outputs (device): sorted_ids int32 [>= T*(k+S) + (E+S)*(block_m-1)],
+ * block_expert int32 [>= T*(k+S)/block_m + E + S], inv int32 [T*(k+S)] (row of each pair),
+ * n_padded int32 [1].  block_m in {16, 32, 64, 128}; E + S <= 1024. */
+pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, int32_t S,
+                       int32_t block_m, int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
+                       int32_t* n_padded, pmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PMOE_H */

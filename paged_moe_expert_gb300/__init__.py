@@ -1,0 +1,158 @@
+"""Paged fused-MoE layer forward for GB300 (sm_103a) -- Python binding of libpmoe.
+
+The layer (Rimuru, paper-daily.com/en, "Expert weights are scattered across pages. How does the
+kernel read them?") reads each expert's gate (W1), up (W3) and down (W2) projection from pages
+of a shared pool, or from a slot of one of two alternating load buffers, through a per-expert
+page table -- never from a contiguous copy.  Every step runs in libpmoe's CUDA kernels; this
+module only converts torch tensors to pointers and sizes and raises on a bad status.  PyTorch
+supplies device memory, streams and events.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import PATH_AUTO, PATH_STREAM, PATH_TC, LayerDesc, PmoeError
+
+__all__ = ["LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
+           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "make_desc"]
+
+
+def make_desc(d, f, num_experts, top_k, renormalize, num_shared_chunks=0, slots_per_buffer=0):
+    return LayerDesc(int(d), int(f), int(num_experts), int(top_k), int(bool(renormalize)),
+                     int(num_shared_chunks), int(slots_per_buffer))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def workspace_size(desc: LayerDesc, max_tokens: int) -> int:
+    return int(_lib.load().pmoe_workspace_size(ctypes.byref(desc), int(max_tokens)))
+
+
+def alloc_workspace(desc: LayerDesc, max_tokens: int, device="cuda") -> torch.Tensor:
+    n = workspace_size(desc, max_tokens)
+    if n == 0:
+        raise PmoeError(_lib.ERR_INVALID_ARG, "bad descriptor or token count")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+class Plan:
+    """Owns a libpmoe plan over a page pool (bf16, num_pages * f * d elements) and up to two
+    load buffers (bf16, slots_per_buffer * 3 * f * d elements each)."""
+
+    def __init__(self, desc: LayerDesc, pool: torch.Tensor, num_pages: int,
+                 load_bufs=(None, None)):
+        self.desc = desc
+        self._keep = (pool,) + tuple(load_bufs)   # the tensors must outlive the plan
+        h = ctypes.c_void_p()
+        b0, b1 = load_bufs
+        _lib.check(_lib.load().pmoe_plan_create(ctypes.byref(desc), _ptr(pool), int(num_pages),
+                                                _ptr(b0), _ptr(b1), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            _lib.check(_lib.load().pmoe_plan_destroy(self._h))
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_path(self, path: int):
+        _lib.check(_lib.load().pmoe_plan_set_path(self._h, int(path)))
+
+    def forward(self, hidden, logits, page_table, buf_slot, out=None, workspace=None,
+                stream=None):
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty_like(hidden)
+        if workspace is None:
+            workspace = alloc_workspace(self.desc, T, hidden.device)
+        _lib.check(_lib.load().moe_paged_forward(
+            self._h, _ptr(hidden), int(T), _ptr(logits), int(self.desc.top_k), _ptr(page_table),
+            _ptr(buf_slot), _ptr(out), _ptr(workspace), int(workspace.numel()), _stream(stream)))
+        return out
+
+    def contig_forward(self, hidden, logits, out=None, workspace=None, stream=None):
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty_like(hidden)
+        if workspace is None:
+            workspace = alloc_workspace(self.desc, T, hidden.device)
+        _lib.check(_lib.load().moe_contig_forward(
+            self._h, _ptr(hidden), int(T), _ptr(logits), int(self.desc.top_k), _ptr(out),
+            _ptr(workspace), int(workspace.numel()), _stream(stream)))
+        return out
+
+    def set_profile_events(self, events):
+        """Record events[i] before the forward's i-th kernel (and one after the last); pass
+        None or [] to stop.  The events must stay alive while set."""
+        events = list(events or [])
+        arr = (ctypes.c_void_p * max(len(events), 1))(*[e.cuda_event for e in events])
+        self._prof = events
+        _lib.check(_lib.load().pmoe_plan_set_profile_events(self._h, arr, len(events)))
+
+    def device_error(self, clear: bool = True, stream=None) -> int:
+        code = ctypes.c_int32(0)
+        _lib.check(_lib.load().pmoe_get_device_error(self._h, int(bool(clear)), ctypes.byref(code),
+                                                     _stream(stream)))
+        return int(code.value)
+
+
+def route(logits: torch.Tensor, top_k: int, renormalize: bool, stream=None):
+    T, E = logits.shape
+    ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((T, top_k), dtype=torch.float32, device=logits.device)
+    _lib.check(_lib.load().pmoe_route(_ptr(logits), int(T), int(E), int(top_k),
+                                      int(bool(renormalize)), _ptr(ids), _ptr(w), _stream(stream)))
+    return ids, w
+
+
+def align(ids: torch.Tensor, E: int, S: int, block_m: int, stream=None):
+    T, k = ids.shape
+    NP = T * (k + S)
+    dev = ids.device
+    sorted_ids = torch.empty(NP + (E + S) * (block_m - 1) + 1, dtype=torch.int32, device=dev)
+    block_expert = torch.empty(NP // block_m + E + S + 1, dtype=torch.int32, device=dev)
+    inv = torch.empty(max(NP, 1), dtype=torch.int32, device=dev)
+    npad = torch.zeros(1, dtype=torch.int32, device=dev)
+    _lib.check(_lib.load().pmoe_align(_ptr(ids), int(T), int(k), int(E), int(S), int(block_m),
+                                      _ptr(sorted_ids), _ptr(block_expert), _ptr(inv), _ptr(npad),
+                                      _stream(stream)))
+    return sorted_ids, block_expert, inv[:NP], npad
+
+
+def prefetch_async(plan: Plan, buf: int, host_experts, slots, copy_stream, buf_free=None,
+                   copy_done=None):
+    """Copy experts (pinned host tensors of 3*f*d bf16: W1|W3|W2) into slots of load buffer
+    `buf` on `copy_stream`, after `buf_free` and before `copy_done` (torch.cuda.Event or None)."""
+    n = len(host_experts)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in host_experts])
+    sl = (ctypes.c_int32 * max(n, 1))(*[int(s) for s in slots])
+    ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None  # noqa: E731
+    _lib.check(_lib.load().pmoe_prefetch_async(plan._h, int(buf), int(n), ptrs, sl,
+                                               _stream(copy_stream), ev(buf_free), ev(copy_done)))
+
+
+def wait_event(event, timeout_ms: int) -> bool:
+    """True when `event` completed within timeout_ms, False on timeout (host polling)."""
+    st = _lib.load().pmoe_wait_event(ctypes.c_void_p(event.cuda_event), int(timeout_ms))
+    if st == _lib.ERR_TIMEOUT:
+        return False
+    _lib.check(st)
+    return True

@@ -1,0 +1,84 @@
+"""ctypes declarations for libpmoe.so (include/pmoe.h).  Marshalling only.
+
+The library must have been built (``paged_moe_expert_gb300.build.build()``); a missing library
+is an error, never a reason to compute anything elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+P = ctypes.c_void_p
+I32 = ctypes.c_int32
+I64 = ctypes.c_int64
+SZ = ctypes.c_size_t
+
+STATUS = {0: "PMOE_OK", 1: "PMOE_ERR_INVALID_ARG", 2: "PMOE_ERR_PAGE_OOB", 3: "PMOE_ERR_SLOT_OOB",
+          4: "PMOE_ERR_UNSUPPORTED", 5: "PMOE_ERR_CUDA", 6: "PMOE_ERR_TIMEOUT",
+          7: "PMOE_ERR_WORKSPACE"}
+OK, ERR_INVALID_ARG, ERR_PAGE_OOB, ERR_SLOT_OOB, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, \
+    ERR_WORKSPACE = range(8)
+PATH_AUTO, PATH_STREAM, PATH_TC = 0, 1, 2
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("d", I32), ("f", I32), ("num_experts", I32), ("top_k", I32),
+                ("renormalize", I32), ("num_shared_chunks", I32), ("slots_per_buffer", I32)]
+
+
+# name -> (restype, argtypes); mirrors include/pmoe.h
+SIGNATURES = {
+    "pmoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pmoe_last_error": (ctypes.c_char_p, []),
+    "pmoe_plan_create": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, ctypes.POINTER(P)]),
+    "pmoe_plan_destroy": (ctypes.c_int, [P]),
+    "pmoe_plan_set_path": (ctypes.c_int, [P, I32]),
+    "pmoe_plan_set_profile_events": (ctypes.c_int, [P, ctypes.POINTER(P), I32]),
+    "pmoe_workspace_size": (SZ, [ctypes.POINTER(LayerDesc), I32]),
+    "moe_paged_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, P, P, SZ, P]),
+    "moe_contig_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, SZ, P]),
+    "pmoe_prefetch_async": (ctypes.c_int, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(I32), P, P, P]),
+    "pmoe_wait_event": (ctypes.c_int, [P, I32]),
+    "pmoe_get_device_error": (ctypes.c_int, [P, I32, ctypes.POINTER(I32), P]),
+    "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),
+    "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PmoeError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), msg))
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError("libpmoe.so is not built (%s); run "
+                                   "`python -m paged_moe_expert_gb300.build`" % path)
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def check(status: int):
+    if status != OK:
+        lib = load()
+        raise PmoeError(status, lib.pmoe_last_error().decode(errors="replace"))

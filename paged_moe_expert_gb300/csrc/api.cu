@@ -1,0 +1,353 @@
+// C ABI of libpmoe: plans, the paged and contiguous layer forward, the double-buffered
+// prefetch, event waits and error reporting.  Every device step runs in this library's own
+// kernels on the caller's stream; nothing here allocates on the forward path.
+#include <stdio.h>
+#include <string.h>
+
+#include <chrono>
+#include <new>
+#include <string>
+#include <thread>
+
+#include "pmoe_internal.cuh"
+
+namespace pmoe {
+
+static thread_local std::string g_last_error;
+
+static pmoe_status fail(pmoe_status s, const char* msg) {
+    g_last_error = msg;
+    return s;
+}
+
+static pmoe_status cuda_fail(cudaError_t e, const char* where) {
+    g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+    return PMOE_ERR_CUDA;
+}
+
+#define PMOE_CUDA(call, where)                      \
+    do {                                            \
+        cudaError_t e_ = (call);                    \
+        if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+    } while (0)
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static bool desc_ok(const pmoe_layer_desc* D) {
+    if (!D) return false;
+    if (D->d <= 0 || D->f <= 0 || D->num_experts <= 0 || D->top_k <= 0) return false;
+    if (D->top_k > D->num_experts || D->top_k > kMaxTopK) return false;
+    if (D->num_shared_chunks < 0 || D->slots_per_buffer < 0) return false;
+    if (D->num_experts + D->num_shared_chunks > kMaxExpertsTotal) return false;
+    return true;
+}
+
+static bool shape_supported(const pmoe_layer_desc* D) {
+    return D->d % 64 == 0 && D->f % 128 == 0 && D->d <= 16384 && D->f <= 65536;
+}
+
+// Rows per sorted block on the weight-streaming path: the smallest power of two covering the
+// largest possible per-expert token count (T), at most 16, and small enough for the block's
+// tokens to fit in shared memory.
+static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
+    int bm = 1;
+    while (bm < T && bm < kStreamMaxBlockM) bm <<= 1;
+    while (bm > 1 && (size_t)bm * D.d * 2 > 128 * 1024) bm >>= 1;
+    return bm;
+}
+
+static int stream_splits(const pmoe_layer_desc& D) {
+    return (D.f + kStreamKChunk - 1) / kStreamKChunk;
+}
+
+// One layout that serves both kernel families for up to T tokens.
+static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
+    WsLayout W{};
+    const int64_t ES = D.num_experts + D.num_shared_chunks;
+    const int64_t k = D.top_k;
+    W.np = T * (k + D.num_shared_chunks);
+    const int64_t cap_tc = (W.np + ES * (kTcBlockM - 1) + kTcBlockM - 1) / kTcBlockM * kTcBlockM;
+    const int64_t cap_st = W.np + ES * (kStreamMaxBlockM - 1);
+    W.cap = cap_tc > cap_st ? cap_tc : cap_st;
+    W.nblk_max = W.np + ES + 1;  // any block size >= 1
+    W.splits = stream_splits(D);
+    size_t o = 0;
+    W.ids = o;    o = align256(o + sizeof(int32_t) * T * k);
+    W.w = o;      o = align256(o + sizeof(float) * T * k);
+    W.sorted = o; o = align256(o + sizeof(int32_t) * W.cap);
+    W.bexp = o;   o = align256(o + sizeof(int32_t) * W.nblk_max);
+    W.inv = o;    o = align256(o + sizeof(int32_t) * (W.np > 0 ? W.np : 1));
+    W.meta = o;   o = align256(o + sizeof(int32_t) * kMetaCount);
+    W.loc = o;    o = align256(o + sizeof(ExpertLoc) * ES * 3);
+    W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
+    W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
+    const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
+    const size_t y_st = sizeof(float) * (size_t)W.splits * cap_st * D.d;
+    W.y = o;      o = align256(o + (y_tc > y_st ? y_tc : y_st));
+    W.total = o;
+    return W;
+}
+
+// Records the plan's i-th profiling event, if the measurement hook is set.
+static cudaError_t mark(const Plan* P, int i, cudaStream_t s) {
+    return i < P->n_prof ? cudaEventRecord(P->prof_ev[i], s) : cudaSuccess;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const float* logits,
+                                int32_t top_k, const int32_t* page_table, const int32_t* buf_slot,
+                                void* out, void* ws, size_t ws_bytes, cudaStream_t stream,
+                                bool contig) {
+    if (!P) return fail(PMOE_ERR_INVALID_ARG, "plan is NULL");
+    const pmoe_layer_desc& D = P->desc;
+    if (T < 0) return fail(PMOE_ERR_INVALID_ARG, "T < 0");
+    if (top_k != D.top_k) return fail(PMOE_ERR_INVALID_ARG, "top_k differs from the plan's");
+    if (T == 0) return PMOE_OK;
+    if (!hidden || !logits || !out || !ws) return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!contig && (!page_table || (D.num_experts > 0 && !buf_slot)))
+        return fail(PMOE_ERR_INVALID_ARG, "NULL page_table or buf_slot");
+    if (((uintptr_t)ws & 255) || ((uintptr_t)hidden & 15) || ((uintptr_t)out & 15))
+        return fail(PMOE_ERR_INVALID_ARG, "misaligned workspace (256 B) or hidden/out (16 B)");
+    if ((int64_t)T * (D.top_k + D.num_shared_chunks) > (int64_t)1 << 30)
+        return fail(PMOE_ERR_INVALID_ARG, "too many tokens");
+    const WsLayout W = layout(D, T);
+    if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
+
+    int path = P->path;
+    if (path == PMOE_PATH_AUTO) path = PMOE_PATH_STREAM;
+    if (path == PMOE_PATH_TC) return fail(PMOE_ERR_UNSUPPORTED, "tensor-core path not built");
+
+    int32_t* ids = at<int32_t>(ws, W.ids);
+    float* w = at<float>(ws, W.w);
+    int32_t* sorted = at<int32_t>(ws, W.sorted);
+    int32_t* bexp = at<int32_t>(ws, W.bexp);
+    int32_t* inv = at<int32_t>(ws, W.inv);
+    int32_t* meta = at<int32_t>(ws, W.meta);
+    ExpertLoc* loc = at<ExpertLoc>(ws, W.loc);
+    uint16_t* h = at<uint16_t>(ws, W.h);
+    float* y = at<float>(ws, W.y);
+
+    int ev = 0;
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    PMOE_CUDA(launch_route(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w, stream), "route");
+
+    ResolveArgs rs{};
+    rs.page_table = page_table;
+    rs.buf_slot = buf_slot;
+    rs.num_pages = P->num_pages;
+    rs.slots_per_buffer = D.slots_per_buffer;
+    rs.have_buf0 = P->buf[0] != nullptr;
+    rs.have_buf1 = P->buf[1] != nullptr;
+    rs.contiguous = contig ? 1 : 0;
+    rs.loc = loc;
+    rs.err = P->d_error;
+
+    LayerPtrs L{};
+    L.map_base[0] = static_cast<const uint16_t*>(P->pool);
+    L.map_base[1] = static_cast<const uint16_t*>(P->buf[0]);
+    L.map_base[2] = static_cast<const uint16_t*>(P->buf[1]);
+    L.d = D.d; L.f = D.f; L.E = D.num_experts; L.k = D.top_k; L.S = D.num_shared_chunks; L.T = T;
+
+    const int bm = stream_block_m(D, T);
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
+                           inv, meta, &rs, stream), "align");
+    const int64_t ES = D.num_experts + D.num_shared_chunks;
+    const int64_t nblk = (W.np + bm - 1) / bm + (ES < W.np ? ES : W.np);
+    const int64_t ystride = W.np + ES * (bm - 1);
+    const ExpertLoc* lp = contig ? nullptr : loc;
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    PMOE_CUDA(launch_stream_gemm1(L, static_cast<const uint16_t*>(hidden), sorted, bexp, meta, lp,
+                                  bm, nblk, h, stream), "gemm1");
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    PMOE_CUDA(launch_stream_gemm2(L, sorted, bexp, meta, lp, bm, nblk, W.splits, ystride, h, y,
+                                  stream), "gemm2");
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    PMOE_CUDA(launch_combine(y, W.splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
+                             static_cast<uint16_t*>(out), stream), "combine");
+    PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    return PMOE_OK;
+}
+
+}  // namespace pmoe
+
+using namespace pmoe;
+
+extern "C" {
+
+const char* pmoe_status_string(pmoe_status s) {
+    switch (s) {
+        case PMOE_OK: return "ok";
+        case PMOE_ERR_INVALID_ARG: return "invalid argument";
+        case PMOE_ERR_PAGE_OOB: return "page index out of range";
+        case PMOE_ERR_SLOT_OOB: return "load-buffer slot out of range";
+        case PMOE_ERR_UNSUPPORTED: return "unsupported shape or path";
+        case PMOE_ERR_CUDA: return "CUDA error";
+        case PMOE_ERR_TIMEOUT: return "timeout";
+        case PMOE_ERR_WORKSPACE: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+const char* pmoe_last_error(void) { return g_last_error.c_str(); }
+
+pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool, int64_t num_pages,
+                             const void* load_buf0, const void* load_buf1, pmoe_plan_t* out) {
+    if (!out) return fail(PMOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!desc_ok(desc)) return fail(PMOE_ERR_INVALID_ARG, "bad layer descriptor");
+    if (!shape_supported(desc)) return fail(PMOE_ERR_UNSUPPORTED, "d must be a multiple of 64 and f of 128");
+    if (!page_pool || num_pages <= 0) return fail(PMOE_ERR_INVALID_ARG, "empty page pool");
+    if (((uintptr_t)page_pool & 15) || ((uintptr_t)load_buf0 & 15) || ((uintptr_t)load_buf1 & 15))
+        return fail(PMOE_ERR_INVALID_ARG, "pool and buffers must be 16-byte aligned");
+    Plan* P = new (std::nothrow) Plan();
+    if (!P) return fail(PMOE_ERR_INVALID_ARG, "out of host memory");
+    P->desc = *desc;
+    P->pool = page_pool;
+    P->num_pages = num_pages;
+    P->buf[0] = load_buf0;
+    P->buf[1] = load_buf1;
+    P->path = PMOE_PATH_AUTO;
+    cudaError_t e = cudaGetDevice(&P->device);
+    if (e == cudaSuccess) e = cudaMalloc(&P->d_error, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(P->d_error, 0, sizeof(int32_t));
+    if (e != cudaSuccess) {
+        if (P->d_error) cudaFree(P->d_error);
+        delete P;
+        return cuda_fail(e, "plan_create");
+    }
+    *out = reinterpret_cast<pmoe_plan_t>(P);
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_plan_destroy(pmoe_plan_t plan) {
+    if (!plan) return PMOE_OK;
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    cudaError_t e = P->d_error ? cudaFree(P->d_error) : cudaSuccess;
+    delete P;
+    return e == cudaSuccess ? PMOE_OK : cuda_fail(e, "plan_destroy");
+}
+
+pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
+    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC)
+        return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
+    reinterpret_cast<Plan*>(plan)->path = path;
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* events, int32_t n) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P || n < 0 || n > 16 || (n > 0 && !events)) return fail(PMOE_ERR_INVALID_ARG, "bad profile events");
+    for (int i = 0; i < n; ++i) P->prof_ev[i] = (cudaEvent_t)events[i];
+    P->n_prof = n;
+    return PMOE_OK;
+}
+
+size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens) {
+    if (!desc_ok(desc) || max_tokens < 0) return 0;
+    return layout(*desc, max_tokens).total;
+}
+
+pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
+                              const float* router_logits, int32_t top_k, const int32_t* page_table,
+                              const int32_t* buf_slot, void* out, void* workspace,
+                              size_t workspace_bytes, pmoe_stream_t stream) {
+    return forward_impl(reinterpret_cast<Plan*>(plan), hidden, T, router_logits, top_k, page_table,
+                        buf_slot, out, workspace, workspace_bytes, (cudaStream_t)stream, false);
+}
+
+pmoe_status moe_contig_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
+                               const float* router_logits, int32_t top_k, void* out,
+                               void* workspace, size_t workspace_bytes, pmoe_stream_t stream) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (P && P->num_pages < 3 * (int64_t)(P->desc.num_experts + P->desc.num_shared_chunks))
+        return fail(PMOE_ERR_INVALID_ARG, "contiguous plan needs 3*(E+S) pages");
+    return forward_impl(P, hidden, T, router_logits, top_k, nullptr, nullptr, out, workspace,
+                        workspace_bytes, (cudaStream_t)stream, true);
+}
+
+pmoe_status pmoe_prefetch_async(pmoe_plan_t plan, int32_t buf, int32_t n,
+                                const void* const* host_experts, const int32_t* slots,
+                                pmoe_stream_t copy_stream, pmoe_event_t buf_free,
+                                pmoe_event_t copy_done) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P) return fail(PMOE_ERR_INVALID_ARG, "plan is NULL");
+    if (buf != 0 && buf != 1) return fail(PMOE_ERR_INVALID_ARG, "buf must be 0 or 1");
+    if (!P->buf[buf]) return fail(PMOE_ERR_INVALID_ARG, "plan has no such load buffer");
+    const int S = P->desc.slots_per_buffer;
+    if (n < 0 || n > S) return fail(PMOE_ERR_INVALID_ARG, "n exceeds expert_offload_limit");
+    if (n > 0 && (!host_experts || !slots)) return fail(PMOE_ERR_INVALID_ARG, "NULL host arrays");
+    for (int i = 0; i < n; ++i) {
+        if (slots[i] < 0 || slots[i] >= S) return fail(PMOE_ERR_SLOT_OOB, "slot out of range");
+        if (!host_experts[i]) return fail(PMOE_ERR_INVALID_ARG, "NULL host expert");
+        for (int j = 0; j < i; ++j)
+            if (slots[j] == slots[i]) return fail(PMOE_ERR_INVALID_ARG, "duplicate slot");
+    }
+    cudaStream_t cs = (cudaStream_t)copy_stream;
+    if (buf_free) PMOE_CUDA(cudaStreamWaitEvent(cs, (cudaEvent_t)buf_free, 0), "wait buf_free");
+    const size_t bytes = (size_t)3 * P->desc.f * P->desc.d * 2;
+    char* base = static_cast<char*>(const_cast<void*>(P->buf[buf]));
+    for (int i = 0; i < n; ++i)
+        PMOE_CUDA(cudaMemcpyAsync(base + (size_t)slots[i] * bytes, host_experts[i], bytes,
+                                  cudaMemcpyHostToDevice, cs), "prefetch copy");
+    if (copy_done) PMOE_CUDA(cudaEventRecord((cudaEvent_t)copy_done, cs), "record copy_done");
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_wait_event(pmoe_event_t ev, int32_t timeout_ms) {
+    if (!ev) return fail(PMOE_ERR_INVALID_ARG, "event is NULL");
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        const cudaError_t e = cudaEventQuery((cudaEvent_t)ev);
+        if (e == cudaSuccess) return PMOE_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(e, "event query");
+        const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                            std::chrono::steady_clock::now() - t0).count();
+        if (ms >= timeout_ms) return fail(PMOE_ERR_TIMEOUT, "event not complete before timeout");
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+pmoe_status pmoe_get_device_error(pmoe_plan_t plan, int32_t clear, int32_t* code,
+                                  pmoe_stream_t stream) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P || !code) return fail(PMOE_ERR_INVALID_ARG, "NULL plan or code");
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t v = 0;
+    PMOE_CUDA(cudaMemcpyAsync(&v, P->d_error, sizeof v, cudaMemcpyDeviceToHost, s), "read error word");
+    PMOE_CUDA(cudaStreamSynchronize(s), "sync");
+    if (clear) {
+        PMOE_CUDA(cudaMemsetAsync(P->d_error, 0, sizeof(int32_t), s), "clear error word");
+        PMOE_CUDA(cudaStreamSynchronize(s), "sync");
+    }
+    *code = v;
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_route(const float* router_logits, int32_t T, int32_t E, int32_t top_k,
+                       int32_t renormalize, int32_t* ids, float* weights, pmoe_stream_t stream) {
+    if (T < 0 || E <= 0 || E > kMaxExpertsTotal || top_k <= 0 || top_k > E || top_k > kMaxTopK)
+        return fail(PMOE_ERR_INVALID_ARG, "bad routing sizes");
+    if (T > 0 && (!router_logits || !ids || !weights)) return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
+    PMOE_CUDA(launch_route(router_logits, T, E, top_k, renormalize, ids, weights, (cudaStream_t)stream), "route");
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, int32_t S,
+                       int32_t block_m, int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
+                       int32_t* n_padded, pmoe_stream_t stream) {
+    if (T < 0 || top_k <= 0 || E <= 0 || S < 0 || E + S > kMaxExpertsTotal)
+        return fail(PMOE_ERR_INVALID_ARG, "bad align sizes");
+    if (block_m < 1 || block_m > 128 || (block_m & (block_m - 1)))
+        return fail(PMOE_ERR_INVALID_ARG, "block_m must be a power of two <= 128");
+    if (!sorted_ids || !block_expert || !n_padded || (T > 0 && (!ids || !inv)))
+        return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
+    if ((int64_t)T * (top_k + S) > (int64_t)1 << 30) return fail(PMOE_ERR_INVALID_ARG, "too many pairs");
+    PMOE_CUDA(launch_align(ids, T, top_k, E, S, block_m, sorted_ids, block_expert, inv, n_padded,
+                           nullptr, (cudaStream_t)stream), "align");
+    return PMOE_OK;
+}
+
+}  // extern "C"

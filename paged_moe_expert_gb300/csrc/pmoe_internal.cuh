@@ -1,0 +1,114 @@
+// Internal declarations shared by the CUDA translation units of libpmoe (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pmoe.h"
+
+namespace pmoe {
+
+constexpr int kMaxExpertsTotal = 1024;  // E + S
+constexpr int kMaxTopK = 16;
+constexpr int kTcBlockM = 128;          // tensor-core path: rows per sorted block
+constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorted block (max)
+constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
+
+// Where one expert matrix lives: map 0 = pool, 1 = load buffer 0, 2 = load buffer 1; `page` is
+// the page index within that map (for a buffer, 3 * slot + matrix).  map < 0: invalid.
+struct ExpertLoc {
+    int32_t map;
+    int32_t page;
+};
+
+// Byte offsets of the workspace regions for one call (all 256-byte aligned).
+struct WsLayout {
+    size_t ids, w, sorted, bexp, inv, meta, loc, x, h, y, total;
+    int64_t np;          // T * (k + S) pairs
+    int64_t cap;         // rows of sorted_ids / h / y / x
+    int64_t nblk_max;    // upper bound on sorted blocks
+    int block_m;
+    int splits;          // down-GEMM K splits (partial y buffers)
+};
+
+// meta[] slots
+enum { kMetaNPadded = 0, kMetaCount = 16 };
+
+struct Plan {
+    pmoe_layer_desc desc;
+    const void* pool;
+    int64_t num_pages;
+    const void* buf[2];
+    int32_t* d_error;    // device error word
+    int device;
+    int path;            // pmoe_path
+    bool have_tmaps;
+    cudaEvent_t prof_ev[16];   // measurement hook (pmoe_plan_set_profile_events)
+    int n_prof;
+    CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
+    CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
+};
+
+// Device helpers ----------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ void raise_error(int32_t* err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Streaming 16-byte load that does not allocate in L1 (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Host-side launchers (defined in the .cu files) -------------------------------------------
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                         float* w, cudaStream_t s);
+
+struct ResolveArgs {
+    const int32_t* page_table;  // [E+S][3]
+    const int32_t* buf_slot;    // [E]
+    int64_t num_pages;
+    int32_t slots_per_buffer;
+    int32_t have_buf0, have_buf1;
+    int32_t contiguous;         // 1: expert e's matrix j is pool page 3e + j, tables unused
+    ExpertLoc* loc;             // [E+S][3] out
+    int32_t* err;
+};
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
+                         int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
+                         int32_t* meta, const ResolveArgs* resolve, cudaStream_t s);
+
+struct LayerPtrs {
+    const uint16_t* map_base[3];  // pool, buf0, buf1 (bf16 elements)
+    int d, f, E, k, S, T;
+};
+
+cudaError_t launch_stream_gemm1(const LayerPtrs& L, const uint16_t* hidden,
+                                const int32_t* sorted_ids, const int32_t* block_expert,
+                                const int32_t* meta, const ExpertLoc* loc, int block_m,
+                                int64_t nblk_max, uint16_t* h, cudaStream_t s);
+cudaError_t launch_stream_gemm2(const LayerPtrs& L, const int32_t* sorted_ids,
+                                const int32_t* block_expert, const int32_t* meta,
+                                const ExpertLoc* loc, int block_m, int64_t nblk_max, int splits,
+                                int64_t cap, const uint16_t* h, float* y, cudaStream_t s);
+cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float* w,
+                           const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
+                           cudaStream_t s);
+
+}  // namespace pmoe

@@ -1,0 +1,249 @@
+// Top-k softmax routing and the stable sort-and-pad of (token, slot) pairs by expert.
+//
+// Both steps sit ahead of the paged GEMMs of Rimuru's fused MoE kernel (paper-daily.com/en,
+// "Expert weights are scattered across pages. How does the kernel read them?": the paged kernel
+// runs on identical inputs and routing to the contiguous one).  Integer outputs are bit-exact
+// and independent of thread scheduling: routing compares fp32 values exactly, and the sort
+// ranks every pair by (expert, pair index) with warp ballots, not by atomic arrival order.
+#include <math.h>
+
+#include "pmoe_internal.cuh"
+
+namespace pmoe {
+
+// ---------------------------------------------------------------------------------------------
+// Routing: one warp per token.  Lane l holds logits l, l+32, l+64, ... (coalesced loads).  k
+// rounds of a warp argmax over the untaken experts, ordered by (value desc, id asc); softmax
+// over all E with the top-1 value as the max; optional renormalisation of the k weights.
+// ---------------------------------------------------------------------------------------------
+template <int EPL>
+__global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int k, int renorm, int32_t* __restrict__ ids,
+                                                    float* __restrict__ wout) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const float* lg = logits + (int64_t)t * E;
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? lg[e] : -INFINITY;
+    }
+    uint32_t taken = 0;
+    int sel_id[kMaxTopK];
+    float sel_v[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !(taken >> i & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        sel_id[j] = bi;
+        sel_v[j] = bv;
+    }
+    const float mx = sel_v[0];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+        if (lane + 32 * i < E) s += expf(v[i] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    float wsel[kMaxTopK];
+    float wsum = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        wsel[j] = expf(sel_v[j] - mx) / s;
+        wsum += wsel[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        if (lane == j) {
+            ids[(int64_t)t * k + j] = sel_id[j];
+            wout[(int64_t)t * k + j] = renorm ? wsel[j] / wsum : wsel[j];
+        }
+    }
+}
+
+cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                         float* w, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((T + 3) / 4)), block(128);
+    if (E <= 32) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 64) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 128) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 256) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else if (E <= 512) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Sort + pad, one CTA of kAlignWarps warps.
+//   pass A  warp w counts the routed pairs of its contiguous segment per expert (cw[w][e]);
+//   scan    per expert: exclusive prefix of cw over warps; padded offsets off[e] over experts;
+//   pass B  warp w walks its segment 32 pairs at a time; lanes with the same expert get their
+//           rank from a match mask, so every pair lands at off[e] + (pairs of e before it).
+// Shared-chunk pairs are already in order (token t of chunk s is its t-th pair) and pads fill
+// the tail of each expert's last block.  The page resolution for the forward call (which map
+// and page each active expert's three matrices come from, with range checks) runs here too,
+// because it needs the per-expert counts.
+// ---------------------------------------------------------------------------------------------
+constexpr int kAlignWarps = 16;
+
+__global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
+    extern __shared__ int32_t smem[];
+    const int ES = E + S;
+    int32_t* cw = smem;                         // [kAlignWarps][ES]
+    int32_t* cnt = cw + kAlignWarps * ES;       // [ES]
+    int32_t* off = cnt + ES;                    // [ES + 1]
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int NT = kAlignWarps * 32;
+    const int64_t NR = (int64_t)T * k;
+    const int64_t NP = (int64_t)T * (k + S);
+
+    for (int i = tid; i < kAlignWarps * ES; i += NT) cw[i] = 0;
+    __syncthreads();
+
+    const int64_t seg = (NR + kAlignWarps - 1) / kAlignWarps;
+    const int64_t s0 = (int64_t)w * seg;
+    const int64_t s1 = s0 + seg < NR ? s0 + seg : NR;
+    for (int64_t i = s0 + lane; i < s1; i += 32) {
+        int e = ids[i];
+        if (e < 0 || e >= E) e = 0;  // routing output is in range; guard the test entry point
+        atomicAdd(&cw[w * ES + e], 1);
+    }
+    __syncthreads();
+
+    for (int e = tid; e < ES; e += NT) {
+        int c = 0;
+        for (int ww = 0; ww < kAlignWarps; ++ww) {
+            const int x = cw[ww * ES + e];
+            cw[ww * ES + e] = c;
+            c += x;
+        }
+        cnt[e] = e < E ? c : T;
+    }
+    __syncthreads();
+
+    if (w == 0) {  // padded exclusive scan over experts
+        const int per = (ES + 31) / 32;
+        const int b0 = lane * per;
+        int local = 0;
+        for (int e = b0; e < b0 + per && e < ES; ++e)
+            local += (cnt[e] + block_m - 1) / block_m * block_m;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - local;
+        for (int e = b0; e < b0 + per && e < ES; ++e) {
+            off[e] = run;
+            run += (cnt[e] + block_m - 1) / block_m * block_m;
+        }
+        if (lane == 31) off[ES] = incl;
+    }
+    __syncthreads();
+
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t base = s0; base < s1; base += 32) {
+        const int64_t i = base + lane;
+        const bool valid = i < s1;
+        int e = valid ? ids[i] : -1 - lane;
+        if (valid && (e < 0 || e >= E)) e = 0;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (valid) {
+            const int pos = off[e] + cw[w * ES + e] + __popc(peers & lt_mask);
+            sorted_ids[pos] = (int32_t)i;
+            inv[i] = pos;
+        }
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) cw[w * ES + e] += __popc(peers);
+        __syncwarp();
+    }
+    for (int64_t idx = tid; idx < (int64_t)S * T; idx += NT) {
+        const int s = (int)(idx / T), t = (int)(idx % T);
+        const int pos = off[E + s] + t;
+        sorted_ids[pos] = (int32_t)(NR + idx);
+        inv[NR + idx] = pos;
+    }
+    for (int e = tid; e < ES; e += NT) {
+        const int o = off[e], c = cnt[e], end = off[e + 1];
+        for (int r = o + c; r < end; ++r) sorted_ids[r] = (int32_t)NP;
+        for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
+    }
+    if (tid == 0) meta[kMetaNPadded] = off[ES];
+
+    if (do_resolve) {
+        for (int idx = tid; idx < ES * 3; idx += NT) {
+            const int e = idx / 3, j = idx % 3;
+            ExpertLoc L{-1, -1};
+            if (cnt[e] > 0) {
+                if (rs.contiguous) {
+                    L = ExpertLoc{0, 3 * e + j};
+                } else {
+                    const int bs = e < E ? rs.buf_slot[e] : -1;
+                    if (bs >= 0) {
+                        const int b = rs.slots_per_buffer > 0 ? bs / rs.slots_per_buffer : 2;
+                        const bool have = (b == 0 && rs.have_buf0) || (b == 1 && rs.have_buf1);
+                        if (b < 2 && have) L = ExpertLoc{1 + b, 3 * (bs % rs.slots_per_buffer) + j};
+                        else raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+                    } else if (bs == -1) {
+                        const int p = rs.page_table[e * 3 + j];
+                        if (p >= 0 && p < rs.num_pages) L = ExpertLoc{0, p};
+                        else raise_error(rs.err, PMOE_ERR_PAGE_OOB);
+                    } else {
+                        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+                    }
+                }
+            }
+            rs.loc[idx] = L;
+        }
+    }
+}
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
+                         int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
+                         int32_t* meta, const ResolveArgs* resolve, cudaStream_t s) {
+    const int ES = E + S;
+    const size_t smem = sizeof(int32_t) * ((size_t)kAlignWarps * ES + ES + ES + 1);
+    static bool attr_set = false;  // idempotent; racing first calls set the same value
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(int32_t) * ((size_t)kAlignWarps * kMaxExpertsTotal +
+                                                                      2 * kMaxExpertsTotal + 1)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    ResolveArgs rs{};
+    if (resolve) rs = *resolve;
+    align_kernel<<<1, kAlignWarps * 32, smem, s>>>(ids, T, k, E, S, block_m, sorted_ids,
+                                                   block_expert, inv, meta, rs, resolve ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace pmoe

@@ -1,0 +1,130 @@
+"""GPU parity: every step of the CUDA path, called through the C ABI, against the oracle on the
+same seeded inputs.  Integer outputs (routing ids, sorted ids, block map, inverse map, padded
+count) must be bit-exact; the layer output must meet the bf16 tolerance in helpers.py; outputs
+must be bit-identical wherever the weights live (Rimuru, paper-daily.com/en, "Expert weights
+are scattered across pages...": the address rule only relocates rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_moe_expert_gb300 as pm
+from paged_moe_expert_gb300 import pool as pl
+from paged_moe_expert_gb300 import synthetic as syn
+
+from helpers import assert_close, oracle_layer, out_bits, setup_layer
+
+pytestmark = pytest.mark.gpu
+
+
+# --------------------------------------------------------------------------------------------
+# routing and sort + pad
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,E,k,renorm,ties", [(1, 8, 2, True, False), (37, 60, 4, False, False),
+                                                (4096, 512, 10, True, False), (300, 16, 5, True, True),
+                                                (129, 512, 10, False, True), (64, 1024, 16, True, False),
+                                                (5, 3, 3, False, True), (8192, 8, 2, True, False)])
+def test_route_bit_exact(T, E, k, renorm, ties):
+    rng = np.random.default_rng(T * 7 + E)
+    if ties:
+        lg = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    else:
+        lg = syn.bf16_bits_to_f32(syn.to_bf16_bits(rng.standard_normal((T, E)).astype(np.float32)))
+    ids, w = pm.route(torch.from_numpy(lg).cuda(), k, renorm)
+    torch.cuda.synchronize()
+    rids, rw = oracle.route(lg, k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(w.cpu().numpy().astype(np.float64), rw, rtol=3e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,E,k,S,BM", [(16, 8, 2, 0, 16), (37, 60, 4, 4, 16), (4096, 512, 10, 1, 128),
+                                         (4096, 60, 4, 4, 128), (8192, 8, 2, 0, 128), (1, 60, 4, 4, 1),
+                                         (0, 8, 2, 1, 16), (33, 3, 3, 2, 4), (1000, 1000, 16, 24, 64)])
+def test_align_bit_exact(T, E, k, S, BM):
+    rng = np.random.default_rng(T + 3 * E)
+    ids = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32).reshape(T, k)
+    s, b, inv, npad = pm.align(torch.from_numpy(ids).cuda(), E, S, BM)
+    torch.cuda.synchronize()
+    ref = oracle.align(ids, E, S, BM)
+    n = int(npad.item())
+    assert n == ref["n_padded"]
+    assert np.array_equal(s[:n].cpu().numpy(), ref["sorted_ids"])
+    assert np.array_equal(b[:n // BM].cpu().numpy(), ref["block_expert"])
+    if T:
+        assert np.array_equal(inv.cpu().numpy(), ref["inv"])
+
+
+# --------------------------------------------------------------------------------------------
+# the whole layer
+# --------------------------------------------------------------------------------------------
+
+SMALL = [
+    syn.CONFIGS["tiny"],
+    syn.custom_config("ragged", d=192, f=256, E=5, k=3, S=2, renormalize=False, n_buffered=2),
+    syn.custom_config("one_expert", d=64, f=128, E=1, k=1, S=0, n_buffered=0, slots_per_buffer=1),
+    syn.custom_config("wide_k", d=320, f=384, E=16, k=16, S=1, n_buffered=5),
+]
+
+
+@pytest.mark.parametrize("path", [pm.PATH_STREAM])
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+@pytest.mark.parametrize("T", [1, 3, 16, 37])
+def test_forward_matches_oracle(cfg, T, path):
+    L = setup_layer(cfg, T)
+    L.plan.set_path(path)
+    out = L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
+    torch.cuda.synchronize()
+    assert L.plan.device_error() == 0
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
+    assert_close(out_bits(out), ref["out_bf16"], "%s T=%d" % (cfg.name, T))
+
+
+@pytest.mark.parametrize("path", [pm.PATH_STREAM])
+def test_output_independent_of_placement(path):
+    cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
+                            num_pages=60)
+    w = syn.make_weights(cfg)
+    T = 29
+    outs = []
+    for pseed, bidx, nb in [(1, 0, 4), (2, 0, 4), (3, 1, 4), (4, 1, 6), (5, 0, 0)]:
+        L = setup_layer(cfg, T, placement_seed=pseed, buffer_index=bidx, n_buffered=nb, weights=w)
+        L.plan.set_path(path)
+        outs.append(out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)))
+        assert L.plan.device_error() == 0
+    # contiguous twin, same inputs and routing
+    cw = pl.contiguous_weights(cfg, w)
+    cplan = pm.Plan(L.desc, cw, 3 * (cfg.E + cfg.S))
+    cplan.set_path(path)
+    outs.append(out_bits(cplan.contig_forward(L.hidden, L.logits)))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    ref = oracle_layer(cfg, w).forward(L.hidden_np, L.logits_np)
+    assert_close(outs[0], ref["out_bf16"])
+
+
+def test_bad_page_sets_device_error():
+    cfg = syn.CONFIGS["tiny"]
+    L = setup_layer(cfg, 16)
+    pt = L.page_table.clone()
+    ids, _ = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
+    e = int(next(x for x in ids.reshape(-1) if not L.placement.buffered[x]))
+    pt[e, 1] = cfg.num_pages          # one past the end
+    L.plan.forward(L.hidden, L.logits, pt, L.buf_slot)
+    assert L.plan.device_error() == pm._lib.ERR_PAGE_OOB
+    assert L.plan.device_error() == 0   # cleared by the previous read
+    bs = L.buf_slot.clone()
+    bs[e] = 2 * cfg.slots_per_buffer    # past both buffers
+    L.plan.forward(L.hidden, L.logits, L.page_table, bs)
+    assert L.plan.device_error() == pm._lib.ERR_SLOT_OOB
+
+
+def test_invalid_arguments_rejected():
+    cfg = syn.CONFIGS["tiny"]
+    L = setup_layer(cfg, 4)
+    with pytest.raises(pm.PmoeError) as ei:
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot,
+                       workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == pm._lib.ERR_WORKSPACE
+    with pytest.raises(pm.PmoeError):
+        pm.Plan(pm.make_desc(100, 128, 8, 2, True), L.pool, 32)   # d not a multiple of 64
