@@ -1,0 +1,439 @@
+"""Benchmark of the paged fused-MoE layer forward on GB300.
+
+One step = one forward of the Qwen1.5-MoE-shaped layer (d=2048, f=1408, 60 routed experts top-4,
+shared expert 4*1408; 45 experts in random pool pages, 15 in a load buffer) over a batch of
+T=4096 synthetic tokens, with weights, tables and activations resident in HBM.  The JSON line
+reports TFLOP/s (algorithmic: 6*T*d*(k*f + S*f)), the same through host buffers (e2e), the
+dominant kernel against its roofline, the paged-vs-contiguous overhead and a token-count sweep,
+and the CPU oracle's throughput on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config qwen15] [--tokens 4096] [--no-sweep] [--no-cpu]
+
+Under torchrun every rank runs its own replica (the path has no collective); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_moe_expert_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "paged fused-MoE TFLOP/s & weight GB/s vs roofline; overhead vs contiguous"
+PATH_NAMES = {0: "auto", 1: "stream", 2: "tc"}
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------------------------
+
+def work(cfg, T, e_act):
+    """Algorithmic FLOPs and bytes of one forward, and of its two GEMM kernels."""
+    d, f, k, S, E = cfg.d, cfg.f, cfg.k, cfg.S, cfg.E
+    pairs = T * (k + S)
+    flops = 6.0 * T * d * (k * f + S * f)
+    wbytes = 6.0 * d * f * (e_act + S)
+    total_bytes = wbytes + 4.0 * T * d + 4.0 * T * E
+    g1 = {"flops": 4.0 * pairs * d * f, "bytes": 4.0 * d * f * (e_act + S) + 2.0 * pairs * (d + f)}
+    g2 = {"flops": 2.0 * pairs * d * f,
+          "bytes": 2.0 * d * f * (e_act + S) + 2.0 * pairs * f + 4.0 * pairs * d}
+    return {"flops": flops, "weight_bytes": wbytes, "bytes": total_bytes, "gemm1": g1, "gemm2": g2}
+
+
+def binding_fraction(flops, nbytes, seconds, peaks, sustained=True):
+    tc = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"] * 1e12
+    bw = peaks["hbm_gbs"] * 1e9
+    t_roof = max(flops / tc, nbytes / bw)
+    return t_roof / seconds, ("tensor" if flops / tc > nbytes / bw else "hbm")
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.p = None
+        self.path = os.path.join("/tmp", "pmoe_clocks_%d_%d.csv" % (os.getpid(), device_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.QUERY,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "util": float(parts[4]),
+                             "hw_slowdown": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power_cap": parts[9]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in loaded:
+            for key in ("hw_slowdown", "hw_thermal", "sw_thermal", "sw_power_cap"):
+                if r[key].lower() == "active":
+                    reasons.add({"hw_thermal": "hw_thermal_slowdown", "sw_thermal": "sw_thermal_slowdown"}.get(key, key))
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in loaded), "reasons": sorted(reasons),
+                "samples": len(loaded)}
+
+
+# ---------------------------------------------------------------------------------------------
+# the CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------------------------
+
+def oracle_throughput(cfg, w, hidden, logits, budget_s, max_tokens):
+    """Time the oracle, as it stands, on the first n tokens of the batch; n is sized from a
+    short calibration run so the timed run takes about budget_s seconds."""
+    import oracle
+    L = oracle.Layer(w.W1, w.W3, w.W2, cfg.k, cfg.renormalize, W1s=w.W1s, W3s=w.W3s, W2s=w.W2s, S=cfg.S)
+    cores = os.cpu_count() or 1
+    n0 = min(max_tokens, cores)
+    t0 = time.perf_counter()
+    L.forward(hidden[:n0], logits[:n0], nthreads=cores)
+    dt = time.perf_counter() - t0
+    n = int(min(max_tokens, max(n0, n0 * budget_s / max(dt, 1e-6))))
+    n = max(cores, n // cores * cores) if n >= cores else n
+    t0 = time.perf_counter()
+    L.forward(hidden[:n], logits[:n], nthreads=cores)
+    dt = time.perf_counter() - t0
+    flops = 6.0 * n * cfg.d * (cfg.k * cfg.f + cfg.S * cfg.f)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d of %d tokens of the same batch, all experts, fp64 C oracle, %.2f s"
+                      % (n, hidden.shape[0], dt), "tokens": n, "seconds": dt}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    cfg = syn.CONFIGS[args.config]
+    T = args.tokens or cfg.tokens[-1]
+    w = syn.make_weights(cfg)
+    hidden, logits = syn.make_tokens(cfg, T)
+    import oracle
+    L = oracle.Layer(w.W1, w.W3, w.W2, cfg.k, cfg.renormalize, W1s=w.W1s, W3s=w.W3s, W2s=w.W2s, S=cfg.S)
+    cores = os.cpu_count() or 1
+    # size one step to about 4 s of CPU work so warmup + steps end within a few minutes
+    cal = oracle_throughput(cfg, w, hidden, logits, 2.0, T)
+    per_tok = cal["seconds"] / cal["tokens"]
+    n = int(max(1, min(T, 4.0 / per_tok)))
+    for _ in range(args.warmup):
+        L.forward(hidden[:n], logits[:n], nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        L.forward(hidden[:n], logits[:n], nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 6.0 * n * cfg.d * (cfg.k * cfg.f + cfg.S * cfg.f)
+    v = flops / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "%s layer forward, T=%d tokens (each step a %d-token sample)"
+                       % (cfg.name, T, n), "tokens": T, "sample_tokens": n},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "first %d of %d tokens per step" % (n, T)},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+class Layer:
+    def __init__(self, cfg, device, contiguous=True):
+        import paged_moe_expert_gb300 as pm
+        from paged_moe_expert_gb300 import pool as pl
+        self.pm, self.cfg, self.device = pm, cfg, device
+        self.w = syn.make_weights(cfg)
+        self.placement = syn.make_placement(cfg)
+        self.pool = pl.new_pool(cfg.num_pages, cfg.f, cfg.d, device)
+        self.bufs = pl.new_load_buffers(cfg.slots_per_buffer, cfg.f, cfg.d, device)
+        pt, bs = pl.place(cfg, self.w, self.placement, self.pool, self.bufs, 0)
+        self.page_table, self.buf_slot = pt.to(device), bs.to(device)
+        self.desc = pm.make_desc(cfg.d, cfg.f, cfg.E, cfg.k, cfg.renormalize, cfg.S,
+                                 cfg.slots_per_buffer)
+        self.plan = pm.Plan(self.desc, self.pool, cfg.num_pages, self.bufs)
+        self.cplan = None
+        if contiguous:
+            self.cweights = pl.contiguous_weights(cfg, self.w, device)
+            self.cplan = pm.Plan(self.desc, self.cweights, 3 * (cfg.E + cfg.S))
+
+    def tokens(self, T):
+        from paged_moe_expert_gb300 import pool as pl
+        h, lg = syn.make_tokens(self.cfg, T)
+        return h, lg, pl._bf16(h).to(self.device), torch.from_numpy(lg).to(self.device)
+
+    def e_act(self, logits_dev):
+        ids, _ = self.pm.route(logits_dev, self.cfg.k, self.cfg.renormalize)
+        return int(torch.unique(ids).numel())
+
+
+def time_iters(fn_list, iters, flush):
+    """Median device time (s) of each fn, interleaved, L2 flushed before every timed call."""
+    times = [[] for _ in fn_list]
+    s = torch.cuda.current_stream()
+    for _ in range(iters):
+        for i, fn in enumerate(fn_list):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            b.synchronize()
+            times[i].append(a.elapsed_time(b) * 1e-3)
+    return [statistics.median(t) for t in times]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen15", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--tokens", type=int, default=0)
+    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sweep-iters", type=int, default=20)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    import paged_moe_expert_gb300 as pm
+    peaks = load_peaks()
+    cfg = syn.CONFIGS[args.config]
+    T = args.tokens or cfg.tokens[-1]
+    lay = Layer(cfg, device)
+    if args.path != "auto":
+        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC}[args.path]
+        lay.plan.set_path(p)
+        lay.cplan.set_path(p)
+    h_np, lg_np, hidden, logits = lay.tokens(T)
+    e_act = lay.e_act(logits)
+    wk = work(cfg, T, e_act)
+    ws = pm.alloc_workspace(lay.desc, T, device)
+    out = torch.empty_like(hidden)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lay.plan.forward(hidden, logits, lay.page_table, lay.buf_slot, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    path, nk = lay.plan.last_run()
+    assert lay.plan.device_error() == 0
+
+    # per-kernel events for every timed step (the measurement hook of the C ABI)
+    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        lay.plan.set_profile_events(prof[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    lay.plan.set_profile_events(None)
+    sec = t_start.elapsed_time(t_end) * 1e-3 / args.steps
+    if dist:
+        tt = torch.tensor([sec], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        sec = float(tt.item())
+    per_kernel = np.array([[prof[i][j].elapsed_time(prof[i][j + 1]) * 1e-3 for j in range(nk)]
+                           for i in range(args.steps)]).mean(axis=0)
+
+    # e2e: host buffers in, result out, copies inside the timed region
+    h_host = hidden.cpu().pin_memory()
+    l_host = logits.cpu().pin_memory()
+    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        hidden.copy_(h_host, non_blocking=True)
+        logits.copy_(l_host, non_blocking=True)
+        step()
+        o_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_sec = e0.elapsed_time(e1) * 1e-3 / args.steps
+    if dist:
+        tt = torch.tensor([e2e_sec], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_sec = float(tt.item())
+
+    # token-count sweep with the contiguous twin (L2 flushed before every timed call)
+    sweep = []
+    if not args.no_sweep and rank == 0:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+        for Ts in cfg.tokens:
+            _, _, hs, ls = lay.tokens(Ts)
+            wss = pm.alloc_workspace(lay.desc, Ts, device)
+            os_ = torch.empty_like(hs)
+            fp = lambda: lay.plan.forward(hs, ls, lay.page_table, lay.buf_slot, out=os_, workspace=wss)  # noqa: E731
+            fc = lambda: lay.cplan.contig_forward(hs, ls, out=os_, workspace=wss)  # noqa: E731
+            for _ in range(3):
+                fp(); fc()
+            tp, tc = time_iters([fp, fc], args.sweep_iters, flush)
+            ps, _ = lay.plan.last_run()
+            ea = lay.e_act(ls)
+            wk_s = work(cfg, Ts, ea)
+            frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks)
+            sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "ms": tp * 1e3,
+                          "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
+                          "tflops": wk_s["flops"] / tp / 1e12,
+                          "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
+                          "tokens_per_s": Ts / tp, "experts_active": ea,
+                          "binding_roof": bound, "roof_frac": frac})
+            del wss
+    clk = clocks.stop()
+
+    # dominant kernel against its roofline
+    names = ["route", "align"] + (["gather"] if path == pm.PATH_TC else []) + ["gemm1", "gemm2", "combine"]
+    names = names[:nk]
+    dom = int(np.argmax(per_kernel))
+    kname = names[dom]
+    kwork = wk.get(kname, {"flops": 0.0, "bytes": 0.0})
+    ksec = float(per_kernel[dom])
+    if path == pm.PATH_TC and kwork["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "tensor", "achieved": kwork["flops"] / ksec / 1e12,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    elif path != pm.PATH_TC and kwork["flops"] / 80e12 > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+        # CUDA-core fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock
+        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": kwork["flops"] / ksec / 1e12, "peak": alu_peak,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": kwork["bytes"] / ksec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = kname
+    roof["peak_source"] = peaks["source"]
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = oracle_throughput(cfg, lay.w, h_np, lg_np, 15.0, T)
+
+    overhead = None
+    for s_ in sweep:
+        if s_["tokens"] == T:
+            overhead = s_["overhead_vs_contig"]
+    value = wk["flops"] * world / sec / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s layer forward (d=%d f=%d E=%d top-%d shared %d), T=%d tokens, "
+                               "%d pool-resident / %d buffered experts"
+                               % (cfg.name, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S * cfg.f, T,
+                                  cfg.E - cfg.n_buffered, cfg.n_buffered),
+                   "tokens": T, "path": PATH_NAMES[path], "experts_active": e_act,
+                   "weight_gbs": wk["weight_bytes"] * world / sec / 1e9,
+                   "tokens_per_s": T * world / sec,
+                   "l2": "inputs larger than L2 (%.0f MB of expert weights per step); sweep flushes L2"
+                         % (wk["weight_bytes"] / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": wk["flops"] * world / e2e_sec / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(hidden.numel() * 2 + logits.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 2)},
+        "gpu_launches": int(nk * args.steps),
+        "clocks": clk,
+        "kernels_ms": {n: float(t) * 1e3 for n, t in zip(names, per_kernel)},
+        "overhead_vs_contig": overhead,
+        "sweep": sweep,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

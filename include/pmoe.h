@@ -100,6 +100,10 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan);
 /* Force a kernel family (tests, benchmarks); PMOE_PATH_AUTO restores the default. */
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path);
 
+/* The kernel family (pmoe_path) the plan's last forward call ran and how many kernels it
+ * launched (0 and 0 before the first call). */
+pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_kernels);
+
 /* Measurement hook: while set, each forward call records events[i] on its stream right before
  * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
  * recorded), so elapsed times between consecutive events are per-kernel durations.  The kernel

@@ -37,6 +37,16 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _event(e, stream=None):
+    """cudaEvent_t of a torch.cuda.Event; torch creates the event on its first record, so an
+    event never recorded is recorded once here (on `stream`) to bring it into existence."""
+    if e is None:
+        return None
+    if e.cuda_event == 0:
+        e.record(stream if stream is not None else torch.cuda.current_stream())
+    return ctypes.c_void_p(e.cuda_event)
+
+
 def workspace_size(desc: LayerDesc, max_tokens: int) -> int:
     return int(_lib.load().pmoe_workspace_size(ctypes.byref(desc), int(max_tokens)))
 
@@ -99,11 +109,17 @@ class Plan:
             _ptr(workspace), int(workspace.numel()), _stream(stream)))
         return out
 
+    def last_run(self):
+        """(path, number of kernels) of the last forward call."""
+        p, n = ctypes.c_int32(0), ctypes.c_int32(0)
+        _lib.check(_lib.load().pmoe_plan_last_run(self._h, ctypes.byref(p), ctypes.byref(n)))
+        return int(p.value), int(n.value)
+
     def set_profile_events(self, events):
         """Record events[i] before the forward's i-th kernel (and one after the last); pass
         None or [] to stop.  The events must stay alive while set."""
         events = list(events or [])
-        arr = (ctypes.c_void_p * max(len(events), 1))(*[e.cuda_event for e in events])
+        arr = (ctypes.c_void_p * max(len(events), 1))(*[_event(e).value for e in events])
         self._prof = events
         _lib.check(_lib.load().pmoe_plan_set_profile_events(self._h, arr, len(events)))
 
@@ -144,13 +160,17 @@ def prefetch_async(plan: Plan, buf: int, host_experts, slots, copy_stream, buf_f
     n = len(host_experts)
     ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in host_experts])
     sl = (ctypes.c_int32 * max(n, 1))(*[int(s) for s in slots])
-    ev = lambda e: ctypes.c_void_p(e.cuda_event) if e is not None else None  # noqa: E731
+    # an event that was never recorded has nothing to wait for
+    free = _event(buf_free) if (buf_free is not None and buf_free.cuda_event != 0) else None
     _lib.check(_lib.load().pmoe_prefetch_async(plan._h, int(buf), int(n), ptrs, sl,
-                                               _stream(copy_stream), ev(buf_free), ev(copy_done)))
+                                               _stream(copy_stream), free,
+                                               _event(copy_done, copy_stream)))
 
 
 def wait_event(event, timeout_ms: int) -> bool:
     """True when `event` completed within timeout_ms, False on timeout (host polling)."""
+    if event.cuda_event == 0:
+        return True   # never recorded: nothing pending
     st = _lib.load().pmoe_wait_event(ctypes.c_void_p(event.cuda_event), int(timeout_ms))
     if st == _lib.ERR_TIMEOUT:
         return False

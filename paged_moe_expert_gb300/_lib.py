@@ -36,6 +36,7 @@ SIGNATURES = {
     "pmoe_plan_create": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, ctypes.POINTER(P)]),
     "pmoe_plan_destroy": (ctypes.c_int, [P]),
     "pmoe_plan_set_path": (ctypes.c_int, [P, I32]),
+    "pmoe_plan_last_run": (ctypes.c_int, [P, ctypes.POINTER(I32), ctypes.POINTER(I32)]),
     "pmoe_plan_set_profile_events": (ctypes.c_int, [P, ctypes.POINTER(P), I32]),
     "pmoe_workspace_size": (SZ, [ctypes.POINTER(LayerDesc), I32]),
     "moe_paged_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, P, P, SZ, P]),

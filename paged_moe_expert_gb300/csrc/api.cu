@@ -168,6 +168,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     PMOE_CUDA(launch_combine(y, W.splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
                              static_cast<uint16_t*>(out), stream), "combine");
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
+    P->last_path = path;
+    P->last_kernels = ev - 1;
     return PMOE_OK;
 }
 
@@ -234,6 +236,14 @@ pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
     if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC)
         return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
     reinterpret_cast<Plan*>(plan)->path = path;
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_kernels) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P || !path || !n_kernels) return fail(PMOE_ERR_INVALID_ARG, "NULL argument");
+    *path = P->last_path;
+    *n_kernels = P->last_kernels;
     return PMOE_OK;
 }
 

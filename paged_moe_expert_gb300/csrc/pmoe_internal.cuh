@@ -47,6 +47,7 @@ struct Plan {
     bool have_tmaps;
     cudaEvent_t prof_ev[16];   // measurement hook (pmoe_plan_set_profile_events)
     int n_prof;
+    int last_path, last_kernels;  // what the last forward ran
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
 };
