@@ -56,6 +56,9 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
     return bm;
 }
 
+// Token counts up to which the automatic path picks the weight-streaming kernels.
+constexpr int kStreamMaxTokens = 16;
+
 static int stream_splits(const pmoe_layer_desc& D) {
     return (D.f + kStreamKChunk - 1) / kStreamKChunk;
 }
@@ -116,8 +119,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
 
     int path = P->path;
-    if (path == PMOE_PATH_AUTO) path = PMOE_PATH_STREAM;
-    if (path == PMOE_PATH_TC) return fail(PMOE_ERR_UNSUPPORTED, "tensor-core path not built");
+    if (path == PMOE_PATH_AUTO) path = T <= kStreamMaxTokens ? PMOE_PATH_STREAM : PMOE_PATH_TC;
+    if (path == PMOE_PATH_TC && !P->have_tmaps)
+        return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
 
     int32_t* ids = at<int32_t>(ws, W.ids);
     float* w = at<float>(ws, W.w);
@@ -126,8 +130,17 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     int32_t* inv = at<int32_t>(ws, W.inv);
     int32_t* meta = at<int32_t>(ws, W.meta);
     ExpertLoc* loc = at<ExpertLoc>(ws, W.loc);
+    uint16_t* x = at<uint16_t>(ws, W.x);
     uint16_t* h = at<uint16_t>(ws, W.h);
     float* y = at<float>(ws, W.y);
+
+    CUtensorMap xmap, hmap;
+    const int64_t ES = D.num_experts + D.num_shared_chunks;
+    const int64_t cap_tc = (W.np + ES * (kTcBlockM - 1) + kTcBlockM - 1) / kTcBlockM * kTcBlockM;
+    if (path == PMOE_PATH_TC) {
+        if (!encode_rows_map(&xmap, x, cap_tc, D.d) || !encode_rows_map(&hmap, h, cap_tc, D.f))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+    }
 
     int ev = 0;
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
@@ -144,28 +157,43 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     rs.loc = loc;
     rs.err = P->d_error;
 
-    LayerPtrs L{};
-    L.map_base[0] = static_cast<const uint16_t*>(P->pool);
-    L.map_base[1] = static_cast<const uint16_t*>(P->buf[0]);
-    L.map_base[2] = static_cast<const uint16_t*>(P->buf[1]);
-    L.d = D.d; L.f = D.f; L.E = D.num_experts; L.k = D.top_k; L.S = D.num_shared_chunks; L.T = T;
-
-    const int bm = stream_block_m(D, T);
+    const int bm = path == PMOE_PATH_TC ? kTcBlockM : stream_block_m(D, T);
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
                            inv, meta, &rs, stream), "align");
-    const int64_t ES = D.num_experts + D.num_shared_chunks;
     const int64_t nblk = (W.np + bm - 1) / bm + (ES < W.np ? ES : W.np);
-    const int64_t ystride = W.np + ES * (bm - 1);
-    const ExpertLoc* lp = contig ? nullptr : loc;
+    int64_t ystride;
+    int splits;
+    if (path == PMOE_PATH_TC) {
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_gather(static_cast<const uint16_t*>(hidden), sorted, meta, T, D.top_k,
+                                D.num_shared_chunks, D.d, cap_tc, x, stream), "gather");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
+                                 P->num_sms, P->d_error, stream), "gate/up gemm");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
+                                 P->num_sms, P->d_error, stream), "down gemm");
+        ystride = cap_tc;
+        splits = 1;
+    } else {
+        LayerPtrs L{};
+        L.map_base[0] = static_cast<const uint16_t*>(P->pool);
+        L.map_base[1] = static_cast<const uint16_t*>(P->buf[0]);
+        L.map_base[2] = static_cast<const uint16_t*>(P->buf[1]);
+        L.d = D.d; L.f = D.f; L.E = D.num_experts; L.k = D.top_k; L.S = D.num_shared_chunks; L.T = T;
+        ystride = W.np + ES * (bm - 1);
+        splits = W.splits;
+        const ExpertLoc* lp = contig ? nullptr : loc;
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_stream_gemm1(L, static_cast<const uint16_t*>(hidden), sorted, bexp, meta,
+                                      lp, bm, nblk, h, stream), "gemm1");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_stream_gemm2(L, sorted, bexp, meta, lp, bm, nblk, splits, ystride, h, y,
+                                      stream), "gemm2");
+    }
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_stream_gemm1(L, static_cast<const uint16_t*>(hidden), sorted, bexp, meta, lp,
-                                  bm, nblk, h, stream), "gemm1");
-    PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_stream_gemm2(L, sorted, bexp, meta, lp, bm, nblk, W.splits, ystride, h, y,
-                                  stream), "gemm2");
-    PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_combine(y, W.splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
+    PMOE_CUDA(launch_combine(y, splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
                              static_cast<uint16_t*>(out), stream), "combine");
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
@@ -213,6 +241,7 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
     P->buf[1] = load_buf1;
     P->path = PMOE_PATH_AUTO;
     cudaError_t e = cudaGetDevice(&P->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
     if (e == cudaSuccess) e = cudaMalloc(&P->d_error, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(P->d_error, 0, sizeof(int32_t));
     if (e != cudaSuccess) {
@@ -220,6 +249,22 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
         delete P;
         return cuda_fail(e, "plan_create");
     }
+    // TMA views of the pool and the buffers: rows [pages*f, d] for gate/up pages, rows
+    // [pages*d, f] for down pages; a buffer slot s holds its matrices as pages 3s, 3s+1, 3s+2.
+    const int64_t f = desc->f, d = desc->d;
+    const int64_t bpages = 3 * (int64_t)desc->slots_per_buffer;
+    bool ok = encode_rows_map(&P->tm_rows_d[0], page_pool, num_pages * f, d) &&
+              encode_rows_map(&P->tm_rows_f[0], page_pool, num_pages * d, f);
+    for (int b = 0; b < 2 && ok; ++b) {
+        if (P->buf[b] && bpages > 0) {
+            ok = encode_rows_map(&P->tm_rows_d[1 + b], P->buf[b], bpages * f, d) &&
+                 encode_rows_map(&P->tm_rows_f[1 + b], P->buf[b], bpages * d, f);
+        } else {
+            P->tm_rows_d[1 + b] = P->tm_rows_d[0];   // never addressed: no slot maps here
+            P->tm_rows_f[1 + b] = P->tm_rows_f[0];
+        }
+    }
+    P->have_tmaps = ok;
     *out = reinterpret_cast<pmoe_plan_t>(P);
     return PMOE_OK;
 }

@@ -48,6 +48,7 @@ struct Plan {
     cudaEvent_t prof_ev[16];   // measurement hook (pmoe_plan_set_profile_events)
     int n_prof;
     int last_path, last_kernels;  // what the last forward ran
+    int num_sms;
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
 };
@@ -110,6 +111,16 @@ cudaError_t launch_stream_gemm2(const LayerPtrs& L, const int32_t* sorted_ids,
                                 int64_t cap, const uint16_t* h, float* y, cudaStream_t s);
 cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float* w,
                            const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
+                           cudaStream_t s);
+
+// Tensor-core path (tc_gemm.cu)
+bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
+cudaError_t launch_gather(const uint16_t* hidden, const int32_t* sorted_ids, const int32_t* meta,
+                          int T, int k, int S, int d, int64_t cap, uint16_t* x, cudaStream_t s);
+// mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32)
+cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
+                           const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
+                           void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
                            cudaStream_t s);
 
 }  // namespace pmoe

@@ -67,20 +67,24 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("path", [pm.PATH_STREAM])
+PATHS = [pm.PATH_STREAM, pm.PATH_TC]
+
+
+@pytest.mark.parametrize("path", PATHS, ids=["stream", "tc"])
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-@pytest.mark.parametrize("T", [1, 3, 16, 37])
+@pytest.mark.parametrize("T", [1, 3, 16, 37, 300])
 def test_forward_matches_oracle(cfg, T, path):
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
     out = L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
     torch.cuda.synchronize()
     assert L.plan.device_error() == 0
+    assert L.plan.last_run()[0] == path
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
     assert_close(out_bits(out), ref["out_bf16"], "%s T=%d" % (cfg.name, T))
 
 
-@pytest.mark.parametrize("path", [pm.PATH_STREAM])
+@pytest.mark.parametrize("path", PATHS, ids=["stream", "tc"])
 def test_output_independent_of_placement(path):
     cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
                             num_pages=60)
@@ -128,3 +132,24 @@ def test_invalid_arguments_rejected():
     assert ei.value.status == pm._lib.ERR_WORKSPACE
     with pytest.raises(pm.PmoeError):
         pm.Plan(pm.make_desc(100, 128, 8, 2, True), L.pool, 32)   # d not a multiple of 64
+
+
+def test_auto_path_by_token_count():
+    cfg = syn.CONFIGS["tiny"]
+    for T, want in [(1, pm.PATH_STREAM), (16, pm.PATH_STREAM), (17, pm.PATH_TC), (512, pm.PATH_TC)]:
+        L = setup_layer(cfg, T)
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
+        assert L.plan.last_run()[0] == want
+
+
+@pytest.mark.parametrize("T", [16, 300])
+def test_paths_agree(T):
+    cfg = syn.custom_config("agree", d=256, f=256, E=6, k=2, S=1, n_buffered=2)
+    L = setup_layer(cfg, T)
+    outs = []
+    for path in PATHS:
+        L.plan.set_path(path)
+        outs.append(out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)))
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
+    for o in outs:
+        assert_close(o, ref["out_bf16"])
