@@ -139,6 +139,27 @@ pmoe_status moe_contig_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
                                const float* router_logits, int32_t top_k, void* out,
                                void* workspace, size_t workspace_bytes, pmoe_stream_t stream);
 
+/* The layer forward without any device allocation, for callers that cannot allocate device
+ * memory when they run the layer (for example server plugins or embedded runtimes given a fixed
+ * device-memory budget at start-up, or latency-critical loops where cudaMalloc would block
+ * until in-flight work finishes); they cannot create a plan either, since a plan owns a device
+ * allocation.  The paper has no counterpart: this is a convenience of this library.
+ * Same arguments and result as moe_paged_forward, with the plan's pool, buffers and descriptor
+ * passed directly; it runs the weight-streaming kernels.  Its scratch is one fixed 16 MiB
+ * device array inside the library, which every GPU that loads the library holds until the
+ * process exits; a call whose layer and T need more returns PMOE_ERR_WORKSPACE (the
+ * Qwen1.5-MoE-shaped layer fits up to 16 tokens).  All calls share that array and it keeps the
+ * last call's contents, so calls that overlap on the GPU (other streams, other threads) race:
+ * serialise them.  device_error (device int32, may be NULL) receives a table error code and is
+ * not cleared by the call.  The first call on a device looks up the array's device address
+ * (with that device current); make that first call before any stream capture. */
+pmoe_status moe_paged_forward_noalloc(const pmoe_layer_desc* desc, const void* page_pool,
+                                      int64_t num_pages, const void* load_buf0,
+                                      const void* load_buf1, const void* hidden, int32_t T,
+                                      const float* router_logits, int32_t top_k,
+                                      const int32_t* page_table, const int32_t* buf_slot,
+                                      void* out, int32_t* device_error, pmoe_stream_t stream);
+
 /* Double-buffered expert prefetch (Rimuru, section "Expert weights are scattered across
  * pages...": two load buffers alternate, one feeds this layer while the other receives the
  * next layer's experts; section "The adjuster...": finish copying before the table points at

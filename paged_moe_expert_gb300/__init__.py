@@ -130,6 +130,20 @@ class Plan:
         return int(code.value)
 
 
+def forward_noalloc(desc: LayerDesc, pool, num_pages, load_bufs, hidden, logits, page_table,
+                    buf_slot, out=None, device_error=None, stream=None):
+    """moe_paged_forward_noalloc: the layer forward with the library's fixed scratch instead of
+    a plan and a workspace (no device allocation in the call; decode-size token counts)."""
+    if out is None:
+        out = torch.empty_like(hidden)
+    b0, b1 = load_bufs
+    _lib.check(_lib.load().moe_paged_forward_noalloc(
+        ctypes.byref(desc), _ptr(pool), int(num_pages), _ptr(b0), _ptr(b1), _ptr(hidden),
+        int(hidden.shape[0]), _ptr(logits), int(desc.top_k), _ptr(page_table), _ptr(buf_slot),
+        _ptr(out), _ptr(device_error), _stream(stream)))
+    return out
+
+
 def route(logits: torch.Tensor, top_k: int, renormalize: bool, stream=None):
     T, E = logits.shape
     ids = torch.empty((T, top_k), dtype=torch.int32, device=logits.device)

@@ -41,6 +41,8 @@ SIGNATURES = {
     "pmoe_workspace_size": (SZ, [ctypes.POINTER(LayerDesc), I32]),
     "moe_paged_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, P, P, SZ, P]),
     "moe_contig_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, SZ, P]),
+    "moe_paged_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, P, I32, P,
+                                                  I32, P, P, P, P, P]),
     "pmoe_prefetch_async": (ctypes.c_int, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(I32), P, P, P]),
     "pmoe_wait_event": (ctypes.c_int, [P, I32]),
     "pmoe_get_device_error": (ctypes.c_int, [P, I32, ctypes.POINTER(I32), P]),
