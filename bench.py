@@ -64,6 +64,26 @@ def work(cfg, T, e_act):
     return {"flops": flops, "weight_bytes": wbytes, "bytes": total_bytes, "gemm1": g1, "gemm2": g2}
 
 
+def measured_traffic(cfg_key, T, kernel):
+    """DRAM traffic per launch (read + write bytes) of `kernel` from the committed ncu summary of
+    this workload, or None when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "tc_gemm_%s_T%d.md" % (cfg_key, T))
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("traffic_"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "paged_moe_expert_gb300", "csrc", "tc_gemm.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("traffic_source_sha256_prefix") != sha:
+        return None
+    v = fields.get("traffic_%s_bytes_per_launch" % kernel)
+    return int(v) if v else None
+
+
 def binding_fraction(flops, nbytes, seconds, peaks, sustained=True):
     tc = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"] * 1e12
     bw = peaks["hbm_gbs"] * 1e9
@@ -220,6 +240,20 @@ class Layer:
         return int(torch.unique(ids).numel())
 
 
+def max_over_ranks(seconds: float, dist, device) -> float:
+    """The slowest rank's time: every rank's replica must finish before the step is done."""
+    if dist is None:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def time_iters(fn_list, iters, flush):
     """Median device time (s) of each fn, interleaved, L2 flushed before every timed call."""
     times = [[] for _ in fn_list]
@@ -270,11 +304,12 @@ def main():
     peaks = load_peaks()
     cfg = syn.CONFIGS[args.config]
     T = args.tokens or cfg.tokens[-1]
-    lay = Layer(cfg, device)
+    lay = Layer(cfg, device, contiguous=not args.no_sweep)
     if args.path != "auto":
         p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC}[args.path]
         lay.plan.set_path(p)
-        lay.cplan.set_path(p)
+        if lay.cplan is not None:
+            lay.cplan.set_path(p)
     h_np, lg_np, hidden, logits = lay.tokens(T)
     e_act = lay.e_act(logits)
     wk = work(cfg, T, e_act)
@@ -309,11 +344,7 @@ def main():
     if dist:
         dist.barrier()
     lay.plan.set_profile_events(None)
-    sec = t_start.elapsed_time(t_end) * 1e-3 / args.steps
-    if dist:
-        tt = torch.tensor([sec], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        sec = float(tt.item())
+    sec = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3 / args.steps, dist, device)
     per_kernel = np.array([[prof[i][j].elapsed_time(prof[i][j + 1]) * 1e-3 for j in range(nk)]
                            for i in range(args.steps)]).mean(axis=0)
 
@@ -339,11 +370,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_sec = e0.elapsed_time(e1) * 1e-3 / args.steps
-    if dist:
-        tt = torch.tensor([e2e_sec], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_sec = float(tt.item())
+    e2e_sec = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, dist, device)
 
     # token-count sweep with the contiguous twin (L2 flushed before every timed call)
     sweep = []
@@ -390,7 +417,7 @@ def main():
         roof = {"bound": "hbm", "achieved": kwork["bytes"] / ksec / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(args.config, T, kname) if path == pm.PATH_TC else None
     roof["kernel"] = kname
     roof["peak_source"] = peaks["source"]
 
@@ -402,7 +429,7 @@ def main():
     for s_ in sweep:
         if s_["tokens"] == T:
             overhead = s_["overhead_vs_contig"]
-    value = wk["flops"] * world / sec / 1e12
+    value = job_throughput(wk["flops"], world, sec) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
@@ -412,14 +439,14 @@ def main():
                                % (cfg.name, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S * cfg.f, T,
                                   cfg.E - cfg.n_buffered, cfg.n_buffered),
                    "tokens": T, "path": PATH_NAMES[path], "experts_active": e_act,
-                   "weight_gbs": wk["weight_bytes"] * world / sec / 1e9,
-                   "tokens_per_s": T * world / sec,
+                   "weight_gbs": job_throughput(wk["weight_bytes"], world, sec) / 1e9,
+                   "tokens_per_s": job_throughput(T, world, sec),
                    "l2": "inputs larger than L2 (%.0f MB of expert weights per step); sweep flushes L2"
                          % (wk["weight_bytes"] / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
-        "e2e": {"value": wk["flops"] * world / e2e_sec / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(wk["flops"], world, e2e_sec) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(hidden.numel() * 2 + logits.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 2)},
         "gpu_launches": int(nk * args.steps),
