@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 from paged_moe_expert_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "paged fused-MoE TFLOP/s & weight GB/s vs roofline; overhead vs contiguous"
-PATH_NAMES = {0: "auto", 1: "stream", 2: "tc"}
+PATH_NAMES = {0: "auto", 1: "stream", 2: "tc", 3: "tc_decode"}
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -240,6 +240,10 @@ class Layer:
         return int(torch.unique(ids).numel())
 
 
+def tc_family_path(path):
+    return path in (2, 3)
+
+
 def max_over_ranks(seconds: float, dist, device) -> float:
     """The slowest rank's time: every rank's replica must finish before the step is done."""
     if dist is None:
@@ -252,6 +256,20 @@ def max_over_ranks(seconds: float, dist, device) -> float:
 def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
     """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
     return units_per_rank * world / seconds
+
+
+def capture(fn):
+    """fn's launches captured once into a CUDA graph (replayed by the sweep)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
 
 
 def time_iters(fn_list, iters, flush):
@@ -278,7 +296,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="qwen15", choices=sorted(syn.CONFIGS))
     ap.add_argument("--tokens", type=int, default=0)
-    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc"])
+    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc", "tc_decode"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-iters", type=int, default=20)
@@ -306,7 +324,7 @@ def main():
     T = args.tokens or cfg.tokens[-1]
     lay = Layer(cfg, device, contiguous=not args.no_sweep)
     if args.path != "auto":
-        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC}[args.path]
+        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC, "tc_decode": pm.PATH_TC_DECODE}[args.path]
         lay.plan.set_path(p)
         if lay.cplan is not None:
             lay.cplan.set_path(p)
@@ -326,8 +344,23 @@ def main():
     path, nk = lay.plan.last_run()
     assert lay.plan.device_error() == 0
 
-    # per-kernel events for every timed step (the measurement hook of the C ABI)
-    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    # which kernel dominates: one untimed pass with an event before every kernel
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    lay.plan.set_profile_events(probe)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    lay.plan.set_profile_events(None)
+    probe_ms = [probe[j].elapsed_time(probe[j + 1]) for j in range(nk)]
+    dom = int(np.argmax(probe_ms))
+
+    # timed region: K steps, the dominant kernel bracketed by its own events in every step
+    prof = []
+    for _ in range(args.steps):
+        evs = [None] * (nk + 1)
+        evs[dom] = torch.cuda.Event(enable_timing=True)
+        evs[dom + 1] = torch.cuda.Event(enable_timing=True)
+        prof.append(evs)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -345,8 +378,7 @@ def main():
         dist.barrier()
     lay.plan.set_profile_events(None)
     sec = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3 / args.steps, dist, device)
-    per_kernel = np.array([[prof[i][j].elapsed_time(prof[i][j + 1]) * 1e-3 for j in range(nk)]
-                           for i in range(args.steps)]).mean(axis=0)
+    dom_sec = float(np.mean([prof[i][dom].elapsed_time(prof[i][dom + 1]) for i in range(args.steps)])) * 1e-3
 
     # e2e: host buffers in, result out, copies inside the timed region
     h_host = hidden.cpu().pin_memory()
@@ -384,12 +416,13 @@ def main():
             fc = lambda: lay.cplan.contig_forward(hs, ls, out=os_, workspace=wss)  # noqa: E731
             for _ in range(3):
                 fp(); fc()
-            tp, tc = time_iters([fp, fc], args.sweep_iters, flush)
             ps, _ = lay.plan.last_run()
+            gp, gc = capture(fp), capture(fc)
+            tp, tc = time_iters([gp.replay, gc.replay], args.sweep_iters, flush)
             ea = lay.e_act(ls)
             wk_s = work(cfg, Ts, ea)
             frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks)
-            sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "ms": tp * 1e3,
+            sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "launch": "cuda_graph", "ms": tp * 1e3,
                           "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
                           "tflops": wk_s["flops"] / tp / 1e12,
                           "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
@@ -399,16 +432,20 @@ def main():
     clk = clocks.stop()
 
     # dominant kernel against its roofline
-    names = ["route", "align"] + (["gather"] if path == pm.PATH_TC else []) + ["gemm1", "gemm2", "combine"]
-    names = names[:nk]
-    dom = int(np.argmax(per_kernel))
+    if nk == 6:
+        names = ["route", "align", "gather", "gemm1", "gemm2", "combine"]
+    elif nk == 5:
+        names = (["prep", "gather"] if tc_family_path(path) else ["route", "align"]) + ["gemm1", "gemm2", "combine"]
+    else:
+        names = ["prep", "gemm1", "gemm2", "combine"]
     kname = names[dom]
     kwork = wk.get(kname, {"flops": 0.0, "bytes": 0.0})
-    ksec = float(per_kernel[dom])
-    if path == pm.PATH_TC and kwork["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+    ksec = dom_sec
+    tc_family = path in (pm.PATH_TC, pm.PATH_TC_DECODE)
+    if tc_family and kwork["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
         roof = {"bound": "tensor", "achieved": kwork["flops"] / ksec / 1e12,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
-    elif path != pm.PATH_TC and kwork["flops"] / 80e12 > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+    elif not tc_family and kwork["flops"] / 80e12 > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
         # CUDA-core fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock
         alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": kwork["flops"] / ksec / 1e12, "peak": alu_peak,
@@ -451,7 +488,7 @@ def main():
                 "d2h_bytes_per_step": int(out.numel() * 2)},
         "gpu_launches": int(nk * args.steps),
         "clocks": clk,
-        "kernels_ms": {n: float(t) * 1e3 for n, t in zip(names, per_kernel)},
+        "kernels_ms": {n: float(t) for n, t in zip(names, probe_ms)},
         "overhead_vs_contig": overhead,
         "sweep": sweep,
     }

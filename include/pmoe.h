@@ -71,7 +71,7 @@ typedef struct {
     int32_t num_experts;       /* E routed experts, 1..1024 */
     int32_t top_k;             /* k, 1..min(E, 16) */
     int32_t renormalize;       /* 1: divide the k routing weights by their sum */
-    int32_t num_shared_chunks; /* S >= 0; shared intermediate size S*f; E + S <= 1024 */
+    int32_t num_shared_chunks; /* S >= 0; shared intermediate size S*f; E + S <= 1024, k + S <= 64 */
     int32_t slots_per_buffer;  /* expert_offload_limit: slots in each of the two load buffers */
 } pmoe_layer_desc;
 
@@ -81,7 +81,9 @@ typedef struct pmoe_plan* pmoe_plan_t;
 typedef enum {
     PMOE_PATH_AUTO = 0,   /* choose by token count */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
-    PMOE_PATH_TC = 2      /* tcgen05 tensor-core grouped GEMMs (large token counts) */
+    PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
+    PMOE_PATH_TC_DECODE = 3 /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
+                               on N: weight streaming for small token counts */
 } pmoe_path;
 
 /* Text of a status; never NULL. */
@@ -107,8 +109,10 @@ pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_kerne
 /* Measurement hook: while set, each forward call records events[i] on its stream right before
  * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
  * recorded), so elapsed times between consecutive events are per-kernel durations.  The kernel
- * order is: routing, sort-and-pad, [row gather,] gate/up GEMM, down GEMM, combine.  The caller
- * owns the events; n = 0 (or events = NULL) turns the hook off.  At most 16 events. */
+ * order is: routing, sort-and-pad, [row gather,] gate/up GEMM, down GEMM, combine, where for
+ * T <= 128 routing and sort-and-pad are one kernel.  NULL entries
+ * are skipped (to bracket one kernel only).  The caller owns the events; n = 0 (or events = NULL)
+ * turns the hook off.  At most 16 events. */
 pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* events, int32_t n);
 
 /* Bytes of device workspace a forward call with up to max_tokens tokens needs (256-aligned
@@ -125,7 +129,9 @@ size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens);
  * Steps, all on `stream`: top-k softmax routing; stable sort of (token, slot) pairs by expert
  * with padding to the GEMM block size; page resolution and validation; gate/up GEMM with the
  * SiLU-and-mul epilogue; down GEMM; weighted top-k combine plus the shared expert.
- * out[t] = bf16( sum_j w[t,j] * y_{t,ids[t,j]} + sum_s y_{t,E+s} ), summed in that order. */
+ * out[t] = bf16( sum_j w[t,j] * y_{t,ids[t,j]} + sum_s y_{t,E+s} ), summed in that order.
+ * The call neither allocates nor synchronises, so it can be captured in a CUDA graph; the
+ * captured launches keep the addresses of this call's buffers and workspace. */
 pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
                               const float* router_logits, int32_t top_k, const int32_t* page_table,
                               const int32_t* buf_slot, void* out, void* workspace,

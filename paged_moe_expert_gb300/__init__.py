@@ -14,10 +14,10 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PATH_AUTO, PATH_STREAM, PATH_TC, LayerDesc, PmoeError
+from ._lib import PATH_AUTO, PATH_STREAM, PATH_TC, PATH_TC_DECODE, LayerDesc, PmoeError
 
 __all__ = ["LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
-           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "make_desc"]
+           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "make_desc"]
 
 
 def make_desc(d, f, num_experts, top_k, renormalize, num_shared_chunks=0, slots_per_buffer=0):
@@ -119,7 +119,8 @@ class Plan:
         """Record events[i] before the forward's i-th kernel (and one after the last); pass
         None or [] to stop.  The events must stay alive while set."""
         events = list(events or [])
-        arr = (ctypes.c_void_p * max(len(events), 1))(*[_event(e).value for e in events])
+        arr = (ctypes.c_void_p * max(len(events), 1))(
+            *[(_event(e).value if e is not None else None) for e in events])
         self._prof = events
         _lib.check(_lib.load().pmoe_plan_set_profile_events(self._h, arr, len(events)))
 

@@ -39,6 +39,7 @@ static bool desc_ok(const pmoe_layer_desc* D) {
     if (D->top_k > D->num_experts || D->top_k > kMaxTopK) return false;
     if (D->num_shared_chunks < 0 || D->slots_per_buffer < 0) return false;
     if (D->num_experts + D->num_shared_chunks > kMaxExpertsTotal) return false;
+    if (D->top_k + D->num_shared_chunks > kMaxPairsPerToken) return false;
     return true;
 }
 
@@ -56,11 +57,40 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
     return bm;
 }
 
-// Token counts up to which the automatic path picks the weight-streaming kernels.
-constexpr int kStreamMaxTokens = 16;
+// Token counts up to which the automatic path picks the small-batch tensor-core kernels, and
+// up to which routing, sort + pad and the row gather run as one single-CTA kernel.
+constexpr int kSwapMaxTokens = 128;
+constexpr int kPrepSmallMaxTokens = 128;
 
 static int stream_splits(const pmoe_layer_desc& D) {
     return (D.f + kStreamKChunk - 1) / kStreamKChunk;
+}
+
+// Small-batch tensor-core path: tokens per block (MMA N), K splits of the down projection and the
+// row stride of its partial outputs.  BN covers the largest per-expert token count (T, reached by
+// the shared chunks) up to 128; the down projection is split along K until there are about two
+// tiles per SM (taking ~160 SMs so the workspace size does not depend on the device).
+struct SwapParams {
+    int bn, splits;
+    int64_t ystride;
+};
+static SwapParams swap_params(const pmoe_layer_desc& D, int64_t T) {
+    SwapParams p{};
+    int bn = 16;
+    while (bn < T && bn < 128) bn <<= 1;
+    p.bn = bn;
+    const int64_t ES = D.num_experts + D.num_shared_chunks;
+    const int64_t np = T * (D.top_k + D.num_shared_chunks);
+    const int64_t active = ES < np ? ES : np;
+    p.ystride = np + active * (bn - 1);
+    const int64_t kb = D.f / 64, wt = (D.d + 127) / 128;
+    int64_t sp = (320 + active * wt - 1) / (active * wt > 0 ? active * wt : 1);
+    if (sp < 1) sp = 1;
+    if (sp > 8) sp = 8;
+    if (sp > kb) sp = kb;
+    const int64_t per = (kb + sp - 1) / sp;
+    p.splits = (int)((kb + per - 1) / per);   // every split non-empty
+    return p;
 }
 
 // One layout that serves both kernel families for up to T tokens.
@@ -86,14 +116,18 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
     const size_t y_st = sizeof(float) * (size_t)W.splits * cap_st * D.d;
-    W.y = o;      o = align256(o + (y_tc > y_st ? y_tc : y_st));
+    const SwapParams sw = swap_params(D, T);
+    const size_t y_sw = sizeof(float) * (size_t)sw.splits * sw.ystride * D.d;
+    size_t y_max = y_tc > y_st ? y_tc : y_st;
+    if (y_sw > y_max) y_max = y_sw;
+    W.y = o;      o = align256(o + y_max);
     W.total = o;
     return W;
 }
 
 // Records the plan's i-th profiling event, if the measurement hook is set.
 static cudaError_t mark(const Plan* P, int i, cudaStream_t s) {
-    return i < P->n_prof ? cudaEventRecord(P->prof_ev[i], s) : cudaSuccess;
+    return (i < P->n_prof && P->prof_ev[i]) ? cudaEventRecord(P->prof_ev[i], s) : cudaSuccess;
 }
 
 template <typename T>
@@ -119,8 +153,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
 
     int path = P->path;
-    if (path == PMOE_PATH_AUTO) path = T <= kStreamMaxTokens ? PMOE_PATH_STREAM : PMOE_PATH_TC;
-    if (path == PMOE_PATH_TC && !P->have_tmaps)
+    if (path == PMOE_PATH_AUTO) path = T <= kSwapMaxTokens ? PMOE_PATH_TC_DECODE : PMOE_PATH_TC;
+    const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE;
+    if (tc_family && !P->have_tmaps)
         return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
 
     int32_t* ids = at<int32_t>(ws, W.ids);
@@ -137,14 +172,15 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     CUtensorMap xmap, hmap;
     const int64_t ES = D.num_experts + D.num_shared_chunks;
     const int64_t cap_tc = (W.np + ES * (kTcBlockM - 1) + kTcBlockM - 1) / kTcBlockM * kTcBlockM;
+    const SwapParams sw = swap_params(D, T);
     if (path == PMOE_PATH_TC) {
-        if (!encode_rows_map(&xmap, x, cap_tc, D.d) || !encode_rows_map(&hmap, h, cap_tc, D.f))
+        if (!encode_rows_map(&xmap, x, cap_tc, D.d, kTcBlockM) ||
+            !encode_rows_map(&hmap, h, cap_tc, D.f, kTcBlockM))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+    } else if (path == PMOE_PATH_TC_DECODE) {
+        if (!encode_rows_map(&xmap, x, cap_tc, D.d, sw.bn) || !encode_rows_map(&hmap, h, cap_tc, D.f, sw.bn))
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
     }
-
-    int ev = 0;
-    PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_route(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w, stream), "route");
 
     ResolveArgs rs{};
     rs.page_table = page_table;
@@ -157,17 +193,32 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     rs.loc = loc;
     rs.err = P->d_error;
 
-    const int bm = path == PMOE_PATH_TC ? kTcBlockM : stream_block_m(D, T);
-    PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
-                           inv, meta, &rs, stream), "align");
+    const int bm = path == PMOE_PATH_TC ? kTcBlockM
+                 : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
+    const uint16_t* hid = static_cast<const uint16_t*>(hidden);
+    int ev = 0;
+    if (T <= kPrepSmallMaxTokens) {
+        // one CTA: routing, sort + pad + page resolution
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_prep_small(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w,
+                                    D.num_shared_chunks, bm, sorted, bexp, inv, meta, rs, hid, D.d,
+                                    nullptr, stream), "prep");
+    } else {
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_route(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w, stream), "route");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
+                               inv, meta, &rs, stream), "align");
+    }
+    if (tc_family) {
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_gather_pairs(hid, inv, T, D.top_k, D.num_shared_chunks, D.d, x, stream),
+                  "gather");
+    }
     const int64_t nblk = (W.np + bm - 1) / bm + (ES < W.np ? ES : W.np);
     int64_t ystride;
     int splits;
     if (path == PMOE_PATH_TC) {
-        PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_gather(static_cast<const uint16_t*>(hidden), sorted, meta, T, D.top_k,
-                                D.num_shared_chunks, D.d, cap_tc, x, stream), "gather");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
                                  P->num_sms, P->d_error, stream), "gate/up gemm");
@@ -176,6 +227,17 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
                                  P->num_sms, P->d_error, stream), "down gemm");
         ystride = cap_tc;
         splits = 1;
+    } else if (path == PMOE_PATH_TC_DECODE) {
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_swap(1, contig, sw.bn, xmap, P->tm_rows_d, sorted, T, D.top_k,
+                                 D.num_shared_chunks, bexp, meta, loc, h, D.f, D.d, 1, 0, nblk,
+                                 P->num_sms, P->d_error, stream), "gate/up gemm");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_swap(2, contig, sw.bn, hmap, P->tm_rows_f, sorted, T, D.top_k,
+                                 D.num_shared_chunks, bexp, meta, loc, y, D.f, D.d, sw.splits,
+                                 sw.ystride, nblk, P->num_sms, P->d_error, stream), "down gemm");
+        ystride = sw.ystride;
+        splits = sw.splits;
     } else {
         LayerPtrs L{};
         L.map_base[0] = static_cast<const uint16_t*>(P->pool);
@@ -186,8 +248,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         splits = W.splits;
         const ExpertLoc* lp = contig ? nullptr : loc;
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_stream_gemm1(L, static_cast<const uint16_t*>(hidden), sorted, bexp, meta,
-                                      lp, bm, nblk, h, stream), "gemm1");
+        PMOE_CUDA(launch_stream_gemm1(L, hid, sorted, bexp, meta, lp, bm, nblk, h, stream), "gemm1");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_stream_gemm2(L, sorted, bexp, meta, lp, bm, nblk, splits, ystride, h, y,
                                       stream), "gemm2");
@@ -278,7 +339,7 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan) {
 }
 
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
-    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC)
+    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC_DECODE)
         return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
     reinterpret_cast<Plan*>(plan)->path = path;
     return PMOE_OK;

@@ -96,7 +96,8 @@ extern "C" pmoe_status moe_paged_forward_noalloc(
     int32_t* device_error, pmoe_stream_t stream) {
     if (!desc || desc->d <= 0 || desc->f <= 0 || desc->num_experts <= 0 || desc->top_k <= 0 ||
         desc->top_k > desc->num_experts || desc->top_k > kMaxTopK || desc->num_shared_chunks < 0 ||
-        desc->slots_per_buffer < 0 || desc->num_experts + desc->num_shared_chunks > kMaxExpertsTotal)
+        desc->slots_per_buffer < 0 || desc->num_experts + desc->num_shared_chunks > kMaxExpertsTotal ||
+        desc->top_k + desc->num_shared_chunks > kMaxPairsPerToken)
         return na_fail(PMOE_ERR_INVALID_ARG, "bad layer descriptor");
     if (desc->d % 64 != 0 || desc->f % 128 != 0)
         return na_fail(PMOE_ERR_UNSUPPORTED, "d must be a multiple of 64 and f of 128");

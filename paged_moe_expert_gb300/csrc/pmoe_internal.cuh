@@ -12,6 +12,7 @@ namespace pmoe {
 
 constexpr int kMaxExpertsTotal = 1024;  // E + S
 constexpr int kMaxTopK = 16;
+constexpr int kMaxPairsPerToken = 64;   // k + S
 constexpr int kTcBlockM = 128;          // tensor-core path: rows per sorted block
 constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorted block (max)
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
@@ -96,6 +97,16 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int blo
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
                          int32_t* meta, const ResolveArgs* resolve, cudaStream_t s);
 
+// Small batches: routing + sort/pad/resolve + row gather (x may be NULL: no gather) in one CTA.
+cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                              float* w, int S, int block_m, int32_t* sorted_ids,
+                              int32_t* block_expert, int32_t* inv, int32_t* meta,
+                              const ResolveArgs& rs, const uint16_t* hidden, int d, uint16_t* x,
+                              cudaStream_t s);
+// X[inv[i]] = hidden[token of pair i] for all T*(k+S) pairs (pad rows untouched).
+cudaError_t launch_gather_pairs(const uint16_t* hidden, const int32_t* inv, int T, int k, int S,
+                                int d, uint16_t* x, cudaStream_t s);
+
 struct LayerPtrs {
     const uint16_t* map_base[3];  // pool, buf0, buf1 (bf16 elements)
     int d, f, E, k, S, T;
@@ -114,13 +125,20 @@ cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float*
                            cudaStream_t s);
 
 // Tensor-core path (tc_gemm.cu)
-bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
-cudaError_t launch_gather(const uint16_t* hidden, const int32_t* sorted_ids, const int32_t* meta,
-                          int T, int k, int S, int d, int64_t cap, uint16_t* x, cudaStream_t s);
+bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                     int box_rows = 128);
 // mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
+                           cudaStream_t s);
+
+// Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials.
+cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act,
+                           const CUtensorMap* wmaps, const int32_t* sorted_ids, int T, int k,
+                           int S, const int32_t* block_expert, const int32_t* meta,
+                           const ExpertLoc* loc, void* out, int f, int d, int splits,
+                           int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
                            cudaStream_t s);
 
 }  // namespace pmoe

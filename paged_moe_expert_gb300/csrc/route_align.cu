@@ -17,13 +17,9 @@ namespace pmoe {
 // over all E with the top-1 value as the max; optional renormalisation of the k weights.
 // ---------------------------------------------------------------------------------------------
 template <int EPL>
-__global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,
-                                                    int k, int renorm, int32_t* __restrict__ ids,
-                                                    float* __restrict__ wout) {
-    const int lane = threadIdx.x & 31;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= T) return;
-    const float* lg = logits + (int64_t)t * E;
+__device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int k, int renorm,
+                                            int lane, int32_t* __restrict__ ids_out,
+                                            float* __restrict__ w_out) {
     float v[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
@@ -78,10 +74,21 @@ __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ lo
     for (int j = 0; j < kMaxTopK; ++j) {
         if (j >= k) break;
         if (lane == j) {
-            ids[(int64_t)t * k + j] = sel_id[j];
-            wout[(int64_t)t * k + j] = renorm ? wsel[j] / wsum : wsel[j];
+            ids_out[j] = sel_id[j];
+            w_out[j] = renorm ? wsel[j] / wsum : wsel[j];
         }
     }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,
+                                                    int k, int renorm, int32_t* __restrict__ ids,
+                                                    float* __restrict__ wout) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    route_token<EPL>(logits + (int64_t)t * E, E, k, renorm, lane, ids + (int64_t)t * k,
+                     wout + (int64_t)t * k);
 }
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
@@ -110,11 +117,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 // ---------------------------------------------------------------------------------------------
 constexpr int kAlignWarps = 16;
 
-__global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
+__device__ __forceinline__ void align_block(
     const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
-    int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
-    extern __shared__ int32_t smem[];
+    int32_t* __restrict__ inv, int32_t* __restrict__ meta, const ResolveArgs& rs, int do_resolve,
+    int32_t* smem) {
     const int ES = E + S;
     int32_t* cw = smem;                         // [kAlignWarps][ES]
     int32_t* cnt = cw + kAlignWarps * ES;       // [ES]
@@ -226,6 +233,59 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
     }
 }
 
+__global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
+    int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
+    extern __shared__ int32_t smem[];
+    align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, do_resolve, smem);
+}
+
+// Copy the hidden row of every (token, expert) pair to its sorted row: X[inv[i]] = hidden[token
+// of pair i].  Pad rows are left as they are: in both MMA orientations a pad row only feeds
+// outputs of its own row, which nothing reads.
+__device__ __forceinline__ void gather_pair(const uint16_t* __restrict__ hidden,
+                                            const int32_t* __restrict__ inv, int i, int T, int k,
+                                            int d, int lane, uint16_t* __restrict__ x) {
+    const int NR = T * k;
+    const int t = i < NR ? i / k : (i - NR) % T;
+    const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)t * d);
+    uint4* dst = reinterpret_cast<uint4*>(x + (int64_t)inv[i] * d);
+    for (int c = lane; c < (d >> 3); c += 32) dst[c] = src[c];
+}
+
+__global__ void __launch_bounds__(256) gather_pairs_kernel(const uint16_t* __restrict__ hidden,
+                                                           const int32_t* __restrict__ inv, int T,
+                                                           int k, int S, int d,
+                                                           uint16_t* __restrict__ x) {
+    const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (i >= T * (k + S)) return;
+    gather_pair(hidden, inv, i, T, k, d, threadIdx.x & 31, x);
+}
+
+// Small batches: routing and sort + pad (with page resolution) in one CTA, so a decode step spends
+// one launch on them instead of two; the optional row gather is for callers without a separate
+// multi-CTA gather.
+template <int EPL>
+__global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int renorm, int32_t* __restrict__ ids,
+    float* __restrict__ wout, int S, int block_m, int32_t* __restrict__ sorted_ids,
+    int32_t* __restrict__ block_expert, int32_t* __restrict__ inv, int32_t* __restrict__ meta,
+    ResolveArgs rs, const uint16_t* __restrict__ hidden, int d, uint16_t* __restrict__ x) {
+    extern __shared__ int32_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < T; t += kAlignWarps)
+        route_token<EPL>(logits + (int64_t)t * E, E, k, renorm, lane, ids + (int64_t)t * k,
+                         wout + (int64_t)t * k);
+    __syncthreads();
+    align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, 1, smem);
+    __syncthreads();
+    if (x) {
+        const int NP = T * (k + S);
+        for (int i = warp; i < NP; i += kAlignWarps) gather_pair(hidden, inv, i, T, k, d, lane, x);
+    }
+}
+
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
                          int32_t* meta, const ResolveArgs* resolve, cudaStream_t s) {
@@ -244,6 +304,57 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int blo
     align_kernel<<<1, kAlignWarps * 32, smem, s>>>(ids, T, k, E, S, block_m, sorted_ids,
                                                    block_expert, inv, meta, rs, resolve ? 1 : 0);
     return cudaGetLastError();
+}
+
+static size_t align_smem_bytes(int ES) {
+    return sizeof(int32_t) * ((size_t)kAlignWarps * ES + ES + ES + 1);
+}
+
+static cudaError_t allow_align_smem(const void* fn) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)align_smem_bytes(kMaxExpertsTotal));
+}
+
+cudaError_t launch_gather_pairs(const uint16_t* hidden, const int32_t* inv, int T, int k, int S,
+                                int d, uint16_t* x, cudaStream_t s) {
+    const int64_t np = (int64_t)T * (k + S);
+    if (np == 0) return cudaSuccess;
+    gather_pairs_kernel<<<(unsigned)((np + 7) / 8), 256, 0, s>>>(hidden, inv, T, k, S, d, x);
+    return cudaGetLastError();
+}
+
+template <int EPL>
+static cudaError_t prep_small_epl(const float* logits, int T, int E, int k, int renorm,
+                                  int32_t* ids, float* w, int S, int block_m, int32_t* sorted_ids,
+                                  int32_t* block_expert, int32_t* inv, int32_t* meta,
+                                  const ResolveArgs& rs, const uint16_t* hidden, int d,
+                                  uint16_t* x, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = allow_align_smem(reinterpret_cast<const void*>(prep_small_kernel<EPL>));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    prep_small_kernel<EPL><<<1, kAlignWarps * 32, align_smem_bytes(E + S), s>>>(
+        logits, T, E, k, renorm, ids, w, S, block_m, sorted_ids, block_expert, inv, meta, rs,
+        hidden, d, x);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                              float* w, int S, int block_m, int32_t* sorted_ids,
+                              int32_t* block_expert, int32_t* inv, int32_t* meta,
+                              const ResolveArgs& rs, const uint16_t* hidden, int d, uint16_t* x,
+                              cudaStream_t s) {
+#define PREP(EPL) prep_small_epl<EPL>(logits, T, E, k, renorm, ids, w, S, block_m, sorted_ids, \
+                                      block_expert, inv, meta, rs, hidden, d, x, s)
+    if (E <= 32) return PREP(1);
+    if (E <= 64) return PREP(2);
+    if (E <= 128) return PREP(4);
+    if (E <= 256) return PREP(8);
+    if (E <= 512) return PREP(16);
+    return PREP(32);
+#undef PREP
 }
 
 }  // namespace pmoe

@@ -281,50 +281,71 @@ cudaError_t launch_stream_gemm2(const LayerPtrs& L, const int32_t* sorted_ids,
 
 // ---------------------------------------------------------------------------------------------
 // Combine: out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]] + sum_s y[inv[T*k + s*T + t]] ), with
-// each y the sum of its K-split partials; the order of every sum is fixed, so the output does
-// not depend on where the experts live or on scheduling.
+// each y the sum of its K-split partials; the order of every sum is fixed (pairs in order j, then
+// shared chunks s, each a fused multiply-add with weight 1 for the shared ones), so the output
+// does not depend on where the experts live or on scheduling.  A thread owns four columns of one
+// token and issues the loads of up to eight pairs before it adds any of them.
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, int splits,
-                                                      int64_t ystride, const float* __restrict__ w,
-                                                      const int32_t* __restrict__ inv, int T, int d,
-                                                      int k, int S, uint16_t* __restrict__ out) {
-    const int t = blockIdx.x;
+constexpr int kCombineThreads = 64;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const float* __restrict__ y, int splits, int64_t ystride, const float* __restrict__ w,
+    const int32_t* __restrict__ inv, int T, int d, int k, int S, uint16_t* __restrict__ out) {
+    const int t = blockIdx.y;
+    const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // float4 column
+    const int P = k + S;
     const int64_t NR = (int64_t)T * k;
-    const int dq = d >> 2;
-    for (int c = threadIdx.x; c < dq; c += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int64_t r = inv[(int64_t)t * k + j];
-            const float wj = w[(int64_t)t * k + j];
-            float4 ys = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < splits; ++sp) {
-                const float4 v = reinterpret_cast<const float4*>(y + ((int64_t)sp * ystride + r) * d)[c];
-                ys.x += v.x; ys.y += v.y; ys.z += v.z; ys.w += v.w;
-            }
-            acc.x = fmaf(wj, ys.x, acc.x);
-            acc.y = fmaf(wj, ys.y, acc.y);
-            acc.z = fmaf(wj, ys.z, acc.z);
-            acc.w = fmaf(wj, ys.w, acc.w);
-        }
-        for (int s = 0; s < S; ++s) {
-            const int64_t r = inv[NR + (int64_t)s * T + t];
-            for (int sp = 0; sp < splits; ++sp) {
-                const float4 v = reinterpret_cast<const float4*>(y + ((int64_t)sp * ystride + r) * d)[c];
-                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-            }
-        }
-        uint2 o;
-        o.x = (uint32_t)f32_to_bf16_bits(acc.x) | ((uint32_t)f32_to_bf16_bits(acc.y) << 16);
-        o.y = (uint32_t)f32_to_bf16_bits(acc.z) | ((uint32_t)f32_to_bf16_bits(acc.w) << 16);
-        reinterpret_cast<uint2*>(out + (int64_t)t * d)[c] = o;
+    __shared__ int64_t s_row[64];
+    __shared__ float s_w[64];
+    for (int p = threadIdx.x; p < P; p += kCombineThreads) {
+        s_row[p] = p < k ? inv[(int64_t)t * k + p] : inv[NR + (int64_t)(p - k) * T + t];
+        s_w[p] = p < k ? w[(int64_t)t * k + p] : 1.f;
     }
+    __syncthreads();
+    if (c >= (d >> 2)) return;
+    const float4* y4 = reinterpret_cast<const float4*>(y);
+    const int64_t dq = d >> 2;
+    const int64_t split_q = ystride * dq;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = 0; p0 < P; p0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p0 + i < P) v[i] = __ldg(y4 + s_row[p0 + i] * dq + c);
+        }
+        for (int sp = 1; sp < splits; ++sp) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (p0 + i < P) {
+                    const float4 u = __ldg(y4 + sp * split_q + s_row[p0 + i] * dq + c);
+                    v[i].x += u.x; v[i].y += u.y; v[i].z += u.z; v[i].w += u.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (p0 + i < P) {
+                const float wp = s_w[p0 + i];
+                acc.x = fmaf(wp, v[i].x, acc.x);
+                acc.y = fmaf(wp, v[i].y, acc.y);
+                acc.z = fmaf(wp, v[i].z, acc.z);
+                acc.w = fmaf(wp, v[i].w, acc.w);
+            }
+        }
+    }
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(acc.x) | ((uint32_t)f32_to_bf16_bits(acc.y) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(acc.z) | ((uint32_t)f32_to_bf16_bits(acc.w) << 16);
+    reinterpret_cast<uint2*>(out + (int64_t)t * d)[c] = o;
 }
 
 cudaError_t launch_combine(const float* y, int splits, int64_t ystride, const float* w,
                            const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 256, 0, s>>>(y, splits, ystride, w, inv, T, d, k, S, out);
+    const dim3 grid((unsigned)((d / 4 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
+    combine_kernel<<<grid, kCombineThreads, 0, s>>>(y, splits, ystride, w, inv, T, d, k, S, out);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,345 @@
+// Paged expert GEMMs for small token counts on the tensor cores, with the operands swapped:
+// the MMA's M side (128 lanes) holds expert weight rows and its N side holds the few tokens of
+// a sorted block (BN = 16..128).  At decode sizes the layer is bound by streaming each active
+// expert's pages once, so this kernel is a TMA streaming engine: a deep ring of weight tiles per
+// SM keeps enough bytes in flight to saturate HBM, and the tensor cores do the dot products at no
+// cost to the stream.
+//
+// The page rule is the one of Rimuru's paged kernel (paper-daily.com/en, "Expert weights are
+// scattered across pages. How does the kernel read them?"): addr_e(n, t) = B_P + p_e(n)*f*d +
+// (n mod f)*d + t.  A tile of expert e reads rows p_e*f + n0 .. +127 of the pool's (or a load
+// buffer's) [pages*f, d] view -- one table lookup per tile, fixed strides after it.  The gate (W1)
+// and up (W3) rows of the same output columns come from their two pages into two operand tiles
+// that feed two accumulators, so silu(gate)*up pairs up in each epilogue thread's registers.
+//
+//   gate/up:  D_g[n][j] = sum_c W1_e[n0+n][c] x_j[c],  D_u likewise with W3 (x_j: the block's
+//             gathered token rows);
+//             h[row_j][n0+n] = bf16(silu(D_g) * D_u)
+//   down:     D[r][j] = sum_{c in K split} W2_e[r0+r][c] h[row_j][c]  ->  y[split][row_j][r0+r]
+//
+// Warp roles as in the large-batch kernel: warp 0 TMA producer, warp 1 MMA issuer (and TMEM
+// owner), warps 2-5 epilogue; two TMEM accumulator sets so the epilogue of one tile overlaps the
+// next tile's loads and MMAs.  All mbarrier waits are bounded.
+#include <math.h>
+
+#include "tc_common.cuh"
+
+namespace pmoe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 64;
+constexpr int WROWS = 128;                  // weight rows per tile (MMA M)
+constexpr int W_BYTES = WROWS * BK * 2;     // 16 KB per weight operand per stage
+constexpr int kThreads = 192;
+constexpr int kRingBytes = 204 * 1024;
+
+enum { kGateUp = 1, kDown = 2 };
+
+template <int kMode, int BN>
+struct Cfg {
+    static constexpr int ACT_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = (kMode == kGateUp ? 2 : 1) * W_BYTES + ACT_BYTES;
+    static constexpr int STAGES_RAW = kRingBytes / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr int ACC_COLS = (kMode == kGateUp ? 2 : 1) * BN;   // one accumulator set
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr uint32_t IDESC = idesc_bf16(WROWS, BN);
+};
+
+struct SwapArgs {
+    const int32_t* sorted_ids;   // gate/up: token rows of each block are loaded straight from hidden
+    int T, k, S;
+    const int32_t* block_expert;
+    const int32_t* meta;
+    const ExpertLoc* loc;
+    void* out;            // h (bf16, row stride f) or y (fp32, row stride d, split stride ystride)
+    int f, d;
+    int k_blocks;         // K / 64 over the whole reduction
+    int w_tiles;          // weight-row tiles per block
+    int splits;           // K splits (down projection only)
+    int64_t ystride;      // rows per split of y
+    int32_t* err;
+};
+
+struct SwapMaps {
+    CUtensorMap act;      // X_sorted [rows][d] or h [rows][f], boxes of BN rows
+    CUtensorMap w[3];     // weights of pool / load buffer 0 / load buffer 1, boxes of 128 rows
+};
+
+template <bool kContig>
+__device__ __forceinline__ ExpertLoc loc_of(const ExpertLoc* loc, int e, int j) {
+    if (kContig) return ExpertLoc{0, 3 * e + j};
+    return loc[e * 3 + j];
+}
+
+template <int kMode, int BN, bool kContig>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_swap_kernel(const __grid_constant__ SwapMaps maps, const SwapArgs args) {
+    using C = Cfg<kMode, BN>;
+    constexpr int STAGES = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    uint32_t* tmem_holder =
+        reinterpret_cast<uint32_t*>(sgen + STAGES * C::STAGE_BYTES + 8 * (2 * STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int nblocks = args.meta[kMetaNPadded] / BN;
+    const int per_block = args.w_tiles * args.splits;
+    const int64_t ntiles = (int64_t)nblocks * per_block;
+    const int kb_per_split = (args.k_blocks + args.splits - 1) / args.splits;
+
+    // tile t -> (block b, weight-row tile wt, split sp, k-block range)
+    auto decode_tile = [&](int64_t t, int& b, int& wt, int& sp, int& kb0, int& kb1) {
+        b = (int)(t / per_block);
+        const int r = (int)(t % per_block);
+        wt = r / args.splits;
+        sp = r % args.splits;
+        kb0 = sp * kb_per_split;
+        kb1 = min(args.k_blocks, kb0 + kb_per_split);
+    };
+    auto tile_valid = [&](int b, ExpertLoc& l0, ExpertLoc& l1) {
+        const int e = args.block_expert[b];
+        if (kMode == kGateUp) {
+            l0 = loc_of<kContig>(args.loc, e, 0);
+            l1 = loc_of<kContig>(args.loc, e, 1);
+            return l0.map >= 0 && l1.map >= 0;
+        }
+        l0 = loc_of<kContig>(args.loc, e, 2);
+        l1 = l0;
+        return l0.map >= 0;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int pend_phase[STAGES];
+            for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int b, wt, sp, kb0, kb1;
+                decode_tile(t, b, wt, sp, kb0, kb1);
+                ExpertLoc l0, l1;
+                if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
+                const int rows_per_page = kMode == kGateUp ? args.f : args.d;
+                const int row0 = l0.page * rows_per_page + wt * WROWS;
+                const int row1 = l1.page * rows_per_page + wt * WROWS;
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+                    tma_load_2d(sa, &maps.w[l0.map], fb, kb * BK, row0);
+                    if (kMode == kGateUp) tma_load_2d(sa + W_BYTES, &maps.w[l1.map], fb, kb * BK, row1);
+                    tma_load_2d(sa + (kMode == kGateUp ? 2 : 1) * W_BYTES, &maps.act, fb, kb * BK, b * BN);
+                    pend_phase[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int s = 0; s < STAGES; ++s)
+                    if (pend_phase[s] >= 0) mbar_wait(full_bar(s), (uint32_t)pend_phase[s], &never, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int b, wt, sp, kb0, kb1;
+                decode_tile(t, b, wt, sp, kb0, kb1);
+                ExpertLoc l0, l1;
+                if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + (uint32_t)(acc * C::ACC_COLS);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+                    const uint64_t w0 = smem_desc(sa);
+                    const uint64_t w1 = smem_desc(sa + W_BYTES);
+                    const uint64_t xa = smem_desc(sa + (kMode == kGateUp ? 2 : 1) * W_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                        mma_bf16(d0, w0 + (uint64_t)(2 * k), xa + (uint64_t)(2 * k), C::IDESC, accum);
+                        if (kMode == kGateUp)
+                            mma_bf16(d0 + BN, w1 + (uint64_t)(2 * k), xa + (uint64_t)(2 * k), C::IDESC, accum);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+        }
+    } else {
+        const int quad = warp & 3;
+        const int wrow = quad * 32 + lane;          // weight row within the tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            int b, wt, sp, kb0, kb1;
+            decode_tile(t, b, wt, sp, kb0, kb1);
+            ExpertLoc l0, l1;
+            if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * C::ACC_COLS) + ((uint32_t)(quad * 32) << 16);
+            const int64_t row_base = (int64_t)b * BN;
+            if (kMode == kGateUp) {
+                uint16_t* h = static_cast<uint16_t*>(args.out) + wt * WROWS + wrow;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(taddr + c0, g);
+                    tmem_ld16(taddr + BN + c0, u);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a = g[j] / (1.f + expf(-g[j])) * u[j];
+                        h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(a);
+                    }
+                }
+            } else {
+                const int r = wt * WROWS + wrow;
+                float* y = static_cast<float*>(args.out) + (int64_t)sp * args.ystride * args.d + r;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_wait_ld();
+                    if (r < args.d) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) y[(row_base + c0 + j) * args.d] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int kMode, int BN, bool kContig>
+cudaError_t launch_swap_one(const SwapMaps& maps, const SwapArgs& a, int grid, cudaStream_t s) {
+    using C = Cfg<kMode, BN>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_swap_kernel<kMode, BN, kContig>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    tc_swap_kernel<kMode, BN, kContig><<<grid, kThreads, C::SMEM, s>>>(maps, a);
+    return cudaGetLastError();
+}
+
+template <int kMode, bool kContig>
+cudaError_t launch_swap_bn(int bn, const SwapMaps& maps, const SwapArgs& a, int grid, cudaStream_t s) {
+    switch (bn) {
+        case 16: return launch_swap_one<kMode, 16, kContig>(maps, a, grid, s);
+        case 32: return launch_swap_one<kMode, 32, kContig>(maps, a, grid, s);
+        case 64: return launch_swap_one<kMode, 64, kContig>(maps, a, grid, s);
+        case 128: return launch_swap_one<kMode, 128, kContig>(maps, a, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act,
+                           const CUtensorMap* wmaps, const int32_t* sorted_ids, int T, int k,
+                           int S, const int32_t* block_expert, const int32_t* meta,
+                           const ExpertLoc* loc, void* out, int f, int d, int splits,
+                           int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
+                           cudaStream_t s) {
+    SwapMaps maps;
+    maps.act = act;
+    for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    SwapArgs a{};
+    a.sorted_ids = sorted_ids;
+    a.T = T;
+    a.k = k;
+    a.S = S;
+    a.block_expert = block_expert;
+    a.meta = meta;
+    a.loc = loc;
+    a.out = out;
+    a.f = f;
+    a.d = d;
+    a.err = err;
+    a.ystride = ystride;
+    if (mode == kGateUp) {
+        a.k_blocks = d / BK;
+        a.w_tiles = f / WROWS;
+        a.splits = 1;
+    } else {
+        a.k_blocks = f / BK;
+        a.w_tiles = (d + WROWS - 1) / WROWS;
+        a.splits = splits;
+    }
+    const int64_t tiles = nblk_max * a.w_tiles * a.splits;
+    const int grid = (int)(tiles < num_sms ? (tiles > 0 ? tiles : 1) : num_sms);
+    if (mode == kGateUp)
+        return contig ? launch_swap_bn<kGateUp, true>(bn, maps, a, grid, s)
+                      : launch_swap_bn<kGateUp, false>(bn, maps, a, grid, s);
+    return contig ? launch_swap_bn<kDown, true>(bn, maps, a, grid, s)
+                  : launch_swap_bn<kDown, false>(bn, maps, a, grid, s);
+}
+
+}  // namespace pmoe

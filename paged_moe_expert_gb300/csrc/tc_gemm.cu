@@ -19,11 +19,13 @@
 // raises the device error word and the CTA unwinds after its own copies have landed.
 #include <math.h>
 
-#include "pmoe_internal.cuh"
+#include "tc_common.cuh"
 
 namespace pmoe {
 
 namespace {
+
+using namespace tc;
 
 constexpr int BM = kTcBlockM;          // 128 rows of sorted (token, expert) pairs
 constexpr int BK = 64;                 // 64 bf16 = one 128-byte swizzle row
@@ -37,10 +39,7 @@ constexpr int kThreads = 192;          // 6 warps
 constexpr uint32_t kTmemCols = 512;    // two 256-column fp32 accumulators
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
-// Instruction descriptor of tcgen05.mma.kind::f16: D fp32, A and B bf16, both K-major,
-// N = 256 (bits 17..22 hold N >> 3), M = 128 (bits 24..28 hold M >> 4).
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 enum { kGateUp = 1, kDown = 2 };
 
@@ -59,124 +58,6 @@ struct TcMaps {
     CUtensorMap a;      // activations: X_sorted [cap][d] or h [cap][f]
     CUtensorMap w[3];   // weights of pool / load buffer 0 / load buffer 1
 };
-
-// ---- PTX wrappers ----------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: gives up after ~2 s (or when another role already gave up), raising the error.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* err) {
-    if (mbar_try(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > 2000000000ull) {
-                *abort_flag = 1;
-                raise_error(err, PMOE_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes in
-// 8-row (1024-byte) groups.  Start address and strides are in 16-byte units; bits 46..47 hold
-// the descriptor version (1), bits 61..63 the swizzle mode (2 = 128-byte).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address
-    d |= (uint64_t)1 << 16;                            // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                            // version
-    d |= (uint64_t)2 << 61;                            // SWIZZLE_128B
-    return d;
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
-        " [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    return (uint32_t)f32_to_bf16_bits(a) | ((uint32_t)f32_to_bf16_bits(b) << 16);
-}
 
 template <bool kContig>
 __device__ __forceinline__ ExpertLoc tile_loc(const ExpertLoc* loc, int e, int j) {
@@ -310,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < BK / 16; ++k) {
                         // advance 16 elements (32 bytes) along K inside the swizzled row
                         mma_bf16(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
-                                 (kb | k) != 0 ? 1u : 0u);
+                                 kIdesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -386,28 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Row gather for the gate/up GEMM: X_sorted[r] = hidden[token of pair sorted_ids[r]], zero rows
-// for pads; one warp per row.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden,
-                                                          const int32_t* __restrict__ sorted_ids,
-                                                          const int32_t* __restrict__ meta, int T,
-                                                          int k, int S, int d,
-                                                          uint16_t* __restrict__ x) {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (row >= meta[kMetaNPadded]) return;
-    const int NR = T * k, NP = T * (k + S);
-    const int pair = sorted_ids[row];
-    uint4* dst = reinterpret_cast<uint4*>(x + (int64_t)row * d);
-    const int dv = d >> 3;
-    if (pair < NP) {
-        const int t = pair < NR ? pair / k : (pair - NR) % T;
-        const uint4* src = reinterpret_cast<const uint4*>(hidden + (int64_t)t * d);
-        for (int c = lane; c < dv; c += 32) dst[c] = src[c];
-    } else {
-        for (int c = lane; c < dv; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-}
-
 // ---- host side -------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -443,24 +302,18 @@ cudaError_t launch_one(const TcMaps& maps, const TcArgs& a, int grid, cudaStream
 
 }  // namespace
 
-// A bf16 row-major matrix [rows][cols] as a TMA map with 64 x 128 boxes and 128-byte swizzle.
-bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+// A bf16 row-major matrix [rows][cols] as a TMA map with boxes of 64 columns x box_rows rows and
+// 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
     EncodeTiledFn fn = encoder();
     if (!fn || !base || rows <= 0 || cols <= 0 || (cols * 2) % 16 != 0) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, 128};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-cudaError_t launch_gather(const uint16_t* hidden, const int32_t* sorted_ids, const int32_t* meta,
-                          int T, int k, int S, int d, int64_t cap, uint16_t* x, cudaStream_t s) {
-    const unsigned grid = (unsigned)((cap + 7) / 8);
-    gather_rows_kernel<<<grid, 256, 0, s>>>(hidden, sorted_ids, meta, T, k, S, d, x);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,

@@ -25,15 +25,19 @@ def weights(name):
     return _W[name]
 
 
-CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 128), ("qwen15", 4096),
-         ("mixtral", 1), ("mixtral", 32), ("mixtral", 2048),
-         ("qwen3next", 1), ("qwen3next", 64), ("qwen3next", 4096)]
+CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 128), ("qwen15", 1024), ("qwen15", 4096),
+         ("mixtral", 1), ("mixtral", 32), ("mixtral", 512), ("mixtral", 2048),
+         ("qwen3next", 1), ("qwen3next", 64), ("qwen3next", 256), ("qwen3next", 4096)]
 
 
 @pytest.mark.parametrize("name,T", CASES)
-def test_full_size_sampled(name, T):
+@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM], ids=["auto", "stream"])
+def test_full_size_sampled(name, T, path):
+    if path == pm.PATH_STREAM and T > 16:
+        pytest.skip("the weight-streaming kernels serve decode sizes")
     cfg = syn.CONFIGS[name]
     L = setup_layer(cfg, T, weights=weights(name))
+    L.plan.set_path(path)
     out = out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot))
     assert L.plan.device_error() == 0
     # routing and sort + pad, whole, bit-exact (block size of the path that ran)
@@ -42,7 +46,8 @@ def test_full_size_sampled(name, T):
     rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
     assert np.array_equal(ids.cpu().numpy(), rids)
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=3e-5, atol=1e-7)
-    bm = 128 if path == pm.PATH_TC else min(16, 1 << max(0, (T - 1).bit_length()))
+    p2 = 1 << max(0, (T - 1).bit_length())            # next power of two >= T
+    bm = {pm.PATH_TC: 128, pm.PATH_TC_DECODE: min(128, max(16, p2)), pm.PATH_STREAM: min(16, p2)}[path]
     s, b, inv, npad = pm.align(ids, cfg.E, cfg.S, bm)
     ref_al = oracle.align(rids, cfg.E, cfg.S, bm)
     n = int(npad.item())

@@ -67,12 +67,13 @@ SMALL = [
 ]
 
 
-PATHS = [pm.PATH_STREAM, pm.PATH_TC]
+PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE]
+PATH_IDS = ["stream", "tc", "tc_decode"]
 
 
-@pytest.mark.parametrize("path", PATHS, ids=["stream", "tc"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-@pytest.mark.parametrize("T", [1, 3, 16, 37, 300])
+@pytest.mark.parametrize("T", [1, 3, 16, 37, 128, 300])
 def test_forward_matches_oracle(cfg, T, path):
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
@@ -84,7 +85,7 @@ def test_forward_matches_oracle(cfg, T, path):
     assert_close(out_bits(out), ref["out_bf16"], "%s T=%d" % (cfg.name, T))
 
 
-@pytest.mark.parametrize("path", PATHS, ids=["stream", "tc"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_output_independent_of_placement(path):
     cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
                             num_pages=60)
@@ -136,7 +137,8 @@ def test_invalid_arguments_rejected():
 
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
-    for T, want in [(1, pm.PATH_STREAM), (16, pm.PATH_STREAM), (17, pm.PATH_TC), (512, pm.PATH_TC)]:
+    for T, want in [(1, pm.PATH_TC_DECODE), (16, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
+                    (129, pm.PATH_TC), (512, pm.PATH_TC)]:
         L = setup_layer(cfg, T)
         L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
         assert L.plan.last_run()[0] == want
@@ -153,3 +155,30 @@ def test_paths_agree(T):
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
     for o in outs:
         assert_close(o, ref["out_bf16"])
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_replays_from_a_cuda_graph(path):
+    cfg = syn.custom_config("graph", d=256, f=256, E=6, k=2, S=1, n_buffered=2)
+    L = setup_layer(cfg, 40)
+    L.plan.set_path(path)
+    ws = pm.alloc_workspace(L.desc, 40)
+    out = torch.empty_like(L.hidden)
+    run = lambda: L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, out=out, workspace=ws)  # noqa: E731
+    run()
+    torch.cuda.synchronize()
+    eager = out_bits(out)
+    out.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_bits(out), eager)
