@@ -197,12 +197,14 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
                  : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
+    // the single-CTA prep also copies the rows when they are few (at most 64 KB)
+    const bool gather_in_prep = T <= kPrepSmallMaxTokens && tc_family && W.np * D.d * 2 <= 64 * 1024;
     if (T <= kPrepSmallMaxTokens) {
         // one CTA: routing, sort + pad + page resolution
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_prep_small(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w,
                                     D.num_shared_chunks, bm, sorted, bexp, inv, meta, rs, hid, D.d,
-                                    nullptr, stream), "prep");
+                                    gather_in_prep ? x : nullptr, stream), "prep");
     } else {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_route(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w, stream), "route");
@@ -210,7 +212,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
                                inv, meta, &rs, stream), "align");
     }
-    if (tc_family) {
+    if (tc_family && !gather_in_prep) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_gather_pairs(hid, inv, T, D.top_k, D.num_shared_chunks, D.d, x, stream),
                   "gather");

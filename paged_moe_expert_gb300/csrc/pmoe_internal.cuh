@@ -77,6 +77,34 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return r;
 }
 
+// Programmatic dependent launch: every kernel of the library lets the next kernel in the stream
+// start its prologue early (launch_dependents) and waits for the previous grid to finish and
+// publish its memory (wait) before it reads or writes any global memory.  A kernel launched
+// without the attribute returns from the wait at once.
+__device__ __forceinline__ void pdl_allow_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prev() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch with the programmatic-stream-serialisation attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Host-side launchers (defined in the .cu files) -------------------------------------------
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* ids,

@@ -84,6 +84,8 @@ template <int EPL>
 __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,
                                                     int k, int renorm, int32_t* __restrict__ ids,
                                                     float* __restrict__ wout) {
+    pdl_allow_next();
+    pdl_wait_prev();
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
@@ -95,13 +97,12 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          float* w, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)((T + 3) / 4)), block(128);
-    if (E <= 32) route_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 64) route_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 128) route_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 256) route_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else if (E <= 512) route_kernel<16><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    else route_kernel<32><<<grid, block, 0, s>>>(logits, T, E, k, renorm, ids, w);
-    return cudaGetLastError();
+    if (E <= 32) return launch_pdl(route_kernel<1>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
+    else if (E <= 64) return launch_pdl(route_kernel<2>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
+    else if (E <= 128) return launch_pdl(route_kernel<4>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
+    else if (E <= 256) return launch_pdl(route_kernel<8>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
+    else if (E <= 512) return launch_pdl(route_kernel<16>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
+    else return launch_pdl(route_kernel<32>, grid, block, 0, s, logits, T, E, k, renorm, ids, w);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -238,6 +239,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
     extern __shared__ int32_t smem[];
+    pdl_allow_next();
+    pdl_wait_prev();
     align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, do_resolve, smem);
 }
 
@@ -258,14 +261,21 @@ __global__ void __launch_bounds__(256) gather_pairs_kernel(const uint16_t* __res
                                                            const int32_t* __restrict__ inv, int T,
                                                            int k, int S, int d,
                                                            uint16_t* __restrict__ x) {
+    pdl_allow_next();
+    pdl_wait_prev();
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (i >= T * (k + S)) return;
     gather_pair(hidden, inv, i, T, k, d, threadIdx.x & 31, x);
 }
 
 // Small batches: routing and sort + pad (with page resolution) in one CTA, so a decode step spends
-// one launch on them instead of two; the optional row gather is for callers without a separate
-// multi-CTA gather.
+// one launch on them instead of two.  The page-table loads are issued before the routing so the
+// two latencies overlap; the routing ids and the tables then stay in shared memory for the sort.
+// When the gathered rows are small, the row gather runs here too (x != NULL).
+constexpr int kPrepTabPerThread = 8;   // (E + 3*(E+S)) / threads for E + S <= 1024
+
+__host__ __device__ constexpr int align_words(int ES) { return kAlignWarps * ES + 2 * ES + 1; }
+
 template <int EPL>
 __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int renorm, int32_t* __restrict__ ids,
@@ -273,54 +283,82 @@ __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
     int32_t* __restrict__ block_expert, int32_t* __restrict__ inv, int32_t* __restrict__ meta,
     ResolveArgs rs, const uint16_t* __restrict__ hidden, int d, uint16_t* __restrict__ x) {
     extern __shared__ int32_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ES = E + S;
+    int32_t* s_align = smem;
+    int32_t* s_ids = s_align + align_words(ES);   // [T*k]
+    int32_t* s_bs = s_ids + T * k;                // [E]
+    int32_t* s_pt = s_bs + E;                     // [ES*3]
+    pdl_allow_next();
+    pdl_wait_prev();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NT = kAlignWarps * 32;
+    const int ntab = rs.contiguous ? 0 : E + 3 * ES;
+    int32_t tv[kPrepTabPerThread];
+#pragma unroll
+    for (int i = 0; i < kPrepTabPerThread; ++i) {
+        const int idx = tid + i * NT;
+        tv[i] = idx < ntab ? (idx < E ? rs.buf_slot[idx] : rs.page_table[idx - E]) : 0;
+    }
     for (int t = warp; t < T; t += kAlignWarps)
-        route_token<EPL>(logits + (int64_t)t * E, E, k, renorm, lane, ids + (int64_t)t * k,
+        route_token<EPL>(logits + (int64_t)t * E, E, k, renorm, lane, s_ids + t * k,
                          wout + (int64_t)t * k);
+#pragma unroll
+    for (int i = 0; i < kPrepTabPerThread; ++i) {
+        const int idx = tid + i * NT;
+        if (idx < ntab) {
+            if (idx < E) s_bs[idx] = tv[i];
+            else s_pt[idx - E] = tv[i];
+        }
+    }
     __syncthreads();
-    align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, 1, smem);
-    __syncthreads();
+    for (int i = tid; i < T * k; i += NT) ids[i] = s_ids[i];
+    ResolveArgs local = rs;
+    if (!rs.contiguous) {
+        local.buf_slot = s_bs;
+        local.page_table = s_pt;
+    }
+    align_block(s_ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, local, 1, s_align);
     if (x) {
+        __syncthreads();
         const int NP = T * (k + S);
         for (int i = warp; i < NP; i += kAlignWarps) gather_pair(hidden, inv, i, T, k, d, lane, x);
     }
 }
 
+static size_t align_smem_bytes(int ES) { return sizeof(int32_t) * (size_t)align_words(ES); }
+
+static size_t prep_smem_bytes(int T, int E, int k, int S) {
+    return sizeof(int32_t) * ((size_t)align_words(E + S) + (size_t)T * k + E + 3 * (size_t)(E + S));
+}
+
+static cudaError_t allow_align_smem(const void* fn) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)prep_smem_bytes(128, kMaxExpertsTotal, kMaxTopK, 0));
+}
+
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
                          int32_t* meta, const ResolveArgs* resolve, cudaStream_t s) {
-    const int ES = E + S;
-    const size_t smem = sizeof(int32_t) * ((size_t)kAlignWarps * ES + ES + ES + 1);
     static bool attr_set = false;  // idempotent; racing first calls set the same value
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(int32_t) * ((size_t)kAlignWarps * kMaxExpertsTotal +
-                                                                      2 * kMaxExpertsTotal + 1)));
+                                             (int)align_smem_bytes(kMaxExpertsTotal));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     ResolveArgs rs{};
     if (resolve) rs = *resolve;
-    align_kernel<<<1, kAlignWarps * 32, smem, s>>>(ids, T, k, E, S, block_m, sorted_ids,
-                                                   block_expert, inv, meta, rs, resolve ? 1 : 0);
-    return cudaGetLastError();
-}
-
-static size_t align_smem_bytes(int ES) {
-    return sizeof(int32_t) * ((size_t)kAlignWarps * ES + ES + ES + 1);
-}
-
-static cudaError_t allow_align_smem(const void* fn) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)align_smem_bytes(kMaxExpertsTotal));
+    return launch_pdl(align_kernel, dim3(1), dim3(kAlignWarps * 32), align_smem_bytes(E + S), s,
+                      ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs,
+                      resolve ? 1 : 0);
 }
 
 cudaError_t launch_gather_pairs(const uint16_t* hidden, const int32_t* inv, int T, int k, int S,
                                 int d, uint16_t* x, cudaStream_t s) {
     const int64_t np = (int64_t)T * (k + S);
     if (np == 0) return cudaSuccess;
-    gather_pairs_kernel<<<(unsigned)((np + 7) / 8), 256, 0, s>>>(hidden, inv, T, k, S, d, x);
-    return cudaGetLastError();
+    return launch_pdl(gather_pairs_kernel, dim3((unsigned)((np + 7) / 8)), dim3(256), 0, s, hidden,
+                      inv, T, k, S, d, x);
 }
 
 template <int EPL>
@@ -335,10 +373,9 @@ static cudaError_t prep_small_epl(const float* logits, int T, int E, int k, int 
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    prep_small_kernel<EPL><<<1, kAlignWarps * 32, align_smem_bytes(E + S), s>>>(
-        logits, T, E, k, renorm, ids, w, S, block_m, sorted_ids, block_expert, inv, meta, rs,
-        hidden, d, x);
-    return cudaGetLastError();
+    return launch_pdl(prep_small_kernel<EPL>, dim3(1), dim3(kAlignWarps * 32),
+                      prep_smem_bytes(T, E, k, S), s, logits, T, E, k, renorm, ids, w, S, block_m,
+                      sorted_ids, block_expert, inv, meta, rs, hidden, d, x);
 }
 
 cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int renorm, int32_t* ids,

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kThreads) stream_gemm1_kernel(
     const int32_t* __restrict__ block_expert, const int32_t* __restrict__ meta,
     const ExpertLoc* __restrict__ loc, uint16_t* __restrict__ h) {
     extern __shared__ uint4 xs[];  // [MT][d/8]
+    pdl_allow_next();
+    pdl_wait_prev();
     const int b = blockIdx.y;
     if (b * MT >= meta[kMetaNPadded]) return;
     const int d = L.d, f = L.f, dv = d >> 3;
@@ -149,6 +151,8 @@ __global__ void __launch_bounds__(kThreads) stream_gemm2_kernel(
     const int32_t* __restrict__ meta, const ExpertLoc* __restrict__ loc,
     const uint16_t* __restrict__ h, float* __restrict__ y, int64_t ystride) {
     extern __shared__ uint4 hs[];  // [MT][kc/8]
+    pdl_allow_next();
+    pdl_wait_prev();
     const int b = blockIdx.y;
     if (b * MT >= meta[kMetaNPadded]) return;
     const int d = L.d, f = L.f;
@@ -222,8 +226,8 @@ cudaError_t gemm1_mt(const LayerPtrs& L, const uint16_t* hidden, const int32_t* 
     }
     const dim3 grid((unsigned)(L.f / kRows1), (unsigned)nblk_max);
     const size_t smem = (size_t)MT * L.d * 2;
-    stream_gemm1_kernel<MT, C><<<grid, kThreads, smem, s>>>(L, hidden, sorted_ids, block_expert, meta, loc, h);
-    return cudaGetLastError();
+    return launch_pdl(stream_gemm1_kernel<MT, C>, grid, dim3(kThreads), smem, s, L, hidden, sorted_ids,
+                      block_expert, meta, loc, h);
 }
 
 template <int MT, bool C>
@@ -238,8 +242,8 @@ cudaError_t gemm2_mt(const LayerPtrs& L, const int32_t* sorted_ids, const int32_
     }
     const dim3 grid((unsigned)(L.d / kRows2), (unsigned)nblk_max, (unsigned)splits);
     const size_t smem = (size_t)MT * (L.f < kStreamKChunk ? L.f : kStreamKChunk) * 2;
-    stream_gemm2_kernel<MT, C><<<grid, kThreads, smem, s>>>(L, sorted_ids, block_expert, meta, loc, h, y, ystride);
-    return cudaGetLastError();
+    return launch_pdl(stream_gemm2_kernel<MT, C>, grid, dim3(kThreads), smem, s, L, sorted_ids,
+                      block_expert, meta, loc, h, y, ystride);
 }
 
 // contiguous addressing is selected by loc == nullptr
@@ -291,6 +295,8 @@ constexpr int kCombineThreads = 64;
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float* __restrict__ y, int splits, int64_t ystride, const float* __restrict__ w,
     const int32_t* __restrict__ inv, int T, int d, int k, int S, uint16_t* __restrict__ out) {
+    pdl_allow_next();
+    pdl_wait_prev();
     const int t = blockIdx.y;
     const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // float4 column
     const int P = k + S;
@@ -345,8 +351,8 @@ cudaError_t launch_combine(const float* y, int splits, int64_t ystride, const fl
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)((d / 4 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
-    combine_kernel<<<grid, kCombineThreads, 0, s>>>(y, splits, ystride, w, inv, T, d, k, S, out);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, splits, ystride, w, inv,
+                      T, d, k, S, out);
 }
 
 }  // namespace pmoe

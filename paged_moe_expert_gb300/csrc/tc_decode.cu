@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // the prologue above touches no global memory; from here on the previous kernel's results
+    // are needed
+    pdl_allow_next();
+    pdl_wait_prev();
 
     const int nblocks = args.meta[kMetaNPadded] / BN;
     const int per_block = args.w_tiles * args.splits;
@@ -285,8 +289,7 @@ cudaError_t launch_swap_one(const SwapMaps& maps, const SwapArgs& a, int grid, c
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc_swap_kernel<kMode, BN, kContig><<<grid, kThreads, C::SMEM, s>>>(maps, a);
-    return cudaGetLastError();
+    return launch_pdl(tc_swap_kernel<kMode, BN, kContig>, dim3(grid), dim3(kThreads), C::SMEM, s, maps, a);
 }
 
 template <int kMode, bool kContig>

@@ -121,6 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // the prologue above touches no global memory; from here on the previous kernel's results
+    // are needed
+    pdl_allow_next();
+    pdl_wait_prev();
 
     const int nblocks = args.meta[kMetaNPadded] / BM;
     const int64_t ntiles = (int64_t)nblocks * args.n_tiles;
@@ -296,8 +300,7 @@ cudaError_t launch_one(const TcMaps& maps, const TcArgs& a, int grid, cudaStream
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    tc_gemm_kernel<kMode, kContig><<<grid, kThreads, kSmemBytes, s>>>(maps, a);
-    return cudaGetLastError();
+    return launch_pdl(tc_gemm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), kSmemBytes, s, maps, a);
 }
 
 }  // namespace
