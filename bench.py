@@ -288,6 +288,78 @@ def time_iters(fn_list, iters, flush):
     return [statistics.median(t) for t in times]
 
 
+def decode_sweep(args):
+    """24 consecutive Qwen1.5-MoE-shaped layers per step, batch 1..256 tokens, resident fraction
+    100% -> 50%: offloaded experts stream from pinned host memory into the two alternating load
+    buffers one layer ahead of compute; the pool layout cycles over 4 pre-placed layouts per step.
+    One JSON line per (resident fraction, tokens)."""
+    from paged_moe_expert_gb300 import pipeline
+    import paged_moe_expert_gb300 as pm
+    torch.cuda.set_device(0)
+    cfg = syn.CONFIGS["qwen15"]
+    w = syn.make_weights(cfg)
+    L = args.layers
+    tokens_list = [int(x) for x in args.tokens_list.split(",")]
+    fractions = [float(x) for x in args.fractions.split(",")]
+    # host -> device copy bandwidth (pinned), for the copy-time estimate
+    hbuf = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dbuf.copy_(hbuf, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        dbuf.copy_(hbuf, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    h2d_gbs = 3 * (1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9
+    del hbuf, dbuf
+    resident_ms = {}
+    for frac in fractions:
+        n_off = int(round((1.0 - frac) * cfg.E))
+        stack = pipeline.DecodeStack(cfg, w, L, n_off, layouts=4, seed=11)
+        for T in tokens_list:
+            rng = np.random.default_rng(1000 + T)
+            steps = args.warmup + args.steps
+            logits = [[syn.bf16_bits_to_f32(syn.to_bf16_bits(
+                rng.standard_normal((T, cfg.E)).astype(np.float32))) for _ in range(L)]
+                for _ in range(steps)]
+            scheds = [stack.schedule(lg) for lg in logits]
+            lg_dev = [[torch.from_numpy(x).cuda() for x in lg] for lg in logits]
+            hidden = torch.from_numpy(syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(
+                np.float32)).view(np.int16)).view(torch.bfloat16).cuda()
+            ws = pm.alloc_workspace(stack.desc, T)
+            acts = [torch.empty_like(hidden) for _ in range(2)]
+            copied = sum(len(sc[0]) for sched in scheds[args.warmup:] for sc in sched) * 6 * cfg.d * cfg.f
+            for s_ in range(args.warmup):
+                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for s_ in range(args.warmup, steps):
+                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            if n_off == 0:
+                resident_ms[T] = ms
+            copy_ms = copied / args.steps / (h2d_gbs * 1e9) * 1e3
+            line = {"metric": "decode sweep: 24-layer step time with double-buffered expert prefetch",
+                    "config": {"workload": "%d Qwen1.5-MoE-shaped layers, %d tokens/step" % (L, T),
+                               "resident_fraction": frac, "offloaded_experts_per_layer": n_off,
+                               "pool_layouts_cycled": 4},
+                    "tokens": T, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+                    "copied_mb_per_step": copied / args.steps / 1e6,
+                    "h2d_gbs": h2d_gbs, "copy_ms_per_step_est": copy_ms,
+                    "all_resident_ms": resident_ms.get(T),
+                    "exposed_copy_frac": (None if T not in resident_ms or copy_ms == 0 else
+                                          max(0.0, (ms - resident_ms[T])) / copy_ms)}
+            print(json.dumps(line), flush=True)
+            del ws, acts
+        del stack
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -300,7 +372,15 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="24-layer decode sweep with prefetch (prints one line per case)")
+    ap.add_argument("--layers", type=int, default=24)
+    ap.add_argument("--tokens-list", default="1,4,16,64,256")
+    ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
     args = ap.parse_args()
+    if args.decode_sweep:
+        decode_sweep(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
