@@ -421,7 +421,7 @@ def main():
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    path, nk = lay.plan.last_run()
+    path, nk, n_launch = lay.plan.last_run()
     assert lay.plan.device_error() == 0
 
     # which kernel dominates: one untimed pass with an event before every kernel
@@ -496,7 +496,7 @@ def main():
             fc = lambda: lay.cplan.contig_forward(hs, ls, out=os_, workspace=wss)  # noqa: E731
             for _ in range(3):
                 fp(); fc()
-            ps, _ = lay.plan.last_run()
+            ps = lay.plan.last_run()[0]
             gp, gc = capture(fp), capture(fc)
             tp, tc = time_iters([gp.replay, gc.replay], args.sweep_iters, flush)
             ea = lay.e_act(ls)
@@ -566,7 +566,7 @@ def main():
         "e2e": {"value": job_throughput(wk["flops"], world, e2e_sec) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(hidden.numel() * 2 + logits.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 2)},
-        "gpu_launches": int(nk * args.steps),
+        "gpu_launches": int(n_launch * args.steps),
         "clocks": clk,
         "kernels_ms": {n: float(t) for n, t in zip(names, probe_ms)},
         "overhead_vs_contig": overhead,

@@ -79,7 +79,7 @@ typedef struct pmoe_plan* pmoe_plan_t;
 
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
-    PMOE_PATH_AUTO = 0,   /* choose by token count */
+    PMOE_PATH_AUTO = 0,   /* TC_DECODE while T*k <= 192*E (routed tokens per expert), else TC */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
     PMOE_PATH_TC_DECODE = 3 /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
@@ -102,9 +102,11 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan);
 /* Force a kernel family (tests, benchmarks); PMOE_PATH_AUTO restores the default. */
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path);
 
-/* The kernel family (pmoe_path) the plan's last forward call ran and how many kernels it
- * launched (0 and 0 before the first call). */
-pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_kernels);
+/* The kernel family (pmoe_path) the plan's last forward call ran, how many steps the measurement
+ * hook brackets (n_steps: events 0..n_steps are recorded) and how many kernels it launched
+ * (zeros before the first call). */
+pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_steps,
+                               int32_t* n_launches);
 
 /* Measurement hook: while set, each forward call records events[i] on its stream right before
  * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
@@ -201,10 +203,13 @@ pmoe_status pmoe_route(const float* router_logits, int32_t T, int32_t E, int32_t
  * ascending index within an expert; an expert with c > 0 pairs owns ceil(c/block_m) blocks,
  * pads hold T*(k+S).  Outputs (device): sorted_ids int32 [>= T*(k+S) + (E+S)*(block_m-1)],
  * block_expert int32 [>= T*(k+S)/block_m + E + S], inv int32 [T*(k+S)] (row of each pair),
- * n_padded int32 [1].  block_m in {16, 32, 64, 128}; E + S <= 1024. */
+ * n_padded int32 [1].  block_m a power of two <= 128; E + S <= 1024.  With scratch != NULL
+ * (device, >= pmoe_align_scratch_size() bytes) the sort runs over several CTAs when there are
+ * more than 2048 routed pairs (the forward's large-batch form); otherwise in one CTA. */
 pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, int32_t S,
                        int32_t block_m, int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
-                       int32_t* n_padded, pmoe_stream_t stream);
+                       int32_t* n_padded, void* scratch, pmoe_stream_t stream);
+size_t pmoe_align_scratch_size(void);
 
 #ifdef __cplusplus
 }

@@ -110,10 +110,11 @@ class Plan:
         return out
 
     def last_run(self):
-        """(path, number of kernels) of the last forward call."""
-        p, n = ctypes.c_int32(0), ctypes.c_int32(0)
-        _lib.check(_lib.load().pmoe_plan_last_run(self._h, ctypes.byref(p), ctypes.byref(n)))
-        return int(p.value), int(n.value)
+        """(path, profiled steps, kernel launches) of the last forward call."""
+        p, n, k = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        _lib.check(_lib.load().pmoe_plan_last_run(self._h, ctypes.byref(p), ctypes.byref(n),
+                                                  ctypes.byref(k)))
+        return int(p.value), int(n.value), int(k.value)
 
     def set_profile_events(self, events):
         """Record events[i] before the forward's i-th kernel (and one after the last); pass
@@ -154,7 +155,7 @@ def route(logits: torch.Tensor, top_k: int, renormalize: bool, stream=None):
     return ids, w
 
 
-def align(ids: torch.Tensor, E: int, S: int, block_m: int, stream=None):
+def align(ids: torch.Tensor, E: int, S: int, block_m: int, stream=None, multi_cta=False):
     T, k = ids.shape
     NP = T * (k + S)
     dev = ids.device
@@ -162,9 +163,12 @@ def align(ids: torch.Tensor, E: int, S: int, block_m: int, stream=None):
     block_expert = torch.empty(NP // block_m + E + S + 1, dtype=torch.int32, device=dev)
     inv = torch.empty(max(NP, 1), dtype=torch.int32, device=dev)
     npad = torch.zeros(1, dtype=torch.int32, device=dev)
+    scratch = None
+    if multi_cta:
+        scratch = torch.empty(int(_lib.load().pmoe_align_scratch_size()), dtype=torch.uint8, device=dev)
     _lib.check(_lib.load().pmoe_align(_ptr(ids), int(T), int(k), int(E), int(S), int(block_m),
                                       _ptr(sorted_ids), _ptr(block_expert), _ptr(inv), _ptr(npad),
-                                      _stream(stream)))
+                                      _ptr(scratch), _stream(stream)))
     return sorted_ids, block_expert, inv[:NP], npad
 
 

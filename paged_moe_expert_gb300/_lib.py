@@ -36,7 +36,8 @@ SIGNATURES = {
     "pmoe_plan_create": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, ctypes.POINTER(P)]),
     "pmoe_plan_destroy": (ctypes.c_int, [P]),
     "pmoe_plan_set_path": (ctypes.c_int, [P, I32]),
-    "pmoe_plan_last_run": (ctypes.c_int, [P, ctypes.POINTER(I32), ctypes.POINTER(I32)]),
+    "pmoe_plan_last_run": (ctypes.c_int, [P, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                          ctypes.POINTER(I32)]),
     "pmoe_plan_set_profile_events": (ctypes.c_int, [P, ctypes.POINTER(P), I32]),
     "pmoe_workspace_size": (SZ, [ctypes.POINTER(LayerDesc), I32]),
     "moe_paged_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, P, P, SZ, P]),
@@ -47,7 +48,8 @@ SIGNATURES = {
     "pmoe_wait_event": (ctypes.c_int, [P, I32]),
     "pmoe_get_device_error": (ctypes.c_int, [P, I32, ctypes.POINTER(I32), P]),
     "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),
-    "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P]),
+    "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P, P]),
+    "pmoe_align_scratch_size": (SZ, []),
 }
 
 _lock = threading.Lock()

@@ -57,9 +57,11 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
     return bm;
 }
 
-// Token counts up to which the automatic path picks the small-batch tensor-core kernels, and
-// up to which routing, sort + pad and the row gather run as one single-CTA kernel.
-constexpr int kSwapMaxTokens = 128;
+// The automatic path takes the small-batch tensor-core kernels (tokens on the MMA's N side) while
+// the routed experts average at most this many tokens (T*k/E), the 128-token-block kernels above
+// (measured crossover on GB300); routing and sort + pad run as one single-CTA kernel up to 128
+// tokens.
+constexpr int kSwapMaxTokensPerExpert = 192;
 constexpr int kPrepSmallMaxTokens = 128;
 
 static int stream_splits(const pmoe_layer_desc& D) {
@@ -112,6 +114,7 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.inv = o;    o = align256(o + sizeof(int32_t) * (W.np > 0 ? W.np : 1));
     W.meta = o;   o = align256(o + sizeof(int32_t) * kMetaCount);
     W.loc = o;    o = align256(o + sizeof(ExpertLoc) * ES * 3);
+    W.part = o;   o = align256(o + align_part_bytes());
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
@@ -153,7 +156,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
 
     int path = P->path;
-    if (path == PMOE_PATH_AUTO) path = T <= kSwapMaxTokens ? PMOE_PATH_TC_DECODE : PMOE_PATH_TC;
+    if (path == PMOE_PATH_AUTO)
+        path = (int64_t)T * D.top_k <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts
+                   ? PMOE_PATH_TC_DECODE : PMOE_PATH_TC;
     const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE;
     if (tc_family && !P->have_tmaps)
         return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
@@ -209,8 +214,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_route(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w, stream), "route");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_align(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm, sorted, bexp,
-                               inv, meta, &rs, stream), "align");
+        PMOE_CUDA(launch_align_multi(ids, T, D.top_k, D.num_experts, D.num_shared_chunks, bm,
+                                     at<int32_t>(ws, W.part), sorted, bexp, inv, meta, &rs, stream),
+                  "align");
     }
     if (tc_family && !gather_in_prep) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
@@ -261,6 +267,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
     P->last_kernels = ev - 1;
+    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
     return PMOE_OK;
 }
 
@@ -347,11 +354,13 @@ pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
     return PMOE_OK;
 }
 
-pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_kernels) {
+pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_steps,
+                               int32_t* n_launches) {
     Plan* P = reinterpret_cast<Plan*>(plan);
-    if (!P || !path || !n_kernels) return fail(PMOE_ERR_INVALID_ARG, "NULL argument");
+    if (!P || !path || !n_steps || !n_launches) return fail(PMOE_ERR_INVALID_ARG, "NULL argument");
     *path = P->last_path;
-    *n_kernels = P->last_kernels;
+    *n_steps = P->last_kernels;
+    *n_launches = P->last_launches;
     return PMOE_OK;
 }
 
@@ -453,9 +462,11 @@ pmoe_status pmoe_route(const float* router_logits, int32_t T, int32_t E, int32_t
     return PMOE_OK;
 }
 
+size_t pmoe_align_scratch_size(void) { return align_part_bytes(); }
+
 pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, int32_t S,
                        int32_t block_m, int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
-                       int32_t* n_padded, pmoe_stream_t stream) {
+                       int32_t* n_padded, void* scratch, pmoe_stream_t stream) {
     if (T < 0 || top_k <= 0 || E <= 0 || S < 0 || E + S > kMaxExpertsTotal)
         return fail(PMOE_ERR_INVALID_ARG, "bad align sizes");
     if (block_m < 1 || block_m > 128 || (block_m & (block_m - 1)))
@@ -463,8 +474,13 @@ pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, 
     if (!sorted_ids || !block_expert || !n_padded || (T > 0 && (!ids || !inv)))
         return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
     if ((int64_t)T * (top_k + S) > (int64_t)1 << 30) return fail(PMOE_ERR_INVALID_ARG, "too many pairs");
-    PMOE_CUDA(launch_align(ids, T, top_k, E, S, block_m, sorted_ids, block_expert, inv, n_padded,
-                           nullptr, (cudaStream_t)stream), "align");
+    if (scratch)
+        PMOE_CUDA(launch_align_multi(ids, T, top_k, E, S, block_m, static_cast<int32_t*>(scratch),
+                                     sorted_ids, block_expert, inv, n_padded, nullptr,
+                                     (cudaStream_t)stream), "align");
+    else
+        PMOE_CUDA(launch_align(ids, T, top_k, E, S, block_m, sorted_ids, block_expert, inv, n_padded,
+                               nullptr, (cudaStream_t)stream), "align");
     return PMOE_OK;
 }
 

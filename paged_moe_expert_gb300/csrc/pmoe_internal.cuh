@@ -26,7 +26,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, x, h, y, total;
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
     int64_t nblk_max;    // upper bound on sorted blocks
@@ -48,7 +48,7 @@ struct Plan {
     bool have_tmaps;
     cudaEvent_t prof_ev[16];   // measurement hook (pmoe_plan_set_profile_events)
     int n_prof;
-    int last_path, last_kernels;  // what the last forward ran
+    int last_path, last_kernels, last_launches;  // what the last forward ran
     int num_sms;
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
@@ -124,6 +124,15 @@ struct ResolveArgs {
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
                          int32_t* meta, const ResolveArgs* resolve, cudaStream_t s);
+
+// Sort + pad over several CTAs when there are many pairs (two launches; `part` is scratch of
+// align_part_bytes()); falls back to the single-CTA kernel for few pairs.
+int align_ctas(int64_t NR);
+size_t align_part_bytes();
+cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, int block_m,
+                               int32_t* part, int32_t* sorted_ids, int32_t* block_expert,
+                               int32_t* inv, int32_t* meta, const ResolveArgs* resolve,
+                               cudaStream_t s);
 
 // Small batches: routing + sort/pad/resolve + row gather (x may be NULL: no gather) in one CTA.
 cudaError_t launch_prep_small(const float* logits, int T, int E, int k, int renorm, int32_t* ids,

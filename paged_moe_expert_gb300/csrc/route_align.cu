@@ -244,6 +244,164 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
     align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, do_resolve, smem);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Sort + pad over many CTAs (large T).  The routed pairs are cut into C contiguous segments.
+//   count    CTA c histograms its segment by expert (shared-memory atomics) -> part[c][e];
+//   scatter  CTA c sums part over all CTAs (expert totals, padded exclusive offsets off[e]) and
+//            over CTAs before it (its base inside each expert), then places its segment exactly
+//            like the single-CTA pass B: per-warp counts, prefix over warps, match-mask ranks.
+//            The result is the same stable order as the single-CTA kernel.  Shared-chunk pairs,
+//            pads, the block map and the page resolution are split across the C CTAs.
+// ---------------------------------------------------------------------------------------------
+constexpr int kAlignMaxCtas = 64;
+constexpr int kAlignPairsPerCta = 2048;
+
+__global__ void __launch_bounds__(kAlignWarps * 32) align_count_kernel(
+    const int32_t* __restrict__ ids, int NR, int E, int ES, int seg, int32_t* __restrict__ part) {
+    extern __shared__ int32_t h[];
+    pdl_allow_next();
+    pdl_wait_prev();
+    const int tid = threadIdx.x, NT = kAlignWarps * 32, c = blockIdx.x;
+    for (int e = tid; e < ES; e += NT) h[e] = 0;
+    __syncthreads();
+    const int64_t s0 = (int64_t)c * seg, s1 = s0 + seg < NR ? s0 + seg : NR;
+    for (int64_t i = s0 + tid; i < s1; i += NT) {
+        int e = ids[i];
+        if (e < 0 || e >= E) e = 0;
+        atomicAdd(&h[e], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < ES; e += NT) part[(int64_t)c * ES + e] = h[e];
+}
+
+__global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m, int seg, int C,
+    const int32_t* __restrict__ part, int32_t* __restrict__ sorted_ids,
+    int32_t* __restrict__ block_expert, int32_t* __restrict__ inv, int32_t* __restrict__ meta,
+    ResolveArgs rs, int do_resolve) {
+    extern __shared__ int32_t sm[];
+    const int ES = E + S;
+    int32_t* off = sm;                 // [ES + 1]
+    int32_t* cnt = off + ES + 1;       // [ES]
+    int32_t* base = cnt + ES;          // [ES]
+    int32_t* cw = base + ES;           // [kAlignWarps][ES]
+    pdl_allow_next();
+    pdl_wait_prev();
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, NT = kAlignWarps * 32;
+    const int c = blockIdx.x;
+    const int64_t NR = (int64_t)T * k, NP = (int64_t)T * (k + S);
+    for (int e = tid; e < ES; e += NT) {
+        int tot = 0, mine = 0;
+        if (e < E) {
+            for (int cc = 0; cc < C; ++cc) {
+                const int v = part[(int64_t)cc * ES + e];
+                if (cc < c) mine += v;
+                tot += v;
+            }
+        } else {
+            tot = T;
+        }
+        cnt[e] = tot;
+        base[e] = mine;
+    }
+    for (int i = tid; i < kAlignWarps * ES; i += NT) cw[i] = 0;
+    __syncthreads();
+
+    if (w == 0) {  // padded exclusive scan over experts
+        const int per = (ES + 31) / 32;
+        const int b0 = lane * per;
+        int local = 0;
+        for (int e = b0; e < b0 + per && e < ES; ++e) local += (cnt[e] + block_m - 1) / block_m * block_m;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - local;
+        for (int e = b0; e < b0 + per && e < ES; ++e) {
+            off[e] = run;
+            run += (cnt[e] + block_m - 1) / block_m * block_m;
+        }
+        if (lane == 31) off[ES] = incl;
+    }
+    // this CTA's segment, split into per-warp sub-segments
+    const int64_t c0 = (int64_t)c * seg, c1 = c0 + seg < NR ? c0 + seg : NR;
+    const int64_t sub = (c1 - c0 + kAlignWarps - 1) / kAlignWarps;
+    const int64_t s0 = c0 + (int64_t)w * sub < c1 ? c0 + (int64_t)w * sub : c1;
+    const int64_t s1 = s0 + sub < c1 ? s0 + sub : c1;
+    for (int64_t i = s0 + lane; i < s1; i += 32) {
+        int e = ids[i];
+        if (e < 0 || e >= E) e = 0;
+        atomicAdd(&cw[w * ES + e], 1);
+    }
+    __syncthreads();
+    for (int e = tid; e < ES; e += NT) {
+        int run = off[e] + base[e];
+        for (int ww = 0; ww < kAlignWarps; ++ww) {
+            const int x = cw[ww * ES + e];
+            cw[ww * ES + e] = run;
+            run += x;
+        }
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t b = s0; b < s1; b += 32) {
+        const int64_t i = b + lane;
+        const bool valid = i < s1;
+        int e = valid ? ids[i] : -1 - lane;
+        if (valid && (e < 0 || e >= E)) e = 0;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (valid) {
+            const int pos = cw[w * ES + e] + __popc(peers & lt_mask);
+            sorted_ids[pos] = (int32_t)i;
+            inv[i] = pos;
+        }
+        __syncwarp();
+        if (valid && (__ffs(peers) - 1) == lane) cw[w * ES + e] += __popc(peers);
+        __syncwarp();
+    }
+    // shared-chunk pairs, pads, block map, resolution: split across the CTAs
+    for (int64_t idx = (int64_t)c * NT + tid; idx < (int64_t)S * T; idx += (int64_t)C * NT) {
+        const int s = (int)(idx / T), t = (int)(idx % T);
+        const int pos = off[E + s] + t;
+        sorted_ids[pos] = (int32_t)(NR + idx);
+        inv[NR + idx] = pos;
+    }
+    for (int e = c + C * tid; e < ES; e += C * NT) {
+        const int o = off[e], n = cnt[e], end = off[e + 1];
+        for (int r = o + n; r < end; ++r) sorted_ids[r] = (int32_t)NP;
+        for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
+    }
+    if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
+    if (do_resolve) {
+        for (int idx = c * NT + tid; idx < ES * 3; idx += C * NT) {
+            const int e = idx / 3, j = idx % 3;
+            ExpertLoc L{-1, -1};
+            if (cnt[e] > 0) {
+                if (rs.contiguous) {
+                    L = ExpertLoc{0, 3 * e + j};
+                } else {
+                    const int bs = e < E ? rs.buf_slot[e] : -1;
+                    if (bs >= 0) {
+                        const int bb = rs.slots_per_buffer > 0 ? bs / rs.slots_per_buffer : 2;
+                        const bool have = (bb == 0 && rs.have_buf0) || (bb == 1 && rs.have_buf1);
+                        if (bb < 2 && have) L = ExpertLoc{1 + bb, 3 * (bs % rs.slots_per_buffer) + j};
+                        else raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+                    } else if (bs == -1) {
+                        const int p = rs.page_table[e * 3 + j];
+                        if (p >= 0 && p < rs.num_pages) L = ExpertLoc{0, p};
+                        else raise_error(rs.err, PMOE_ERR_PAGE_OOB);
+                    } else {
+                        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+                    }
+                }
+            }
+            rs.loc[idx] = L;
+        }
+    }
+}
+
 // Copy the hidden row of every (token, expert) pair to its sorted row: X[inv[i]] = hidden[token
 // of pair i].  Pad rows are left as they are: in both MMA orientations a pad row only feeds
 // outputs of its own row, which nothing reads.
@@ -350,6 +508,43 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int blo
     if (resolve) rs = *resolve;
     return launch_pdl(align_kernel, dim3(1), dim3(kAlignWarps * 32), align_smem_bytes(E + S), s,
                       ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs,
+                      resolve ? 1 : 0);
+}
+
+int align_ctas(int64_t NR) {
+    int64_t c = (NR + kAlignPairsPerCta - 1) / kAlignPairsPerCta;
+    if (c < 1) c = 1;
+    if (c > kAlignMaxCtas) c = kAlignMaxCtas;
+    return (int)c;
+}
+
+size_t align_part_bytes() { return sizeof(int32_t) * (size_t)kAlignMaxCtas * kMaxExpertsTotal; }
+
+cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, int block_m,
+                               int32_t* part, int32_t* sorted_ids, int32_t* block_expert,
+                               int32_t* inv, int32_t* meta, const ResolveArgs* resolve,
+                               cudaStream_t s) {
+    const int64_t NR = (int64_t)T * k;
+    const int C = align_ctas(NR);
+    if (C == 1)
+        return launch_align(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, resolve, s);
+    const int ES = E + S;
+    const int seg = (int)((NR + C - 1) / C);
+    const size_t sm2 = sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * ES + 1);
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * kMaxExpertsTotal + 1)));
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    ResolveArgs rs{};
+    if (resolve) rs = *resolve;
+    cudaError_t e = launch_pdl(align_count_kernel, dim3(C), dim3(kAlignWarps * 32),
+                               sizeof(int32_t) * ES, s, ids, (int)NR, E, ES, seg, part);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(align_scatter_kernel, dim3(C), dim3(kAlignWarps * 32), sm2, s, ids, T, k, E, S,
+                      block_m, seg, C, (const int32_t*)part, sorted_ids, block_expert, inv, meta, rs,
                       resolve ? 1 : 0);
 }
 

@@ -69,7 +69,7 @@ def test_host_validation_statuses(lib):
         _lib.ERR_INVALID_ARG
     assert lib.pmoe_prefetch_async(None, 0, 1, None, None, None, None, None) == _lib.ERR_INVALID_ARG
     assert lib.pmoe_route(None, 4, 0, 1, 0, None, None, None) == _lib.ERR_INVALID_ARG
-    assert lib.pmoe_align(None, 4, 2, 8, 0, 3, None, None, None, None, None) == _lib.ERR_INVALID_ARG
+    assert lib.pmoe_align(None, 4, 2, 8, 0, 3, None, None, None, None, None, None) == _lib.ERR_INVALID_ARG
     assert lib.pmoe_wait_event(None, 10) == _lib.ERR_INVALID_ARG
     assert lib.pmoe_plan_set_path(None, 0) == _lib.ERR_INVALID_ARG
     assert lib.pmoe_plan_destroy(None) == _lib.OK

@@ -41,7 +41,7 @@ def test_full_size_sampled(name, T, path):
     out = out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot))
     assert L.plan.device_error() == 0
     # routing and sort + pad, whole, bit-exact (block size of the path that ran)
-    path, _ = L.plan.last_run()
+    path = L.plan.last_run()[0]
     ids, w = pm.route(L.logits, cfg.k, cfg.renormalize)
     rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
     assert np.array_equal(ids.cpu().numpy(), rids)

@@ -38,13 +38,20 @@ def test_route_bit_exact(T, E, k, renorm, ties):
     np.testing.assert_allclose(w.cpu().numpy().astype(np.float64), rw, rtol=3e-5, atol=1e-7)
 
 
+@pytest.mark.parametrize("multi", [False, True], ids=["one_cta", "multi_cta"])
 @pytest.mark.parametrize("T,E,k,S,BM", [(16, 8, 2, 0, 16), (37, 60, 4, 4, 16), (4096, 512, 10, 1, 128),
                                          (4096, 60, 4, 4, 128), (8192, 8, 2, 0, 128), (1, 60, 4, 4, 1),
-                                         (0, 8, 2, 1, 16), (33, 3, 3, 2, 4), (1000, 1000, 16, 24, 64)])
-def test_align_bit_exact(T, E, k, S, BM):
+                                         (0, 8, 2, 1, 16), (33, 3, 3, 2, 4), (1000, 1000, 16, 24, 64),
+                                         (30000, 512, 10, 1, 128), (2049, 7, 1, 0, 32)])
+def test_align_bit_exact(T, E, k, S, BM, multi):
     rng = np.random.default_rng(T + 3 * E)
-    ids = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32).reshape(T, k)
-    s, b, inv, npad = pm.align(torch.from_numpy(ids).cuda(), E, S, BM)
+    if T > 5000:   # skewed: a few experts take most pairs
+        pop = np.exp(-1.1 * np.log(np.arange(1, E + 1)))
+        ids = np.array([rng.choice(E, size=k, replace=False, p=pop / pop.sum()) for _ in range(T)],
+                       np.int32).reshape(T, k)
+    else:
+        ids = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32).reshape(T, k)
+    s, b, inv, npad = pm.align(torch.from_numpy(ids).cuda(), E, S, BM, multi_cta=multi)
     torch.cuda.synchronize()
     ref = oracle.align(ids, E, S, BM)
     n = int(npad.item())
@@ -137,8 +144,9 @@ def test_invalid_arguments_rejected():
 
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
+    # tiny: E=8, k=2 -> the small-batch kernels while T*k <= 192*E, i.e. T <= 768
     for T, want in [(1, pm.PATH_TC_DECODE), (16, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
-                    (129, pm.PATH_TC), (512, pm.PATH_TC)]:
+                    (768, pm.PATH_TC_DECODE), (769, pm.PATH_TC), (2048, pm.PATH_TC)]:
         L = setup_layer(cfg, T)
         L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
         assert L.plan.last_run()[0] == want
