@@ -79,11 +79,14 @@ typedef struct pmoe_plan* pmoe_plan_t;
 
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
-    PMOE_PATH_AUTO = 0,   /* TC_DECODE while T*k <= 192*E (routed tokens per expert), else TC */
+    PMOE_PATH_AUTO = 0,   /* by routed tokens per expert T*k/E: <= 192 TC_DECODE, < 384 TC,
+                             else TC2 */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
-    PMOE_PATH_TC_DECODE = 3 /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
-                               on N: weight streaming for small token counts */
+    PMOE_PATH_TC_DECODE = 3, /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
+                                on N: weight streaming for small token counts */
+    PMOE_PATH_TC2 = 4       /* tcgen05 on CTA pairs (cta_group::2), 256-token blocks, 256x256
+                               tiles: the largest token counts */
 } pmoe_path;
 
 /* Text of a status; never NULL. */

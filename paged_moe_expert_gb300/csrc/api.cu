@@ -57,11 +57,12 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
     return bm;
 }
 
-// The automatic path takes the small-batch tensor-core kernels (tokens on the MMA's N side) while
-// the routed experts average at most this many tokens (T*k/E), the 128-token-block kernels above
-// (measured crossover on GB300); routing and sort + pad run as one single-CTA kernel up to 128
-// tokens.
+// The automatic path, by the routed tokens per expert T*k/E (measured crossovers on GB300): up to
+// 192 the small-batch tensor-core kernels (tokens on the MMA's N side), below 384 the single-CTA
+// 128-token-block kernels, from 384 on the CTA-pair kernels, whose 256-token blocks pad little
+// there.  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
 constexpr int kSwapMaxTokensPerExpert = 192;
+constexpr int kPairMinTokensPerExpert = 384;
 constexpr int kPrepSmallMaxTokens = 128;
 
 static int stream_splits(const pmoe_layer_desc& D) {
@@ -101,7 +102,8 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     const int64_t ES = D.num_experts + D.num_shared_chunks;
     const int64_t k = D.top_k;
     W.np = T * (k + D.num_shared_chunks);
-    const int64_t cap_tc = (W.np + ES * (kTcBlockM - 1) + kTcBlockM - 1) / kTcBlockM * kTcBlockM;
+    // rows for any block size up to the pair path's 256
+    const int64_t cap_tc = (W.np + ES * (kTcPairBlockM - 1) + kTcPairBlockM - 1) / kTcPairBlockM * kTcPairBlockM;
     const int64_t cap_st = W.np + ES * (kStreamMaxBlockM - 1);
     W.cap = cap_tc > cap_st ? cap_tc : cap_st;
     W.nblk_max = W.np + ES + 1;  // any block size >= 1
@@ -156,10 +158,13 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
 
     int path = P->path;
-    if (path == PMOE_PATH_AUTO)
-        path = (int64_t)T * D.top_k <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts
-                   ? PMOE_PATH_TC_DECODE : PMOE_PATH_TC;
-    const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE;
+    if (path == PMOE_PATH_AUTO) {
+        const int64_t routed = (int64_t)T * D.top_k;   // routed tokens; per expert: routed / E
+        path = routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
+             : routed < (int64_t)kPairMinTokensPerExpert * D.num_experts ? PMOE_PATH_TC
+             : PMOE_PATH_TC2;
+    }
+    const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE || path == PMOE_PATH_TC2;
     if (tc_family && !P->have_tmaps)
         return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
 
@@ -176,9 +181,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
 
     CUtensorMap xmap, hmap;
     const int64_t ES = D.num_experts + D.num_shared_chunks;
-    const int64_t cap_tc = (W.np + ES * (kTcBlockM - 1) + kTcBlockM - 1) / kTcBlockM * kTcBlockM;
+    const int64_t cap_tc = (W.np + ES * (kTcPairBlockM - 1) + kTcPairBlockM - 1) / kTcPairBlockM * kTcPairBlockM;
     const SwapParams sw = swap_params(D, T);
-    if (path == PMOE_PATH_TC) {
+    if (path == PMOE_PATH_TC || path == PMOE_PATH_TC2) {
         if (!encode_rows_map(&xmap, x, cap_tc, D.d, kTcBlockM) ||
             !encode_rows_map(&hmap, h, cap_tc, D.f, kTcBlockM))
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
@@ -199,6 +204,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     rs.err = P->d_error;
 
     const int bm = path == PMOE_PATH_TC ? kTcBlockM
+                 : path == PMOE_PATH_TC2 ? kTcPairBlockM
                  : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
@@ -233,6 +239,15 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
                                  P->num_sms, P->d_error, stream), "down gemm");
+        ystride = cap_tc;
+        splits = 1;
+    } else if (path == PMOE_PATH_TC2) {
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
+                                    P->num_sms, P->d_error, stream), "gate/up gemm");
+        PMOE_CUDA(mark(P, ev++, stream), "profile event");
+        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
+                                    P->num_sms, P->d_error, stream), "down gemm");
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC_DECODE) {
@@ -348,7 +363,7 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan) {
 }
 
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
-    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC_DECODE)
+    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC2)
         return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
     reinterpret_cast<Plan*>(plan)->path = path;
     return PMOE_OK;

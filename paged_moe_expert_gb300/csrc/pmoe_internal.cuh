@@ -14,6 +14,7 @@ constexpr int kMaxExpertsTotal = 1024;  // E + S
 constexpr int kMaxTopK = 16;
 constexpr int kMaxPairsPerToken = 64;   // k + S
 constexpr int kTcBlockM = 128;          // tensor-core path: rows per sorted block
+constexpr int kTcPairBlockM = 256;      // CTA-pair tensor-core path: rows per sorted block
 constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorted block (max)
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
 
@@ -169,6 +170,12 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
                            cudaStream_t s);
+
+// CTA-pair tensor-core path (tc_gemm2sm.cu): 256-row blocks; mode 1 gate/up -> h, 2 down -> y.
+cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
+                              const CUtensorMap* wmaps, const int32_t* block_expert,
+                              const int32_t* meta, const ExpertLoc* loc, void* out, int f, int d,
+                              int64_t nblk_max, int num_sms, int32_t* err, cudaStream_t s);
 
 // Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials.
 cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act,

@@ -1,0 +1,365 @@
+// Paged grouped expert GEMMs on CTA pairs (tcgen05.mma.cta_group::2, sm_103a).
+//
+// Same operation as the single-CTA kernel in tc_gemm.cu -- Rimuru's paged MoE GEMMs
+// (paper-daily.com/en, "Expert weights are scattered across pages. How does the kernel read
+// them?"; page rule addr_e(n,t) = B_P + p_e(n)*f*d + (n mod f)*d + t as one TMA row coordinate
+// per tile) -- with each 256x256 output tile computed by a pair of CTAs on two SMs.  The pair
+// shares one B operand: each CTA stages half of it, the tensor cores of both SMs read both
+// halves, so every SM moves 32 KB per k-block instead of 48 KB and the shared-memory traffic per
+// MMA drops by a third.  Rows come in blocks of 256 sorted pairs of one expert (128 per CTA).
+//
+//   gate/up: B = [128 rows of the W1 page | 128 rows of the W3 page] for output columns
+//            n0..n0+127: the leader CTA stages the W1 half, its peer the W3 half; every CTA's
+//            accumulator holds gate (columns 0..127) and up (128..255) for its own 128 rows.
+//   down:    B = 256 rows of the W2 page, 128 staged by each CTA.
+//
+// Protocol: both CTAs' TMA loads complete on the leader's full barrier; the leader issues the
+// MMAs and commits them to the empty and accumulator-full barriers of both CTAs (multicast);
+// each CTA's epilogue reads its own TMEM and releases the accumulator on the leader's barrier.
+// Every mbarrier wait is bounded; on a time-out the pair unwinds through the same cluster
+// barriers and TMEM release as a normal exit.
+#include <math.h>
+
+#include "tc_common.cuh"
+
+namespace pmoe {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BMP = 256;               // rows per pair block
+constexpr int BK = 64;
+constexpr int BN = 256;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows
+constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t kIdesc = idesc_bf16(BMP, BN);
+
+enum { kGateUp = 1, kDown = 2 };
+
+struct Tc2Args {
+    const int32_t* block_expert;   // per 256-row block
+    const int32_t* meta;
+    const ExpertLoc* loc;
+    void* out;
+    int f, d;
+    int k_blocks;
+    int n_tiles;
+    int32_t* err;
+};
+
+struct Tc2Maps {
+    CUtensorMap a;      // X_sorted [cap][d] or h [cap][f], 128-row boxes
+    CUtensorMap w[3];   // pool / buffer 0 / buffer 1 weight views, 128-row boxes
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// TMA load into this CTA's shared memory that completes on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        : "memory");
+}
+
+// Arrive (once) on the barrier at this shared-memory offset in both CTAs when the MMAs issued so
+// far have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
+template <bool kContig>
+__device__ __forceinline__ ExpertLoc loc2(const ExpertLoc* loc, int e, int j) {
+    if (kContig) return ExpertLoc{0, 3 * e + j};
+    return loc[e * 3 + j];
+}
+
+template <int kMode, bool kContig>
+__device__ __forceinline__ bool weights_of(const Tc2Args& A, int pb, ExpertLoc& l0, ExpertLoc& l1) {
+    const int e = A.block_expert[pb];
+    if (kMode == kGateUp) {
+        l0 = loc2<kContig>(A.loc, e, 0);
+        l1 = loc2<kContig>(A.loc, e, 1);
+        return l0.map >= 0 && l1.map >= 0;
+    }
+    l0 = loc2<kContig>(A.loc, e, 2);
+    l1 = l0;
+    return l0.map >= 0;
+}
+
+template <int kMode, bool kContig>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_gemm2sm_kernel(const __grid_constant__ Tc2Maps maps, const Tc2Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);     // used on the leader: its producer's expect_tx
+            mbar_init(empty_bar(s), 1);    // the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);    // the leader's multicast commit
+            mbar_init(tempty_bar(a), 8);   // used on the leader: 4 epilogue warps x 2 CTAs
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        // one warp of each CTA allocates the pair's tensor memory together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();            // the peer's barriers exist before anyone signals them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    pdl_allow_next();
+    pdl_wait_prev();
+
+    const int nblocks = args.meta[kMetaNPadded] / BMP;
+    const int64_t ntiles = (int64_t)nblocks * args.n_tiles;
+    const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int pend_phase[STAGES];
+            for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
+            bool ok = true;
+            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+                const int pb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+                ExpertLoc l0, l1;
+                if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
+                const int row_a = pb * BMP + (int)rank * 128;
+                const CUtensorMap* wm;
+                int row_b;
+                if (kMode == kGateUp) {
+                    wm = leader ? &maps.w[l0.map] : &maps.w[l1.map];
+                    row_b = (leader ? l0.page : l1.page) * args.f + nt * 128;
+                } else {
+                    wm = &maps.w[l0.map];
+                    row_b = l0.page * args.d + nt * BN + (int)rank * 128;
+                }
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                    const uint32_t fb_leader = map_to_rank(full_bar(stage), 0);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                    const uint32_t sa = sbase + stage * STAGE_BYTES;
+                    tma_load_2d_pair(sa, &maps.a, fb_leader, kb * BK, row_a);
+                    tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
+                    pend_phase[stage] = (int)phase;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok && leader) {
+                volatile int never = 0;
+                for (int s = 0; s < STAGES; ++s)
+                    if (pend_phase[s] >= 0) mbar_wait(full_bar(s), (uint32_t)pend_phase[s], &never, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
+                const int pb = (int)(t / args.n_tiles);
+                ExpertLoc l0, l1;
+                if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + stage * STAGE_BYTES;
+                    const uint64_t adesc = smem_desc(sa);
+                    const uint64_t bdesc = smem_desc(sa + A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        mma_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
+                                 (kb | k) != 0 ? 1u : 0u);
+                    mma_commit_pair(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit_pair(tfull_bar(acc));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+        }
+    } else {
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t t = cid; t < ntiles; t += ncl) {
+            const int pb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+            ExpertLoc l0, l1;
+            if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
+            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+            const int64_t grow = (int64_t)pb * BMP + (int64_t)rank * 128 + row;
+            if (kMode == kGateUp) {
+                uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 128; c0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(taddr + c0, g);
+                    tmem_ld16(taddr + 128 + c0, u);
+                    tmem_wait_ld();
+                    uint32_t p[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float a0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
+                        const float a1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                        p[i] = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(h + c0);
+                    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                }
+            } else {
+                float* y = static_cast<float*>(args.out) + grow * args.d;
+                const int r0 = nt * BN;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_wait_ld();
+                    if (r0 + c0 < args.d) {
+                        float4* dst = reinterpret_cast<float4*>(y + r0 + c0);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();            // the leader's MMAs no longer read the peer's shared memory
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+template <int kMode, bool kContig>
+cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm2sm_kernel<kMode, kContig>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    return launch_pdl(tc_gemm2sm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), kSmemBytes, s,
+                      maps, a);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
+                              const CUtensorMap* wmaps, const int32_t* block_expert,
+                              const int32_t* meta, const ExpertLoc* loc, void* out, int f, int d,
+                              int64_t nblk_max, int num_sms, int32_t* err, cudaStream_t s) {
+    Tc2Maps maps;
+    maps.a = act;
+    for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    Tc2Args a{};
+    a.block_expert = block_expert;
+    a.meta = meta;
+    a.loc = loc;
+    a.out = out;
+    a.f = f;
+    a.d = d;
+    a.err = err;
+    if (mode == kGateUp) {
+        a.k_blocks = d / BK;
+        a.n_tiles = f / 128;
+    } else {
+        a.k_blocks = f / BK;
+        a.n_tiles = (d + BN - 1) / BN;
+    }
+    const int64_t tiles = nblk_max * a.n_tiles;
+    int64_t clusters = num_sms / 2;
+    if (tiles < clusters) clusters = tiles > 0 ? tiles : 1;
+    const int grid = (int)(2 * clusters);
+    if (mode == kGateUp)
+        return contig ? launch2<kGateUp, true>(maps, a, grid, s) : launch2<kGateUp, false>(maps, a, grid, s);
+    return contig ? launch2<kDown, true>(maps, a, grid, s) : launch2<kDown, false>(maps, a, grid, s);
+}
+
+}  // namespace pmoe

@@ -74,8 +74,8 @@ SMALL = [
 ]
 
 
-PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE]
-PATH_IDS = ["stream", "tc", "tc_decode"]
+PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2]
+PATH_IDS = ["stream", "tc", "tc_decode", "tc2"]
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
@@ -144,9 +144,10 @@ def test_invalid_arguments_rejected():
 
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
-    # tiny: E=8, k=2 -> the small-batch kernels while T*k <= 192*E, i.e. T <= 768
+    # tiny: E=8, k=2 -> T*k/E = T/4: small-batch kernels up to T=768, pairs from T=1536
     for T, want in [(1, pm.PATH_TC_DECODE), (16, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
-                    (768, pm.PATH_TC_DECODE), (769, pm.PATH_TC), (2048, pm.PATH_TC)]:
+                    (768, pm.PATH_TC_DECODE), (769, pm.PATH_TC), (1535, pm.PATH_TC),
+                    (1536, pm.PATH_TC2), (4096, pm.PATH_TC2)]:
         L = setup_layer(cfg, T)
         L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
         assert L.plan.last_run()[0] == want
