@@ -206,7 +206,7 @@ pmoe_status pmoe_route(const float* router_logits, int32_t T, int32_t E, int32_t
  * ascending index within an expert; an expert with c > 0 pairs owns ceil(c/block_m) blocks,
  * pads hold T*(k+S).  Outputs (device): sorted_ids int32 [>= T*(k+S) + (E+S)*(block_m-1)],
  * block_expert int32 [>= T*(k+S)/block_m + E + S], inv int32 [T*(k+S)] (row of each pair),
- * n_padded int32 [1].  block_m a power of two <= 128; E + S <= 1024.  With scratch != NULL
+ * n_padded int32 [1].  block_m a power of two <= 256; E + S <= 1024.  With scratch != NULL
  * (device, >= pmoe_align_scratch_size() bytes) the sort runs over several CTAs when there are
  * more than 2048 routed pairs (the forward's large-batch form); otherwise in one CTA. */
 pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, int32_t S,

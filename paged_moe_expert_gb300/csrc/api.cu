@@ -252,13 +252,19 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         splits = 1;
     } else if (path == PMOE_PATH_TC_DECODE) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_swap(1, contig, sw.bn, xmap, P->tm_rows_d, sorted, T, D.top_k,
+        // few-token blocks: half-size (stacked) tiles once the full-size ones outnumber the SMs,
+        // so the persistent CTAs finish together; below that, full tiles (less epilogue work)
+        const int64_t act_est = (ES < W.np ? ES : W.np);
+        const bool stacked = sw.bn <= 32 && act_est * (D.f / 128) > P->num_sms;
+        PMOE_CUDA(launch_tc_swap(stacked ? 3 : 1, contig, sw.bn, xmap,
+                                 stacked ? P->tm_rows_d64 : P->tm_rows_d, sorted, T, D.top_k,
                                  D.num_shared_chunks, bexp, meta, loc, h, D.f, D.d, 1, 0, nblk,
-                                 P->num_sms, P->d_error, stream), "gate/up gemm");
+                                 P->num_sms, P->d_error, gather_in_prep ? 0 : 1, stream),
+                  "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_swap(2, contig, sw.bn, hmap, P->tm_rows_f, sorted, T, D.top_k,
                                  D.num_shared_chunks, bexp, meta, loc, y, D.f, D.d, sw.splits,
-                                 sw.ystride, nblk, P->num_sms, P->d_error, stream), "down gemm");
+                                 sw.ystride, nblk, P->num_sms, P->d_error, 1, stream), "down gemm");
         ystride = sw.ystride;
         splits = sw.splits;
     } else {
@@ -339,13 +345,16 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
     const int64_t f = desc->f, d = desc->d;
     const int64_t bpages = 3 * (int64_t)desc->slots_per_buffer;
     bool ok = encode_rows_map(&P->tm_rows_d[0], page_pool, num_pages * f, d) &&
+              encode_rows_map(&P->tm_rows_d64[0], page_pool, num_pages * f, d, 64) &&
               encode_rows_map(&P->tm_rows_f[0], page_pool, num_pages * d, f);
     for (int b = 0; b < 2 && ok; ++b) {
         if (P->buf[b] && bpages > 0) {
             ok = encode_rows_map(&P->tm_rows_d[1 + b], P->buf[b], bpages * f, d) &&
+                 encode_rows_map(&P->tm_rows_d64[1 + b], P->buf[b], bpages * f, d, 64) &&
                  encode_rows_map(&P->tm_rows_f[1 + b], P->buf[b], bpages * d, f);
         } else {
             P->tm_rows_d[1 + b] = P->tm_rows_d[0];   // never addressed: no slot maps here
+            P->tm_rows_d64[1 + b] = P->tm_rows_d64[0];
             P->tm_rows_f[1 + b] = P->tm_rows_f[0];
         }
     }
@@ -484,8 +493,8 @@ pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, 
                        int32_t* n_padded, void* scratch, pmoe_stream_t stream) {
     if (T < 0 || top_k <= 0 || E <= 0 || S < 0 || E + S > kMaxExpertsTotal)
         return fail(PMOE_ERR_INVALID_ARG, "bad align sizes");
-    if (block_m < 1 || block_m > 128 || (block_m & (block_m - 1)))
-        return fail(PMOE_ERR_INVALID_ARG, "block_m must be a power of two <= 128");
+    if (block_m < 1 || block_m > 256 || (block_m & (block_m - 1)))
+        return fail(PMOE_ERR_INVALID_ARG, "block_m must be a power of two <= 256");
     if (!sorted_ids || !block_expert || !n_padded || (T > 0 && (!ids || !inv)))
         return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
     if ((int64_t)T * (top_k + S) > (int64_t)1 << 30) return fail(PMOE_ERR_INVALID_ARG, "too many pairs");

@@ -52,6 +52,7 @@ struct Plan {
     int last_path, last_kernels, last_launches;  // what the last forward ran
     int num_sms;
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
+    CUtensorMap tm_rows_d64[3];  // the same views with 64-row boxes (stacked gate/up tiles)
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
 };
 
@@ -78,10 +79,12 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return r;
 }
 
-// Programmatic dependent launch: every kernel of the library lets the next kernel in the stream
-// start its prologue early (launch_dependents) and waits for the previous grid to finish and
-// publish its memory (wait) before it reads or writes any global memory.  A kernel launched
-// without the attribute returns from the wait at once.
+// Programmatic dependent launch: every kernel of the library waits for the previous grid to
+// finish and publish its memory (wait) before it reads or writes global memory that grid
+// touches, and only then lets the next kernel in the stream start (launch_dependents).  So the
+// next kernel's launch and prologue overlap this kernel's work, and a kernel may read what the
+// kernel two launches back wrote before its own wait.  A kernel launched without the attribute
+// returns from the wait at once.
 __device__ __forceinline__ void pdl_allow_next() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -177,12 +180,13 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const int32_t* meta, const ExpertLoc* loc, void* out, int f, int d,
                               int64_t nblk_max, int num_sms, int32_t* err, cudaStream_t s);
 
-// Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials.
+// Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials,
+// mode 3 gate/up with 64+64-row stacked tiles (bn <= 32; weight maps with 64-row boxes).
 cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act,
                            const CUtensorMap* wmaps, const int32_t* sorted_ids, int T, int k,
                            int S, const int32_t* block_expert, const int32_t* meta,
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s);
+                           int early, cudaStream_t s);
 
 }  // namespace pmoe

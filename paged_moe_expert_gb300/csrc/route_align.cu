@@ -84,8 +84,8 @@ template <int EPL>
 __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,
                                                     int k, int renorm, int32_t* __restrict__ ids,
                                                     float* __restrict__ wout) {
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
@@ -239,8 +239,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
     extern __shared__ int32_t smem[];
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, do_resolve, smem);
 }
 
@@ -259,8 +259,8 @@ constexpr int kAlignPairsPerCta = 2048;
 __global__ void __launch_bounds__(kAlignWarps * 32) align_count_kernel(
     const int32_t* __restrict__ ids, int NR, int E, int ES, int seg, int32_t* __restrict__ part) {
     extern __shared__ int32_t h[];
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int tid = threadIdx.x, NT = kAlignWarps * 32, c = blockIdx.x;
     for (int e = tid; e < ES; e += NT) h[e] = 0;
     __syncthreads();
@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
     int32_t* cnt = off + ES + 1;       // [ES]
     int32_t* base = cnt + ES;          // [ES]
     int32_t* cw = base + ES;           // [kAlignWarps][ES]
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, NT = kAlignWarps * 32;
     const int c = blockIdx.x;
     const int64_t NR = (int64_t)T * k, NP = (int64_t)T * (k + S);
@@ -419,8 +419,8 @@ __global__ void __launch_bounds__(256) gather_pairs_kernel(const uint16_t* __res
                                                            const int32_t* __restrict__ inv, int T,
                                                            int k, int S, int d,
                                                            uint16_t* __restrict__ x) {
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (i >= T * (k + S)) return;
     gather_pair(hidden, inv, i, T, k, d, threadIdx.x & 31, x);
@@ -446,8 +446,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
     int32_t* s_ids = s_align + align_words(ES);   // [T*k]
     int32_t* s_bs = s_ids + T * k;                // [E]
     int32_t* s_pt = s_bs + E;                     // [ES*3]
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NT = kAlignWarps * 32;
     const int ntab = rs.contiguous ? 0 : E + 3 * ES;

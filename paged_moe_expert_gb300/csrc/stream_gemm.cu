@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(kThreads) stream_gemm1_kernel(
     const int32_t* __restrict__ block_expert, const int32_t* __restrict__ meta,
     const ExpertLoc* __restrict__ loc, uint16_t* __restrict__ h) {
     extern __shared__ uint4 xs[];  // [MT][d/8]
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int b = blockIdx.y;
     if (b * MT >= meta[kMetaNPadded]) return;
     const int d = L.d, f = L.f, dv = d >> 3;
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(kThreads) stream_gemm2_kernel(
     const int32_t* __restrict__ meta, const ExpertLoc* __restrict__ loc,
     const uint16_t* __restrict__ h, float* __restrict__ y, int64_t ystride) {
     extern __shared__ uint4 hs[];  // [MT][kc/8]
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int b = blockIdx.y;
     if (b * MT >= meta[kMetaNPadded]) return;
     const int d = L.d, f = L.f;
@@ -295,8 +295,8 @@ constexpr int kCombineThreads = 64;
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float* __restrict__ y, int splits, int64_t ystride, const float* __restrict__ w,
     const int32_t* __restrict__ inv, int T, int d, int k, int S, uint16_t* __restrict__ out) {
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
     const int t = blockIdx.y;
     const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // float4 column
     const int P = k + S;

@@ -36,17 +36,27 @@ constexpr int W_BYTES = WROWS * BK * 2;     // 16 KB per weight operand per stag
 constexpr int kThreads = 192;
 constexpr int kRingBytes = 204 * 1024;
 
-enum { kGateUp = 1, kDown = 2 };
+// kGateUp:        tile = 128 W1 rows and 128 W3 rows, two accumulators (gate, up).
+// kDown:          tile = 128 W2 rows.
+// kGateUpStacked: tile = 64 W1 rows stacked over 64 W3 rows in one 128-row operand, one
+//                 accumulator whose lanes 0..63 hold gate and 64..127 up; the epilogue pairs them
+//                 through shared memory.  Half-size tiles: twice as many work items for few-token
+//                 batches, so the persistent CTAs finish together.
+enum { kGateUp = 1, kDown = 2, kGateUpStacked = 3 };
 
 template <int kMode, int BN>
 struct Cfg {
+    static constexpr bool kGateFamily = kMode != kDown;
+    static constexpr int WR = kMode == kGateUpStacked ? 64 : WROWS;   // weight rows per tile (per matrix)
+    static constexpr int W_STAGE = kMode == kGateUp ? 2 * W_BYTES : W_BYTES;
     static constexpr int ACT_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = (kMode == kGateUp ? 2 : 1) * W_BYTES + ACT_BYTES;
-    static constexpr int STAGES_RAW = kRingBytes / STAGE_BYTES;
+    static constexpr int STAGE_BYTES = W_STAGE + ACT_BYTES;
+    static constexpr int XCH_BYTES = kMode == kGateUpStacked ? 64 * BN * 4 : 0;
+    static constexpr int STAGES_RAW = (kRingBytes - XCH_BYTES) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
     static constexpr int ACC_COLS = (kMode == kGateUp ? 2 : 1) * BN;   // one accumulator set
     static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS < 32 ? 32 : 2 * ACC_COLS;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCH_BYTES + 1024 + 256;
     static constexpr uint32_t IDESC = idesc_bf16(WROWS, BN);
 };
 
@@ -62,6 +72,7 @@ struct SwapArgs {
     int w_tiles;          // weight-row tiles per block
     int splits;           // K splits (down projection only)
     int64_t ystride;      // rows per split of y
+    int early;            // 1: the sort's outputs are complete at launch (see the priming below)
     int32_t* err;
 };
 
@@ -85,13 +96,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - raw);
-    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES;
+    // layout: ring | stacked-mode exchange buffer | barriers | TMEM address | abort flag
+    const uint32_t bar0 = sbase + STAGES * C::STAGE_BYTES + C::XCH_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     uint32_t* tmem_holder =
-        reinterpret_cast<uint32_t*>(sgen + STAGES * C::STAGE_BYTES + 8 * (2 * STAGES + 4));
+        reinterpret_cast<uint32_t*>(sgen + STAGES * C::STAGE_BYTES + C::XCH_BYTES + 8 * (2 * STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,15 +131,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // the prologue above touches no global memory; from here on the previous kernel's results
-    // are needed
-    pdl_allow_next();
-    pdl_wait_prev();
-
-    const int nblocks = args.meta[kMetaNPadded] / BN;
-    const int per_block = args.w_tiles * args.splits;
-    const int64_t ntiles = (int64_t)nblocks * per_block;
-    const int kb_per_split = (args.k_blocks + args.splits - 1) / args.splits;
+    int nblocks = 0, per_block = 0, kb_per_split = 0;
+    int64_t ntiles = 0;
+    auto read_work = [&]() {
+        nblocks = args.meta[kMetaNPadded] / BN;
+        per_block = args.w_tiles * args.splits;
+        ntiles = (int64_t)nblocks * per_block;
+        kb_per_split = (args.k_blocks + args.splits - 1) / args.splits;
+    };
 
     // tile t -> (block b, weight-row tile wt, split sp, k-block range)
     auto decode_tile = [&](int64_t t, int& b, int& wt, int& sp, int& kb0, int& kb1) {
@@ -140,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto tile_valid = [&](int b, ExpertLoc& l0, ExpertLoc& l1) {
         const int e = args.block_expert[b];
-        if (kMode == kGateUp) {
+        if (C::kGateFamily) {
             l0 = loc_of<kContig>(args.loc, e, 0);
             l1 = loc_of<kContig>(args.loc, e, 1);
             return l0.map >= 0 && l1.map >= 0;
@@ -150,6 +161,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         return l0.map >= 0;
     };
 
+    // The weight operand of one stage: gate/up two 128-row boxes (W1, W3); stacked a 64-row W1 box
+    // over a 64-row W3 box; down one 128-row W2 box.
+    auto load_weights = [&](uint32_t sa, uint32_t fb, int kb, const ExpertLoc& l0,
+                            const ExpertLoc& l1, int row0, int row1) {
+        tma_load_2d(sa, &maps.w[l0.map], fb, kb * BK, row0);
+        if (kMode == kGateUp) tma_load_2d(sa + W_BYTES, &maps.w[l1.map], fb, kb * BK, row1);
+        if (kMode == kGateUpStacked) tma_load_2d(sa + W_BYTES / 2, &maps.w[l1.map], fb, kb * BK, row1);
+    };
+
+    // Priming: expert weights do not depend on the previous kernel.  When the sort's outputs are
+    // already complete at launch (args.early: the kernel before this one waited for them), the
+    // producer fills the first round of the ring with weight tiles before waiting for the
+    // previous kernel, whose output (the activations) only the other half of each stage needs.
+    int primed = 0;
+    if (args.early) {
+        read_work();
+        if (warp == 0 && lane == 0) {
+            int stage = 0;
+            for (int64_t t = blockIdx.x; t < ntiles && primed < STAGES; t += gridDim.x) {
+                int b, wt, sp, kb0, kb1;
+                decode_tile(t, b, wt, sp, kb0, kb1);
+                ExpertLoc l0, l1;
+                if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
+                const int rows_per_page = C::kGateFamily ? args.f : args.d;
+                const int row0 = l0.page * rows_per_page + wt * C::WR;
+                const int row1 = l1.page * rows_per_page + wt * C::WR;
+                for (int kb = kb0; kb < kb1 && primed < STAGES; ++kb) {
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t sa = sbase + stage * C::STAGE_BYTES;
+                    load_weights(sa, fb, kb, l0, l1, row0, row1);
+                    ++primed;
+                    ++stage;
+                }
+            }
+        }
+    }
+    // the prologue above touches no global memory the previous kernel writes
+    pdl_wait_prev();
+    pdl_allow_next();
+    if (!args.early) read_work();
+
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
@@ -157,22 +210,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pend_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
+            int step = 0;   // (tile, k-block) steps issued; the first `primed` have their weights
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 int b, wt, sp, kb0, kb1;
                 decode_tile(t, b, wt, sp, kb0, kb1);
                 ExpertLoc l0, l1;
                 if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
-                const int rows_per_page = kMode == kGateUp ? args.f : args.d;
-                const int row0 = l0.page * rows_per_page + wt * WROWS;
-                const int row1 = l1.page * rows_per_page + wt * WROWS;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                const int rows_per_page = C::kGateFamily ? args.f : args.d;
+                const int row0 = l0.page * rows_per_page + wt * C::WR;
+                const int row1 = l1.page * rows_per_page + wt * C::WR;
+                for (int kb = kb0; kb < kb1; ++kb, ++step) {
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
                     const uint32_t sa = sbase + stage * C::STAGE_BYTES;
-                    tma_load_2d(sa, &maps.w[l0.map], fb, kb * BK, row0);
-                    if (kMode == kGateUp) tma_load_2d(sa + W_BYTES, &maps.w[l1.map], fb, kb * BK, row1);
-                    tma_load_2d(sa + (kMode == kGateUp ? 2 : 1) * W_BYTES, &maps.act, fb, kb * BK, b * BN);
+                    if (step >= primed) {
+                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
+                        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                        load_weights(sa, fb, kb, l0, l1, row0, row1);
+                    }
+                    tma_load_2d(sa + C::W_STAGE, &maps.act, fb, kb * BK, b * BN);
                     pend_phase[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -204,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + stage * C::STAGE_BYTES;
                     const uint64_t w0 = smem_desc(sa);
                     const uint64_t w1 = smem_desc(sa + W_BYTES);
-                    const uint64_t xa = smem_desc(sa + (kMode == kGateUp ? 2 : 1) * W_BYTES);
+                    const uint64_t xa = smem_desc(sa + C::W_STAGE);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
@@ -247,6 +302,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float a = g[j] / (1.f + expf(-g[j])) * u[j];
                         h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(a);
                     }
+                }
+            } else if (kMode == kGateUpStacked) {
+                // lanes 64..127 (quads 2, 3) hold up, lanes 0..63 (quads 0, 1) gate, both for the
+                // tile's 64 output columns: up goes through shared memory, token-major
+                float* xch = reinterpret_cast<float*>(sgen + STAGES * C::STAGE_BYTES);
+                const bool up_half = quad >= 2;
+                const int r = wrow & 63;
+                uint16_t* h = static_cast<uint16_t*>(args.out) + wt * 64 + r;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_wait_ld();
+                    if (up_half) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) xch[(c0 + j) * 64 + r] = v[j];
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (!up_half) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g = v[j], u = xch[(c0 + j) * 64 + r];
+                            h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(g / (1.f + expf(-g)) * u);
+                        }
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
                 }
             } else {
                 const int r = wt * WROWS + wrow;
@@ -297,8 +378,12 @@ cudaError_t launch_swap_bn(int bn, const SwapMaps& maps, const SwapArgs& a, int 
     switch (bn) {
         case 16: return launch_swap_one<kMode, 16, kContig>(maps, a, grid, s);
         case 32: return launch_swap_one<kMode, 32, kContig>(maps, a, grid, s);
-        case 64: return launch_swap_one<kMode, 64, kContig>(maps, a, grid, s);
-        case 128: return launch_swap_one<kMode, 128, kContig>(maps, a, grid, s);
+        case 64:
+            if constexpr (kMode != kGateUpStacked) return launch_swap_one<kMode, 64, kContig>(maps, a, grid, s);
+            return cudaErrorInvalidValue;
+        case 128:
+            if constexpr (kMode != kGateUpStacked) return launch_swap_one<kMode, 128, kContig>(maps, a, grid, s);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
@@ -310,7 +395,7 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
                            int S, const int32_t* block_expert, const int32_t* meta,
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s) {
+                           int early, cudaStream_t s) {
     SwapMaps maps;
     maps.act = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
@@ -327,9 +412,10 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
     a.d = d;
     a.err = err;
     a.ystride = ystride;
-    if (mode == kGateUp) {
+    a.early = early;
+    if (mode == kGateUp || mode == kGateUpStacked) {
         a.k_blocks = d / BK;
-        a.w_tiles = f / WROWS;
+        a.w_tiles = f / (mode == kGateUp ? WROWS : 64);
         a.splits = 1;
     } else {
         a.k_blocks = f / BK;
@@ -341,6 +427,11 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
     if (mode == kGateUp)
         return contig ? launch_swap_bn<kGateUp, true>(bn, maps, a, grid, s)
                       : launch_swap_bn<kGateUp, false>(bn, maps, a, grid, s);
+    if (mode == kGateUpStacked) {
+        if (bn > 32) return cudaErrorInvalidValue;   // stacked tiles serve few-token blocks
+        return contig ? launch_swap_bn<kGateUpStacked, true>(bn, maps, a, grid, s)
+                      : launch_swap_bn<kGateUpStacked, false>(bn, maps, a, grid, s);
+    }
     return contig ? launch_swap_bn<kDown, true>(bn, maps, a, grid, s)
                   : launch_swap_bn<kDown, false>(bn, maps, a, grid, s);
 }

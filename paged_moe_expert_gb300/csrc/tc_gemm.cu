@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_holder;
     // the prologue above touches no global memory; from here on the previous kernel's results
     // are needed
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
 
     const int nblocks = args.meta[kMetaNPadded] / BM;
     const int64_t ntiles = (int64_t)nblocks * args.n_tiles;

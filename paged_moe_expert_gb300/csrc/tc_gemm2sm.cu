@@ -173,8 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();            // the peer's barriers exist before anyone signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    pdl_allow_next();
     pdl_wait_prev();
+    pdl_allow_next();
 
     const int nblocks = args.meta[kMetaNPadded] / BMP;
     const int64_t ntiles = (int64_t)nblocks * args.n_tiles;

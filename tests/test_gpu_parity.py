@@ -42,7 +42,7 @@ def test_route_bit_exact(T, E, k, renorm, ties):
 @pytest.mark.parametrize("T,E,k,S,BM", [(16, 8, 2, 0, 16), (37, 60, 4, 4, 16), (4096, 512, 10, 1, 128),
                                          (4096, 60, 4, 4, 128), (8192, 8, 2, 0, 128), (1, 60, 4, 4, 1),
                                          (0, 8, 2, 1, 16), (33, 3, 3, 2, 4), (1000, 1000, 16, 24, 64),
-                                         (30000, 512, 10, 1, 128), (2049, 7, 1, 0, 32)])
+                                         (30000, 512, 10, 1, 128), (2049, 7, 1, 0, 32), (8192, 8, 2, 0, 256)])
 def test_align_bit_exact(T, E, k, S, BM, multi):
     rng = np.random.default_rng(T + 3 * E)
     if T > 5000:   # skewed: a few experts take most pairs
