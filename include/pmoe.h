@@ -85,8 +85,9 @@ typedef enum {
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
     PMOE_PATH_TC_DECODE = 3, /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
                                 on N: weight streaming for small token counts */
-    PMOE_PATH_TC2 = 4       /* tcgen05 on CTA pairs (cta_group::2), 256-token blocks, 256x256
-                               tiles: the largest token counts */
+    PMOE_PATH_TC2 = 4       /* 128-token blocks, taken two at a time per expert by CTA pairs
+                               (tcgen05 cta_group::2, 256x256 tiles); an expert's odd last
+                               block runs on one CTA */
 } pmoe_path;
 
 /* Text of a status; never NULL. */

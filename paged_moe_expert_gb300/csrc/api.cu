@@ -117,6 +117,8 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.meta = o;   o = align256(o + sizeof(int32_t) * kMetaCount);
     W.loc = o;    o = align256(o + sizeof(ExpertLoc) * ES * 3);
     W.part = o;   o = align256(o + align_part_bytes());
+    W.pairs = o;  o = align256(o + sizeof(int32_t) * (W.nblk_max / 2 + 1));
+    W.singles = o; o = align256(o + sizeof(int32_t) * (ES + 1));
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
@@ -203,9 +205,14 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     rs.loc = loc;
     rs.err = P->d_error;
 
-    const int bm = path == PMOE_PATH_TC ? kTcBlockM
-                 : path == PMOE_PATH_TC2 ? kTcPairBlockM
+    const int bm = (path == PMOE_PATH_TC || path == PMOE_PATH_TC2) ? kTcBlockM
                  : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
+    int32_t* pair_list = at<int32_t>(ws, W.pairs);
+    int32_t* single_list = at<int32_t>(ws, W.singles);
+    if (path == PMOE_PATH_TC2) {
+        rs.pair_list = pair_list;
+        rs.single_list = single_list;
+    }
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
@@ -242,12 +249,22 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC2) {
+        // pairs of 128-row blocks on CTA pairs, then each expert's odd last block on one CTA
+        const int64_t npairs_max = nblk / 2 + 1, nsingles_max = ES < nblk ? ES : nblk;
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
-                                    P->num_sms, P->d_error, stream), "gate/up gemm");
+        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, pair_list, meta, loc, h,
+                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
+                  "gate/up gemm (pairs)");
+        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d,
+                                 nsingles_max, P->num_sms, P->d_error, stream, single_list,
+                                 kMetaSingles), "gate/up gemm (singles)");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
-                                    P->num_sms, P->d_error, stream), "down gemm");
+        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, pair_list, meta, loc, y,
+                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
+                  "down gemm (pairs)");
+        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d,
+                                 nsingles_max, P->num_sms, P->d_error, stream, single_list,
+                                 kMetaSingles), "down gemm (singles)");
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC_DECODE) {
@@ -288,7 +305,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
     P->last_kernels = ev - 1;
-    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
+    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0) +
+                       (path == PMOE_PATH_TC2 ? 2 : 0);
     return PMOE_OK;
 }
 

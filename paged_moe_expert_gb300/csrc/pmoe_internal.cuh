@@ -27,7 +27,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, part, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, pairs, singles, x, h, y, total;
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
     int64_t nblk_max;    // upper bound on sorted blocks
@@ -36,7 +36,7 @@ struct WsLayout {
 };
 
 // meta[] slots
-enum { kMetaNPadded = 0, kMetaCount = 16 };
+enum { kMetaNPadded = 0, kMetaPairs = 1, kMetaSingles = 2, kMetaCount = 16 };
 
 struct Plan {
     pmoe_layer_desc desc;
@@ -123,6 +123,11 @@ struct ResolveArgs {
     int32_t contiguous;         // 1: expert e's matrix j is pool page 3e + j, tables unused
     ExpertLoc* loc;             // [E+S][3] out
     int32_t* err;
+    // optional work lists over the sorted blocks (NULL: not written): for each expert, its blocks
+    // taken two at a time (first block of each pair) and its odd last block; counts in
+    // meta[kMetaPairs], meta[kMetaSingles]
+    int32_t* pair_list;
+    int32_t* single_list;
 };
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
@@ -169,16 +174,19 @@ cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float*
 bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                      int box_rows = 128);
 // mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32)
+// list != NULL: only the blocks in list[0 .. meta[list_meta]) (single blocks of the pair path)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s);
+                           cudaStream_t s, const int32_t* list = nullptr, int list_meta = 0);
 
-// CTA-pair tensor-core path (tc_gemm2sm.cu): 256-row blocks; mode 1 gate/up -> h, 2 down -> y.
+// CTA-pair tensor-core path (tc_gemm2sm.cu): pairs of consecutive 128-row blocks of one expert
+// from pair_list (count meta[kMetaPairs]); mode 1 gate/up -> h, 2 down -> y.
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
-                              const int32_t* meta, const ExpertLoc* loc, void* out, int f, int d,
-                              int64_t nblk_max, int num_sms, int32_t* err, cudaStream_t s);
+                              const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
+                              void* out, int f, int d, int64_t npairs_max, int num_sms,
+                              int32_t* err, cudaStream_t s);
 
 // Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials,
 // mode 3 gate/up with 64+64-row stacked tiles (bn <= 32; weight maps with 64-row boxes).

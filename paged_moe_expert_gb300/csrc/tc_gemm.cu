@@ -52,6 +52,8 @@ struct TcArgs {
     int k_blocks;       // K / 64
     int n_tiles;        // N tiles per sorted block
     int32_t* err;
+    const int32_t* list;   // NULL: every block; else the blocks list[0 .. meta[list_meta])
+    int list_meta;
 };
 
 struct TcMaps {
@@ -126,8 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_prev();
     pdl_allow_next();
 
-    const int nblocks = args.meta[kMetaNPadded] / BM;
+    const int nblocks = args.list ? args.meta[args.list_meta] : args.meta[kMetaNPadded] / BM;
     const int64_t ntiles = (int64_t)nblocks * args.n_tiles;
+    auto block_of = [&](int64_t t) {
+        const int i = (int)(t / args.n_tiles);
+        return args.list ? args.list[i] : i;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -138,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int mb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+                const int mb = block_of(t), nt = (int)(t % args.n_tiles);
                 ExpertLoc l0, l1;
                 if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
                 const CUtensorMap* w0 = &maps.w[l0.map];
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int mb = (int)(t / args.n_tiles);
+                const int mb = block_of(t);
                 ExpertLoc l0, l1;
                 if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-            const int mb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+            const int mb = block_of(t), nt = (int)(t % args.n_tiles);
             ExpertLoc l0, l1;
             if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
@@ -322,7 +328,7 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s) {
+                           cudaStream_t s, const int32_t* list, int list_meta) {
     TcMaps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
@@ -334,6 +340,8 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
     a.f = f;
     a.d = d;
     a.err = err;
+    a.list = list;
+    a.list_meta = list_meta;
     if (mode == kGateUp) {
         a.k_blocks = d / BK;
         a.n_tiles = f / 128;

@@ -6,7 +6,9 @@
 // per tile) -- with each 256x256 output tile computed by a pair of CTAs on two SMs.  The pair
 // shares one B operand: each CTA stages half of it, the tensor cores of both SMs read both
 // halves, so every SM moves 32 KB per k-block instead of 48 KB and the shared-memory traffic per
-// MMA drops by a third.  Rows come in blocks of 256 sorted pairs of one expert (128 per CTA).
+// MMA drops by a third.  A tile's 256 rows are two consecutive 128-row blocks of one expert (one
+// per CTA), taken from the sort's pair list; an expert's odd last block goes to the single-CTA
+// kernel, so no row is padded beyond 128.
 //
 //   gate/up: B = [128 rows of the W1 page | 128 rows of the W3 page] for output columns
 //            n0..n0+127: the leader CTA stages the W1 half, its peer the W3 half; every CTA's
@@ -28,7 +30,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int BMP = 256;               // rows per pair block
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int STAGES = 6;
@@ -38,12 +39,13 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint32_t kIdesc = idesc_bf16(BMP, BN);
+constexpr uint32_t kIdesc = idesc_bf16(256, BN);   // M = 256: 128 rows on each CTA
 
 enum { kGateUp = 1, kDown = 2 };
 
 struct Tc2Args {
-    const int32_t* block_expert;   // per 256-row block
+    const int32_t* block_expert;   // per 128-row block
+    const int32_t* pair_list;      // first block of each pair (the pair is blocks b, b+1)
     const int32_t* meta;
     const ExpertLoc* loc;
     void* out;
@@ -117,8 +119,8 @@ __device__ __forceinline__ ExpertLoc loc2(const ExpertLoc* loc, int e, int j) {
 }
 
 template <int kMode, bool kContig>
-__device__ __forceinline__ bool weights_of(const Tc2Args& A, int pb, ExpertLoc& l0, ExpertLoc& l1) {
-    const int e = A.block_expert[pb];
+__device__ __forceinline__ bool weights_of(const Tc2Args& A, int b, ExpertLoc& l0, ExpertLoc& l1) {
+    const int e = A.block_expert[b];
     if (kMode == kGateUp) {
         l0 = loc2<kContig>(A.loc, e, 0);
         l1 = loc2<kContig>(A.loc, e, 1);
@@ -176,8 +178,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pdl_wait_prev();
     pdl_allow_next();
 
-    const int nblocks = args.meta[kMetaNPadded] / BMP;
-    const int64_t ntiles = (int64_t)nblocks * args.n_tiles;
+    const int npairs = args.meta[kMetaPairs];
+    const int64_t ntiles = (int64_t)npairs * args.n_tiles;
     const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
     if (warp == 0) {
@@ -188,10 +190,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
             for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                const int pb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+                const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
                 ExpertLoc l0, l1;
                 if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
-                const int row_a = pb * BMP + (int)rank * 128;
+                const int row_a = (pb + (int)rank) * 128;
                 const CUtensorMap* wm;
                 int row_b;
                 if (kMode == kGateUp) {
@@ -226,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                const int pb = (int)(t / args.n_tiles);
+                const int pb = args.pair_list[t / args.n_tiles];
                 ExpertLoc l0, l1;
                 if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
@@ -256,13 +258,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int64_t t = cid; t < ntiles; t += ncl) {
-            const int pb = (int)(t / args.n_tiles), nt = (int)(t % args.n_tiles);
+            const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
             ExpertLoc l0, l1;
             if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-            const int64_t grow = (int64_t)pb * BMP + (int64_t)rank * 128 + row;
+            const int64_t grow = (int64_t)(pb + (int)rank) * 128 + row;
             if (kMode == kGateUp) {
                 uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128;
 #pragma unroll 1
@@ -333,13 +335,15 @@ cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_
 
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
-                              const int32_t* meta, const ExpertLoc* loc, void* out, int f, int d,
-                              int64_t nblk_max, int num_sms, int32_t* err, cudaStream_t s) {
+                              const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
+                              void* out, int f, int d, int64_t npairs_max, int num_sms,
+                              int32_t* err, cudaStream_t s) {
     Tc2Maps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
     Tc2Args a{};
     a.block_expert = block_expert;
+    a.pair_list = pair_list;
     a.meta = meta;
     a.loc = loc;
     a.out = out;
@@ -353,7 +357,7 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
         a.k_blocks = f / BK;
         a.n_tiles = (d + BN - 1) / BN;
     }
-    const int64_t tiles = nblk_max * a.n_tiles;
+    const int64_t tiles = npairs_max * a.n_tiles;
     int64_t clusters = num_sms / 2;
     if (tiles < clusters) clusters = tiles > 0 ? tiles : 1;
     const int grid = (int)(2 * clusters);

@@ -47,7 +47,7 @@ def test_full_size_sampled(name, T, path):
     assert np.array_equal(ids.cpu().numpy(), rids)
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=3e-5, atol=1e-7)
     p2 = 1 << max(0, (T - 1).bit_length())            # next power of two >= T
-    bm = {pm.PATH_TC: 128, pm.PATH_TC2: 256, pm.PATH_TC_DECODE: min(128, max(16, p2)),
+    bm = {pm.PATH_TC: 128, pm.PATH_TC2: 128, pm.PATH_TC_DECODE: min(128, max(16, p2)),
           pm.PATH_STREAM: min(16, p2)}[path]
     s, b, inv, npad = pm.align(ids, cfg.E, cfg.S, bm)
     ref_al = oracle.align(rids, cfg.E, cfg.S, bm)
