@@ -460,26 +460,50 @@ def main():
     sec = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3 / args.steps, dist, device)
     dom_sec = float(np.mean([prof[i][dom].elapsed_time(prof[i][dom + 1]) for i in range(args.steps)])) * 1e-3
 
-    # e2e: host buffers in, result out, copies inside the timed region
+    # e2e: every step copies its inputs from pinned host memory and its result back, inside the
+    # timed region.  Device buffers are double-buffered so step i+1's host->device copy and step
+    # i-1's device->host copy (on their own streams) overlap step i's forward, ordered by events.
     h_host = hidden.cpu().pin_memory()
     l_host = logits.cpu().pin_memory()
-    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    o_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    hid_d = [hidden, torch.empty_like(hidden)]
+    lg_d = [logits, torch.empty_like(logits)]
+    out_d = [out, torch.empty_like(out)]
+    cp_in, cp_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    read_done = [torch.cuda.Event() for _ in range(2)]   # the forward of this slot finished
+    out_done = [torch.cuda.Event() for _ in range(2)]    # the result of this slot is on the host
+    for b in range(2):
+        read_done[b].record(stream)
+        out_done[b].record(stream)
 
-    def e2e_step():
-        hidden.copy_(h_host, non_blocking=True)
-        logits.copy_(l_host, non_blocking=True)
-        step()
-        o_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(cp_in):
+            cp_in.wait_event(read_done[b])           # the slot's previous forward has read it
+            hid_d[b].copy_(h_host, non_blocking=True)
+            lg_d[b].copy_(l_host, non_blocking=True)
+            in_ready[b].record(cp_in)
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_done[b])               # the slot's previous result has left
+        lay.plan.forward(hid_d[b], lg_d[b], lay.page_table, lay.buf_slot, out=out_d[b], workspace=ws)
+        read_done[b].record(stream)
+        with torch.cuda.stream(cp_out):
+            cp_out.wait_event(read_done[b])
+            o_host[b].copy_(out_d[b], non_blocking=True)
+            out_done[b].record(cp_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    cp_in.wait_event(e0)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_event(out_done[(args.steps - 1) % 2])   # the last result is on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_sec = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, dist, device)
