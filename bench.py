@@ -32,7 +32,7 @@ if ROOT not in sys.path:
 from paged_moe_expert_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "paged fused-MoE TFLOP/s & weight GB/s vs roofline; overhead vs contiguous"
-PATH_NAMES = {0: "auto", 1: "stream", 2: "tc", 3: "tc_decode", 4: "tc2"}
+PATH_NAMES = {0: "auto", 1: "stream", 2: "tc", 3: "tc_decode", 4: "tc2", 5: "fused"}
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -241,7 +241,7 @@ class Layer:
 
 
 def tc_family_path(path):
-    return path in (2, 3, 4)
+    return path in (2, 3, 4, 5)
 
 
 def max_over_ranks(seconds: float, dist, device) -> float:
@@ -368,7 +368,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="qwen15", choices=sorted(syn.CONFIGS))
     ap.add_argument("--tokens", type=int, default=0)
-    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc", "tc_decode", "tc2"])
+    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc", "tc_decode", "tc2", "fused"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sweep-iters", type=int, default=20)
@@ -404,7 +404,8 @@ def main():
     T = args.tokens or cfg.tokens[-1]
     lay = Layer(cfg, device, contiguous=not args.no_sweep)
     if args.path != "auto":
-        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC, "tc_decode": pm.PATH_TC_DECODE, "tc2": pm.PATH_TC2}[args.path]
+        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC, "tc_decode": pm.PATH_TC_DECODE, "tc2": pm.PATH_TC2,
+             "fused": pm.PATH_FUSED}[args.path]
         lay.plan.set_path(p)
         if lay.cplan is not None:
             lay.cplan.set_path(p)
@@ -540,12 +541,15 @@ def main():
         names = ["route", "align", "gather", "gemm1", "gemm2", "combine"]
     elif nk == 5:
         names = (["prep", "gather"] if tc_family_path(path) else ["route", "align"]) + ["gemm1", "gemm2", "combine"]
+    elif nk == 1:
+        names = ["fused"]   # routing, both projections and the combine in one kernel
     else:
         names = ["prep", "gemm1", "gemm2", "combine"]
     kname = names[dom]
+    wk["fused"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
     kwork = wk.get(kname, {"flops": 0.0, "bytes": 0.0})
     ksec = dom_sec
-    tc_family = path in (pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2)
+    tc_family = path in (pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED)
     if tc_family and kwork["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
         roof = {"bound": "tensor", "achieved": kwork["flops"] / ksec / 1e12,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}

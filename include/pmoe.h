@@ -79,15 +79,19 @@ typedef struct pmoe_plan* pmoe_plan_t;
 
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
-    PMOE_PATH_AUTO = 0,   /* by routed tokens per expert T*k/E: <= 192 TC_DECODE, < 384 TC,
+    PMOE_PATH_AUTO = 0,   /* FUSED up to 32 tokens (E <= 128) or 16 tokens (E > 128); above,
+                             by routed tokens per expert T*k/E: <= 192 TC_DECODE, < 384 TC,
                              else TC2 */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
     PMOE_PATH_TC_DECODE = 3, /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
                                 on N: weight streaming for small token counts */
-    PMOE_PATH_TC2 = 4       /* 128-token blocks, taken two at a time per expert by CTA pairs
+    PMOE_PATH_TC2 = 4,      /* 128-token blocks, taken two at a time per expert by CTA pairs
                                (tcgen05 cta_group::2, 256x256 tiles); an expert's odd last
                                block runs on one CTA */
+    PMOE_PATH_FUSED = 5     /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
+                               (one CTA per SM) whose weight streams are split evenly over the
+                               SMs; see moe_paged_forward for what it requires of the caller */
 } pmoe_path;
 
 /* Text of a status; never NULL. */
@@ -116,7 +120,7 @@ pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_steps
  * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
  * recorded), so elapsed times between consecutive events are per-kernel durations.  The kernel
  * order is: routing, sort-and-pad, [row gather,] gate/up GEMM, down GEMM, combine, where for
- * T <= 128 routing and sort-and-pad are one kernel.  NULL entries
+ * T <= 128 routing and sort-and-pad are one kernel; the fused decode path is one kernel.  NULL entries
  * are skipped (to bracket one kernel only).  The caller owns the events; n = 0 (or events = NULL)
  * turns the hook off.  At most 16 events. */
 pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* events, int32_t n);
@@ -137,7 +141,18 @@ size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens);
  * SiLU-and-mul epilogue; down GEMM; weighted top-k combine plus the shared expert.
  * out[t] = bf16( sum_j w[t,j] * y_{t,ids[t,j]} + sum_s y_{t,E+s} ), summed in that order.
  * The call neither allocates nor synchronises, so it can be captured in a CUDA graph; the
- * captured launches keep the addresses of this call's buffers and workspace. */
+ * captured launches keep the addresses of this call's buffers and workspace.
+ * Kernels are launched with programmatic dependent launch: a kernel may start while the
+ * previous kernel of the stream is finishing, and before it waits for that kernel it already
+ * reads the page pool, the load buffers, page_table and buf_slot (never hidden, logits or the
+ * workspace).  So those four must not be written by a kernel of the same stream that triggers
+ * its dependents early (no kernel of this library writes them; ordinary kernels and copies are
+ * complete before the next launch starts).
+ * The fused decode path (T <= 32) synchronises its CTAs through two words that the plan owns, so
+ * forward calls of one plan must not overlap on the GPU (the plan's error word is shared the same
+ * way).  Its waits give up after about 2 s with PMOE_ERR_TIMEOUT in the error word (only if the
+ * GPU cannot hold one CTA per SM for this call, e.g. when other work occupies SMs indefinitely);
+ * reading the error word with clear != 0 resets the plan's words for the next call. */
 pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
                               const float* router_logits, int32_t top_k, const int32_t* page_table,
                               const int32_t* buf_slot, void* out, void* workspace,
@@ -190,7 +205,8 @@ pmoe_status pmoe_prefetch_async(pmoe_plan_t plan, int32_t buf, int32_t n,
 pmoe_status pmoe_wait_event(pmoe_event_t ev, int32_t timeout_ms);
 
 /* Read (and, if clear != 0, reset to 0) the plan's device error word: 0 or a pmoe_status code
- * raised by a kernel.  Synchronises with `stream` (NULL = legacy default stream). */
+ * raised by a kernel.  Clearing also resets the fused decode path's grid-barrier words.
+ * Synchronises with `stream` (NULL = legacy default stream). */
 pmoe_status pmoe_get_device_error(pmoe_plan_t plan, int32_t clear, int32_t* code,
                                   pmoe_stream_t stream);
 

@@ -14,10 +14,12 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import PATH_AUTO, PATH_STREAM, PATH_TC, PATH_TC2, PATH_TC_DECODE, LayerDesc, PmoeError
+from ._lib import (PATH_AUTO, PATH_FUSED, PATH_STREAM, PATH_TC, PATH_TC2, PATH_TC_DECODE, LayerDesc,
+                   PmoeError)
 
 __all__ = ["LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
-           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "make_desc"]
+           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
+           "make_desc"]
 
 
 def make_desc(d, f, num_experts, top_k, renormalize, num_shared_chunks=0, slots_per_buffer=0):

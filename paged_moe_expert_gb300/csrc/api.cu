@@ -33,6 +33,14 @@ static pmoe_status cuda_fail(cudaError_t e, const char* where) {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Device words a plan owns: the error word, (at 1 KB) one barrier word per CTA, (at 2 KB)
+// the fused decode kernel's gate/up tile counters (8 B) and ready words (4 B), one per tile of
+// f/64 columns of every expert and shared chunk.
+static size_t plan_words_bytes(const pmoe_layer_desc& D) {
+    const size_t tiles = (size_t)(D.num_experts + D.num_shared_chunks) * (D.f / 64);
+    return 2048 + 12 * tiles;
+}
+
 static bool desc_ok(const pmoe_layer_desc* D) {
     if (!D) return false;
     if (D->d <= 0 || D->f <= 0 || D->num_experts <= 0 || D->top_k <= 0) return false;
@@ -96,6 +104,27 @@ static SwapParams swap_params(const pmoe_layer_desc& D, int64_t T) {
     return p;
 }
 
+// Fused decode kernel sizes for T <= kFusedMaxTokens tokens: MMA N (16 or 32), active-expert
+// slots (shared chunks first), and piece slots of the stream-K partial buffers (one per unit plus
+// one per CTA boundary inside a unit, for at most kFusedMaxGrid CTAs per iteration space).
+struct FusedShape {
+    int bn;
+    int64_t a_max, u1_shared, u1_routed_max, u2_max, p1_pieces, p2_pieces;
+};
+static FusedShape fused_shape(const pmoe_layer_desc& D, int64_t T) {
+    FusedShape F{};
+    F.bn = T <= 16 ? 16 : 32;
+    const int64_t routed = T * D.top_k < D.num_experts ? T * D.top_k : D.num_experts;
+    F.a_max = routed + D.num_shared_chunks;
+    const int64_t f64 = D.f / 64, m2 = (D.d + 127) / 128;
+    F.u1_shared = D.num_shared_chunks * f64;
+    F.u1_routed_max = routed * f64;
+    F.u2_max = F.a_max * m2;
+    F.p1_pieces = F.u1_shared + F.u1_routed_max + 2 * kFusedMaxGrid;
+    F.p2_pieces = F.u2_max + kFusedMaxGrid;
+    return F;
+}
+
 // One layout that serves both kernel families for up to T tokens.
 static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     WsLayout W{};
@@ -129,6 +158,16 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     if (y_sw > y_max) y_max = y_sw;
     W.y = o;      o = align256(o + y_max);
     W.total = o;
+    // fused decode kernel (T <= kFusedMaxTokens): partials and h, over the regions above
+    W.fp1 = W.fh = W.fp2 = 0;
+    if (T <= kFusedMaxTokens) {
+        const FusedShape F = fused_shape(D, T);
+        size_t q = W.x;
+        W.fp1 = q; q = align256(q + sizeof(float) * (size_t)F.p1_pieces * F.bn * 128);
+        W.fh = q;  q = align256(q + 2 * (size_t)F.a_max * F.bn * D.f);
+        W.fp2 = q; q = align256(q + sizeof(float) * (size_t)F.p2_pieces * F.bn * 128);
+        if (q > W.total) W.total = q;
+    }
     return W;
 }
 
@@ -160,13 +199,21 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (ws_bytes < W.total) return fail(PMOE_ERR_WORKSPACE, "workspace too small");
 
     int path = P->path;
+    if (path == PMOE_PATH_FUSED && T > kFusedMaxTokens)
+        return fail(PMOE_ERR_UNSUPPORTED, "the fused decode kernel takes at most 32 tokens");
     if (path == PMOE_PATH_AUTO) {
         const int64_t routed = (int64_t)T * D.top_k;   // routed tokens; per expert: routed / E
-        path = routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
+        // the fused decode kernel up to 32 tokens for layers of at most 128 experts and up to 16
+        // tokens otherwise (measured on GB300: with hundreds of small experts at 17..32 tokens
+        // the small-batch kernels stream a little faster)
+        const int fused_max = D.num_experts <= 128 ? kFusedMaxTokens : 16;
+        path = T <= fused_max ? PMOE_PATH_FUSED
+             : routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
              : routed < (int64_t)kPairMinTokensPerExpert * D.num_experts ? PMOE_PATH_TC
              : PMOE_PATH_TC2;
     }
-    const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE || path == PMOE_PATH_TC2;
+    const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE || path == PMOE_PATH_TC2 ||
+                           path == PMOE_PATH_FUSED;
     if (tc_family && !P->have_tmaps)
         return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
 
@@ -192,6 +239,58 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     } else if (path == PMOE_PATH_TC_DECODE) {
         if (!encode_rows_map(&xmap, x, cap_tc, D.d, sw.bn) || !encode_rows_map(&hmap, h, cap_tc, D.f, sw.bn))
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+    }
+
+    if (path == PMOE_PATH_FUSED) {
+        // routing, gate/up + SiLU-and-mul, down and the combine in one persistent launch
+        const FusedShape F = fused_shape(D, T);
+        const int grid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;
+        CUtensorMap fx, fh;
+        if (!encode_rows_map(&fx, hidden, T, D.d, F.bn) ||
+            !encode_rows_map(&fh, at<uint16_t>(ws, W.fh), F.a_max * F.bn, D.f, F.bn))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+        FusedArgs fa{};
+        fa.logits = logits;
+        fa.page_table = page_table;
+        fa.buf_slot = buf_slot;
+        fa.p1 = at<float>(ws, W.fp1);
+        fa.h = at<uint16_t>(ws, W.fh);
+        fa.p2 = at<float>(ws, W.fp2);
+        fa.out = static_cast<uint16_t*>(out);
+        fa.flags = P->d_flags;
+        fa.ucnt = P->d_ucnt;
+        fa.hflag = P->d_hflag;
+        fa.err = P->d_error;
+        fa.num_pages = P->num_pages;
+        fa.p1_base1 = F.u1_shared + grid;
+        // the shared chunks' gate/up (streamed before routing is known) goes to the first g0
+        // CTAs, with pieces of at least 8 k-blocks each
+        {
+            const int64_t i0 = (int64_t)D.num_shared_chunks * (D.f / 64) * (D.d / 64);
+            const int64_t g0 = i0 / 8;
+            fa.g0 = (int)(g0 < 1 ? 1 : (g0 > grid ? grid : g0));
+        }
+        fa.T = T;
+        fa.E = D.num_experts;
+        fa.k = D.top_k;
+        fa.S = D.num_shared_chunks;
+        fa.renorm = D.renormalize;
+        fa.d = D.d;
+        fa.f = D.f;
+        fa.slots_per_buffer = D.slots_per_buffer;
+        fa.have_buf0 = P->buf[0] != nullptr;
+        fa.have_buf1 = P->buf[1] != nullptr;
+        fa.contig = contig ? 1 : 0;
+        fa.epl = 1;
+        while (32 * fa.epl < D.num_experts) fa.epl <<= 1;
+        PMOE_CUDA(mark(P, 0, stream), "profile event");
+        PMOE_CUDA(launch_fused_decode(fx, fh, P->tm_rows_d64, P->tm_rows_f, fa, F.bn, grid, stream),
+                  "fused decode");
+        PMOE_CUDA(mark(P, 1, stream), "profile event");
+        P->last_path = path;
+        P->last_kernels = 1;
+        P->last_launches = 1;
+        return PMOE_OK;
     }
 
     ResolveArgs rs{};
@@ -351,8 +450,17 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
     P->path = PMOE_PATH_AUTO;
     cudaError_t e = cudaGetDevice(&P->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
-    if (e == cudaSuccess) e = cudaMalloc(&P->d_error, sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaMemset(P->d_error, 0, sizeof(int32_t));
+    // one allocation of device words: the error word, the fused kernel's barrier words and tiles
+    P->words_bytes = plan_words_bytes(*desc);
+    if (e == cudaSuccess) e = cudaMalloc(&P->d_error, P->words_bytes);
+    if (e == cudaSuccess) e = cudaMemset(P->d_error, 0, P->words_bytes);
+    if (e == cudaSuccess) {
+        char* base = reinterpret_cast<char*>(P->d_error);
+        const size_t tiles = (size_t)(desc->num_experts + desc->num_shared_chunks) * (desc->f / 64);
+        P->d_flags = reinterpret_cast<uint32_t*>(base + 1024);
+        P->d_ucnt = reinterpret_cast<unsigned long long*>(base + 2048);
+        P->d_hflag = reinterpret_cast<uint32_t*>(base + 2048 + 8 * tiles);
+    }
     if (e != cudaSuccess) {
         if (P->d_error) cudaFree(P->d_error);
         delete P;
@@ -390,7 +498,7 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan) {
 }
 
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
-    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_TC2)
+    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_FUSED)
         return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
     reinterpret_cast<Plan*>(plan)->path = path;
     return PMOE_OK;
@@ -488,7 +596,9 @@ pmoe_status pmoe_get_device_error(pmoe_plan_t plan, int32_t clear, int32_t* code
     PMOE_CUDA(cudaMemcpyAsync(&v, P->d_error, sizeof v, cudaMemcpyDeviceToHost, s), "read error word");
     PMOE_CUDA(cudaStreamSynchronize(s), "sync");
     if (clear) {
-        PMOE_CUDA(cudaMemsetAsync(P->d_error, 0, sizeof(int32_t), s), "clear error word");
+        // also resets the fused kernel's barrier and tile words, which a kernel that timed out
+        // may leave behind
+        PMOE_CUDA(cudaMemsetAsync(P->d_error, 0, P->words_bytes, s), "clear error word");
         PMOE_CUDA(cudaStreamSynchronize(s), "sync");
     }
     *code = v;

@@ -17,6 +17,8 @@ constexpr int kTcBlockM = 128;          // tensor-core path: rows per sorted blo
 constexpr int kTcPairBlockM = 256;      // CTA-pair tensor-core path: rows per sorted block
 constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorted block (max)
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
+constexpr int kFusedMaxTokens = 32;     // fused decode kernel: tokens per call (MMA N <= 32)
+constexpr int kFusedMaxGrid = 256;      // fused decode kernel: CTAs (one per SM)
 
 // Where one expert matrix lives: map 0 = pool, 1 = load buffer 0, 2 = load buffer 1; `page` is
 // the page index within that map (for a buffer, 3 * slot + matrix).  map < 0: invalid.
@@ -28,6 +30,7 @@ struct ExpertLoc {
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
     size_t ids, w, sorted, bexp, inv, meta, loc, part, pairs, singles, x, h, y, total;
+    size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
     int64_t nblk_max;    // upper bound on sorted blocks
@@ -44,6 +47,10 @@ struct Plan {
     int64_t num_pages;
     const void* buf[2];
     int32_t* d_error;    // device error word
+    uint32_t* d_flags;   // grid-barrier words of the fused decode kernel (one per CTA)
+    unsigned long long* d_ucnt;   // its gate/up tile counters, (E+S)*f/64 of them
+    uint32_t* d_hflag;            // its gate/up tile ready words, (E+S)*f/64 of them
+    size_t words_bytes;           // bytes of the plan's device words (error word onwards)
     int device;
     int path;            // pmoe_path
     bool have_tmaps;
@@ -187,6 +194,31 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
                               void* out, int f, int d, int64_t npairs_max, int num_sms,
                               int32_t* err, cudaStream_t s);
+
+// Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
+// tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.
+struct FusedArgs {
+    const float* logits;        // [T][E]
+    const int32_t* page_table;  // [E+S][3]
+    const int32_t* buf_slot;    // [E]
+    float* p1;                  // gate/up partials: [pieces][bn][128] fp32
+    uint16_t* h;                // [A_max * bn][f] bf16
+    float* p2;                  // down partials: [pieces][bn][128] fp32
+    uint16_t* out;              // [T][d] bf16
+    uint32_t* flags;            // grid-barrier words, one per CTA (plan-owned)
+    unsigned long long* ucnt;   // per gate/up tile: (epoch << 32 | pieces done) (plan-owned)
+    uint32_t* hflag;            // per gate/up tile: epoch once its h is written (plan-owned)
+    int32_t* err;
+    int64_t num_pages;
+    int64_t p1_base1;           // first piece slot of the routed gate/up space
+    int g0;                     // CTAs that share the shared chunks' gate/up (1..grid)
+    int T, E, k, S, renorm, d, f;
+    int slots_per_buffer, have_buf0, have_buf1, contig;
+    int epl;                    // logits per lane in routing: 1, 2, 4, ..., 32 (E <= 32 * epl)
+};
+cudaError_t launch_fused_decode(const CUtensorMap& xmap, const CUtensorMap& hmap,
+                                const CUtensorMap* w64, const CUtensorMap* wf, const FusedArgs& a,
+                                int bn, int grid, cudaStream_t s);
 
 // Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials,
 // mode 3 gate/up with 64+64-row stacked tiles (bn <= 32; weight maps with 64-row boxes).

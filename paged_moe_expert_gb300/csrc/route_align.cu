@@ -8,77 +8,9 @@
 #include <math.h>
 
 #include "pmoe_internal.cuh"
+#include "route_common.cuh"
 
 namespace pmoe {
-
-// ---------------------------------------------------------------------------------------------
-// Routing: one warp per token.  Lane l holds logits l, l+32, l+64, ... (coalesced loads).  k
-// rounds of a warp argmax over the untaken experts, ordered by (value desc, id asc); softmax
-// over all E with the top-1 value as the max; optional renormalisation of the k weights.
-// ---------------------------------------------------------------------------------------------
-template <int EPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int k, int renorm,
-                                            int lane, int32_t* __restrict__ ids_out,
-                                            float* __restrict__ w_out) {
-    float v[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? lg[e] : -INFINITY;
-    }
-    uint32_t taken = 0;
-    int sel_id[kMaxTopK];
-    float sel_v[kMaxTopK];
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        if (j >= k) break;
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !(taken >> i & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
-                bv = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        sel_id[j] = bi;
-        sel_v[j] = bv;
-    }
-    const float mx = sel_v[0];
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i)
-        if (lane + 32 * i < E) s += expf(v[i] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    float wsel[kMaxTopK];
-    float wsum = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        if (j >= k) break;
-        wsel[j] = expf(sel_v[j] - mx) / s;
-        wsum += wsel[j];
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        if (j >= k) break;
-        if (lane == j) {
-            ids_out[j] = sel_id[j];
-            w_out[j] = renorm ? wsel[j] / wsum : wsel[j];
-        }
-    }
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(128) route_kernel(const float* __restrict__ logits, int T, int E,

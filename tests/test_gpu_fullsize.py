@@ -25,16 +25,20 @@ def weights(name):
     return _W[name]
 
 
-CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 128), ("qwen15", 1024), ("qwen15", 4096),
-         ("mixtral", 1), ("mixtral", 32), ("mixtral", 512), ("mixtral", 2048),
-         ("qwen3next", 1), ("qwen3next", 64), ("qwen3next", 256), ("qwen3next", 4096)]
+CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 32), ("qwen15", 128), ("qwen15", 1024),
+         ("qwen15", 4096), ("mixtral", 1), ("mixtral", 32), ("mixtral", 512), ("mixtral", 2048),
+         ("qwen3next", 1), ("qwen3next", 16), ("qwen3next", 64), ("qwen3next", 256),
+         ("qwen3next", 4096)]
 
 
 @pytest.mark.parametrize("name,T", CASES)
-@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM], ids=["auto", "stream"])
+@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM, pm.PATH_TC_DECODE],
+                         ids=["auto", "stream", "tc_decode"])
 def test_full_size_sampled(name, T, path):
     if path == pm.PATH_STREAM and T > 16:
         pytest.skip("the weight-streaming kernels serve decode sizes")
+    if path == pm.PATH_TC_DECODE and T > 32:
+        pytest.skip("covered by the automatic path above 32 tokens")
     cfg = syn.CONFIGS[name]
     L = setup_layer(cfg, T, weights=weights(name))
     L.plan.set_path(path)
@@ -48,13 +52,14 @@ def test_full_size_sampled(name, T, path):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=3e-5, atol=1e-7)
     p2 = 1 << max(0, (T - 1).bit_length())            # next power of two >= T
     bm = {pm.PATH_TC: 128, pm.PATH_TC2: 128, pm.PATH_TC_DECODE: min(128, max(16, p2)),
-          pm.PATH_STREAM: min(16, p2)}[path]
-    s, b, inv, npad = pm.align(ids, cfg.E, cfg.S, bm)
-    ref_al = oracle.align(rids, cfg.E, cfg.S, bm)
-    n = int(npad.item())
-    assert n == ref_al["n_padded"]
-    assert np.array_equal(s[:n].cpu().numpy(), ref_al["sorted_ids"])
-    assert np.array_equal(inv.cpu().numpy(), ref_al["inv"])
+          pm.PATH_STREAM: min(16, p2), pm.PATH_FUSED: None}[path]
+    if bm is not None:   # the fused decode kernel routes in place and needs no sort
+        s, b, inv, npad = pm.align(ids, cfg.E, cfg.S, bm)
+        ref_al = oracle.align(rids, cfg.E, cfg.S, bm)
+        n = int(npad.item())
+        assert n == ref_al["n_padded"]
+        assert np.array_equal(s[:n].cpu().numpy(), ref_al["sorted_ids"])
+        assert np.array_equal(inv.cpu().numpy(), ref_al["inv"])
     # sampled tokens through the oracle
     rng = np.random.default_rng(T)
     rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=min(T, 6), replace=False)]))

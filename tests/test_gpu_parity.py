@@ -74,14 +74,19 @@ SMALL = [
 ]
 
 
-PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2]
-PATH_IDS = ["stream", "tc", "tc_decode", "tc2"]
+PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED]
+PATH_IDS = ["stream", "tc", "tc_decode", "tc2", "fused"]
+FUSED_MAX_T = 32
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-@pytest.mark.parametrize("T", [1, 3, 16, 37, 128, 300])
+@pytest.mark.parametrize("T", [1, 3, 16, 17, 32, 37, 128, 300])
 def test_forward_matches_oracle(cfg, T, path):
+    if path == pm.PATH_FUSED and T > FUSED_MAX_T:
+        pytest.skip("the fused decode kernel takes at most 32 tokens")
+    if path != pm.PATH_FUSED and T in (17, 32):
+        pytest.skip("token counts that only change the fused kernel's tile width")
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
     out = L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
@@ -97,7 +102,7 @@ def test_output_independent_of_placement(path):
     cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
                             num_pages=60)
     w = syn.make_weights(cfg)
-    T = 29
+    T = 29   # <= 32: every path serves it
     outs = []
     for pseed, bidx, nb in [(1, 0, 4), (2, 0, 4), (3, 1, 4), (4, 1, 6), (5, 0, 0)]:
         L = setup_layer(cfg, T, placement_seed=pseed, buffer_index=bidx, n_buffered=nb, weights=w)
@@ -144,8 +149,10 @@ def test_invalid_arguments_rejected():
 
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
-    # tiny: E=8, k=2 -> T*k/E = T/4: small-batch kernels up to T=768, pairs from T=1536
-    for T, want in [(1, pm.PATH_TC_DECODE), (16, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
+    # up to 32 tokens the fused decode kernel; then by T*k/E (tiny: E=8, k=2 -> T/4): small-batch
+    # kernels up to T=768, pairs from T=1536
+    for T, want in [(1, pm.PATH_FUSED), (16, pm.PATH_FUSED), (32, pm.PATH_FUSED),
+                    (33, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
                     (768, pm.PATH_TC_DECODE), (769, pm.PATH_TC), (1535, pm.PATH_TC),
                     (1536, pm.PATH_TC2), (4096, pm.PATH_TC2)]:
         L = setup_layer(cfg, T)
@@ -159,6 +166,8 @@ def test_paths_agree(T):
     L = setup_layer(cfg, T)
     outs = []
     for path in PATHS:
+        if path == pm.PATH_FUSED and T > FUSED_MAX_T:
+            continue
         L.plan.set_path(path)
         outs.append(out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)))
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
@@ -169,9 +178,10 @@ def test_paths_agree(T):
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_forward_replays_from_a_cuda_graph(path):
     cfg = syn.custom_config("graph", d=256, f=256, E=6, k=2, S=1, n_buffered=2)
-    L = setup_layer(cfg, 40)
+    T = 24 if path == pm.PATH_FUSED else 40
+    L = setup_layer(cfg, T)
     L.plan.set_path(path)
-    ws = pm.alloc_workspace(L.desc, 40)
+    ws = pm.alloc_workspace(L.desc, T)
     out = torch.empty_like(L.hidden)
     run = lambda: L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, out=out, workspace=ws)  # noqa: E731
     run()
@@ -191,3 +201,31 @@ def test_forward_replays_from_a_cuda_graph(path):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(out_bits(out), eager)
+
+
+def test_fused_rejects_more_than_32_tokens():
+    cfg = syn.CONFIGS["tiny"]
+    L = setup_layer(cfg, 33)
+    L.plan.set_path(pm.PATH_FUSED)
+    with pytest.raises(pm.PmoeError) as ei:
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
+    assert ei.value.status == pm._lib.ERR_UNSUPPORTED
+
+
+def test_fused_back_to_back_calls_reuse_the_grid_barrier():
+    """Many fused calls in a row on one stream (each passes three grid barriers through the plan's
+    words) stay bit-identical, with no error raised."""
+    cfg = syn.custom_config("repeat", d=256, f=384, E=16, k=4, S=2, n_buffered=3)
+    L = setup_layer(cfg, 9)
+    L.plan.set_path(pm.PATH_FUSED)
+    ws = pm.alloc_workspace(L.desc, 9)
+    outs = [torch.empty_like(L.hidden) for _ in range(20)]
+    for o in outs:
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    assert L.plan.device_error() == 0
+    first = out_bits(outs[0])
+    for o in outs[1:]:
+        assert np.array_equal(out_bits(o), first)
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
+    assert_close(first, ref["out_bf16"])
