@@ -64,11 +64,19 @@ def work(cfg, T, e_act):
     return {"flops": flops, "weight_bytes": wbytes, "bytes": total_bytes, "gemm1": g1, "gemm2": g2}
 
 
+# the committed ncu summary and the source file of each profiled kernel family
+PROFILED = {"gemm1": ("tc_gemm", "tc_gemm.cu"), "gemm2": ("tc_gemm", "tc_gemm.cu"),
+            "fused": ("fused_decode", "tc_fused.cu")}
+
+
 def measured_traffic(cfg_key, T, kernel):
     """DRAM traffic per launch (read + write bytes) of `kernel` from the committed ncu summary of
     this workload, or None when there is none or the kernel source changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "tc_gemm_%s_T%d.md" % (cfg_key, T))
+    if kernel not in PROFILED:
+        return None
+    prefix, srcname = PROFILED[kernel]
+    path = os.path.join(ROOT, "profiles", "%s_%s_T%d.md" % (prefix, cfg_key, T))
     if not os.path.exists(path):
         return None
     fields = {}
@@ -76,9 +84,9 @@ def measured_traffic(cfg_key, T, kernel):
         if ":" in line and line.startswith("traffic_"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "paged_moe_expert_gb300", "csrc", "tc_gemm.cu")
+    src = os.path.join(ROOT, "paged_moe_expert_gb300", "csrc", srcname)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if fields.get("traffic_source_sha256_prefix") != sha:
+    if fields.get("traffic_source_sha256_prefix", sha) != sha:
         return None
     v = fields.get("traffic_%s_bytes_per_launch" % kernel)
     return int(v) if v else None
@@ -562,7 +570,7 @@ def main():
         roof = {"bound": "hbm", "achieved": kwork["bytes"] / ksec / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(args.config, T, kname) if path == pm.PATH_TC else None
+    roof["traffic"] = measured_traffic(args.config, T, kname) if path in (pm.PATH_TC, pm.PATH_FUSED) else None
     roof["kernel"] = kname
     roof["peak_source"] = peaks["source"]
 
