@@ -330,18 +330,28 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
                                      at<int32_t>(ws, W.part), sorted, bexp, inv, meta, &rs, stream),
                   "align");
     }
+    // With a separate row gather, the gate/up GEMMs read the shared chunks' rows (every token, in
+    // order) from hidden itself and the gather copies routed pairs only.
+    SharedRows sh{};
+    CUtensorMap hidmap;
     if (tc_family && !gather_in_prep) {
+        sh.direct = 1;
+        sh.E = D.num_experts;
+        sh.S = D.num_shared_chunks;
+        sh.rows = (int)((T + bm - 1) / bm * bm);
+        if (!encode_rows_map(&hidmap, hidden, T, D.d, path == PMOE_PATH_TC_DECODE ? sw.bn : kTcBlockM))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_gather_pairs(hid, inv, T, D.top_k, D.num_shared_chunks, D.d, x, stream),
-                  "gather");
+        PMOE_CUDA(launch_gather_pairs(hid, inv, T, D.top_k, 0, D.d, x, stream), "gather");
     }
+    const CUtensorMap* hidp = sh.direct ? &hidmap : nullptr;
     const int64_t nblk = (W.np + bm - 1) / bm + (ES < W.np ? ES : W.np);
     int64_t ystride;
     int splits;
     if (path == PMOE_PATH_TC) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
-                                 P->num_sms, P->d_error, stream), "gate/up gemm");
+                                 P->num_sms, P->d_error, stream, nullptr, 0, hidp, sh), "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
                                  P->num_sms, P->d_error, stream), "down gemm");
@@ -352,11 +362,11 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         const int64_t npairs_max = nblk / 2 + 1, nsingles_max = ES < nblk ? ES : nblk;
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, pair_list, meta, loc, h,
-                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
+                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream, hidp, sh),
                   "gate/up gemm (pairs)");
         PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d,
                                  nsingles_max, P->num_sms, P->d_error, stream, single_list,
-                                 kMetaSingles), "gate/up gemm (singles)");
+                                 kMetaSingles, hidp, sh), "gate/up gemm (singles)");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, pair_list, meta, loc, y,
                                     D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
@@ -375,7 +385,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         PMOE_CUDA(launch_tc_swap(stacked ? 3 : 1, contig, sw.bn, xmap,
                                  stacked ? P->tm_rows_d64 : P->tm_rows_d, sorted, T, D.top_k,
                                  D.num_shared_chunks, bexp, meta, loc, h, D.f, D.d, 1, 0, nblk,
-                                 P->num_sms, P->d_error, gather_in_prep ? 0 : 1, stream),
+                                 P->num_sms, P->d_error, gather_in_prep ? 0 : 1, stream, hidp, sh),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_swap(2, contig, sw.bn, hmap, P->tm_rows_f, sorted, T, D.top_k,

@@ -177,6 +177,21 @@ cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float*
                            const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
                            cudaStream_t s);
 
+// The blocks of the shared-expert chunks hold every token in order (chunk s, sorted row
+// start_s + t is token t), and those chunks are the last experts of the sorted order.  With
+// `direct` set the gate/up GEMMs load those rows from hidden itself, so the row gather copies
+// routed pairs only.
+struct SharedRows {
+    int direct;   // 1: shared-chunk blocks read hidden
+    int E, S;     // routed experts, shared chunks
+    int rows;     // sorted rows of one shared chunk: T rounded up to the block size
+};
+
+// Row of hidden that sorted row `srow` of expert e (>= E) holds, given the padded row count.
+__device__ __forceinline__ int shared_token_row(const SharedRows& sh, int e, int srow, int npad) {
+    return srow - (npad - (sh.S - (e - sh.E)) * sh.rows);
+}
+
 // Tensor-core path (tc_gemm.cu)
 bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                      int box_rows = 128);
@@ -185,7 +200,8 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s, const int32_t* list = nullptr, int list_meta = 0);
+                           cudaStream_t s, const int32_t* list = nullptr, int list_meta = 0,
+                           const CUtensorMap* hid = nullptr, SharedRows sh = SharedRows{});
 
 // CTA-pair tensor-core path (tc_gemm2sm.cu): pairs of consecutive 128-row blocks of one expert
 // from pair_list (count meta[kMetaPairs]); mode 1 gate/up -> h, 2 down -> y.
@@ -193,7 +209,8 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
                               const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
                               void* out, int f, int d, int64_t npairs_max, int num_sms,
-                              int32_t* err, cudaStream_t s);
+                              int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
+                              SharedRows sh = SharedRows{});
 
 // Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
 // tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.
@@ -227,6 +244,7 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
                            int S, const int32_t* block_expert, const int32_t* meta,
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
-                           int early, cudaStream_t s);
+                           int early, cudaStream_t s, const CUtensorMap* hid = nullptr,
+                           SharedRows sh = SharedRows{});
 
 }  // namespace pmoe

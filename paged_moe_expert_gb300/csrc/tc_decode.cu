@@ -74,11 +74,13 @@ struct SwapArgs {
     int64_t ystride;      // rows per split of y
     int early;            // 1: the sort's outputs are complete at launch (see the priming below)
     int32_t* err;
+    SharedRows sh;        // gate/up: shared-chunk blocks straight from hidden
 };
 
 struct SwapMaps {
     CUtensorMap act;      // X_sorted [rows][d] or h [rows][f], boxes of BN rows
     CUtensorMap w[3];     // weights of pool / load buffer 0 / load buffer 1, boxes of 128 rows
+    CUtensorMap hid;      // hidden [T][d], boxes of BN rows, when args.sh.direct
 };
 
 template <bool kContig>
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
             int step = 0;   // (tile, k-block) steps issued; the first `primed` have their weights
+            const int npad = args.meta[kMetaNPadded];
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 int b, wt, sp, kb0, kb1;
                 decode_tile(t, b, wt, sp, kb0, kb1);
@@ -219,6 +222,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rows_per_page = C::kGateFamily ? args.f : args.d;
                 const int row0 = l0.page * rows_per_page + wt * C::WR;
                 const int row1 = l1.page * rows_per_page + wt * C::WR;
+                // the block's token rows: sorted rows, or hidden itself for a shared-chunk block
+                const CUtensorMap* am = &maps.act;
+                int arow = b * BN;
+                if (C::kGateFamily && args.sh.direct) {
+                    const int e = args.block_expert[b];
+                    if (e >= args.sh.E) {
+                        am = &maps.hid;
+                        arow = shared_token_row(args.sh, e, b * BN, npad);
+                    }
+                }
                 for (int kb = kb0; kb < kb1; ++kb, ++step) {
                     const uint32_t fb = full_bar(stage);
                     const uint32_t sa = sbase + stage * C::STAGE_BYTES;
@@ -227,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
                         load_weights(sa, fb, kb, l0, l1, row0, row1);
                     }
-                    tma_load_2d(sa + C::W_STAGE, &maps.act, fb, kb * BK, b * BN);
+                    tma_load_2d(sa + C::W_STAGE, am, fb, kb * BK, arow);
                     pend_phase[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -395,10 +408,11 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
                            int S, const int32_t* block_expert, const int32_t* meta,
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
-                           int early, cudaStream_t s) {
+                           int early, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
     SwapMaps maps;
     maps.act = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    maps.hid = hid ? *hid : act;
     SwapArgs a{};
     a.sorted_ids = sorted_ids;
     a.T = T;
@@ -413,6 +427,7 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
     a.err = err;
     a.ystride = ystride;
     a.early = early;
+    a.sh = hid ? sh : SharedRows{};
     if (mode == kGateUp || mode == kGateUpStacked) {
         a.k_blocks = d / BK;
         a.w_tiles = f / (mode == kGateUp ? WROWS : 64);

@@ -54,11 +54,13 @@ struct TcArgs {
     int32_t* err;
     const int32_t* list;   // NULL: every block; else the blocks list[0 .. meta[list_meta])
     int list_meta;
+    SharedRows sh;         // gate/up: shared-chunk blocks straight from hidden
 };
 
 struct TcMaps {
     CUtensorMap a;      // activations: X_sorted [cap][d] or h [cap][f]
     CUtensorMap w[3];   // weights of pool / load buffer 0 / load buffer 1
+    CUtensorMap hid;    // hidden [T][d] (128-row boxes), when args.sh.direct
 };
 
 template <bool kContig>
@@ -143,12 +145,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pend_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
+            const int npad = args.meta[kMetaNPadded];
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const int mb = block_of(t), nt = (int)(t % args.n_tiles);
                 ExpertLoc l0, l1;
                 if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
                 const CUtensorMap* w0 = &maps.w[l0.map];
                 const CUtensorMap* w1 = &maps.w[l1.map];
+                // the tile's token rows: sorted rows, or hidden itself for a shared-chunk block
+                const CUtensorMap* am = &maps.a;
+                int arow = mb * BM;
+                if (kMode == kGateUp && args.sh.direct) {
+                    const int e = args.block_expert[mb];
+                    if (e >= args.sh.E) {
+                        am = &maps.hid;
+                        arow = shared_token_row(args.sh, e, mb * BM, npad);
+                    }
+                }
                 int row0, row1;
                 if (kMode == kGateUp) {
                     row0 = l0.page * args.f + nt * 128;   // W1 rows of output columns n0..n0+127
@@ -162,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
-                    tma_load_2d(sa, &maps.a, fb, kb * BK, mb * BM);
+                    tma_load_2d(sa, am, fb, kb * BK, arow);
                     tma_load_2d(sa + A_BYTES, w0, fb, kb * BK, row0);
                     tma_load_2d(sa + A_BYTES + B_HALF, w1, fb, kb * BK, row1);
                     pend_phase[stage] = (int)phase;
@@ -328,10 +341,12 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s, const int32_t* list, int list_meta) {
+                           cudaStream_t s, const int32_t* list, int list_meta,
+                           const CUtensorMap* hid, SharedRows sh) {
     TcMaps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    maps.hid = hid ? *hid : act;
     TcArgs a{};
     a.block_expert = block_expert;
     a.meta = meta;
@@ -342,6 +357,7 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
     a.err = err;
     a.list = list;
     a.list_meta = list_meta;
+    a.sh = hid ? sh : SharedRows{};
     if (mode == kGateUp) {
         a.k_blocks = d / BK;
         a.n_tiles = f / 128;

@@ -53,11 +53,13 @@ struct Tc2Args {
     int k_blocks;
     int n_tiles;
     int32_t* err;
+    SharedRows sh;      // gate/up: shared-chunk blocks straight from hidden
 };
 
 struct Tc2Maps {
     CUtensorMap a;      // X_sorted [cap][d] or h [cap][f], 128-row boxes
     CUtensorMap w[3];   // pool / buffer 0 / buffer 1 weight views, 128-row boxes
+    CUtensorMap hid;    // hidden [T][d], 128-row boxes, when args.sh.direct
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -189,11 +191,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int pend_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
             bool ok = true;
+            const int npad = args.meta[kMetaNPadded];
             for (int64_t t = cid; t < ntiles && ok; t += ncl) {
                 const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
                 ExpertLoc l0, l1;
                 if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
-                const int row_a = (pb + (int)rank) * 128;
+                // this CTA's token rows: sorted rows, or hidden itself for a shared-chunk block
+                const CUtensorMap* am = &maps.a;
+                int row_a = (pb + (int)rank) * 128;
+                if (kMode == kGateUp && args.sh.direct) {
+                    const int e = args.block_expert[pb];
+                    if (e >= args.sh.E) {
+                        am = &maps.hid;
+                        row_a = shared_token_row(args.sh, e, row_a, npad);
+                    }
+                }
                 const CUtensorMap* wm;
                 int row_b;
                 if (kMode == kGateUp) {
@@ -208,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb_leader = map_to_rank(full_bar(stage), 0);
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
-                    tma_load_2d_pair(sa, &maps.a, fb_leader, kb * BK, row_a);
+                    tma_load_2d_pair(sa, am, fb_leader, kb * BK, row_a);
                     tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
                     pend_phase[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -337,10 +349,11 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
                               const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
                               void* out, int f, int d, int64_t npairs_max, int num_sms,
-                              int32_t* err, cudaStream_t s) {
+                              int32_t* err, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
     Tc2Maps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    maps.hid = hid ? *hid : act;
     Tc2Args a{};
     a.block_expert = block_expert;
     a.pair_list = pair_list;
@@ -350,6 +363,7 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
     a.f = f;
     a.d = d;
     a.err = err;
+    a.sh = hid ? sh : SharedRows{};
     if (mode == kGateUp) {
         a.k_blocks = d / BK;
         a.n_tiles = f / 128;
