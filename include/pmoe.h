@@ -30,7 +30,9 @@
  *              chunk s is the expert E + s with weight 1 on every token.
  *   ownership  the caller owns every buffer: pool, load buffers, tables, activations, outputs,
  *              workspace, pinned host memory, streams and events.  The library allocates only
- *              in pmoe_plan_create (the plan object and one device error word) and frees it in
+ *              in pmoe_plan_create (the plan object and one block of device words: the error
+ *              word and the fused decode kernel's barrier words, tile counters and ready words,
+ *              2 KB + 12 bytes per f/64 columns of every expert) and frees it in
  *              pmoe_plan_destroy.  Forward calls allocate nothing and never synchronise the host.
  *   errors     argument checks are synchronous and return a status.  Table contents are checked
  *              on the device: an out-of-range page or slot of an expert that the routing
