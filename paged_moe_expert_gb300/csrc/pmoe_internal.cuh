@@ -73,6 +73,15 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// SiLU(g) * u = g / (1 + e^-g) * u with the hardware exponential and reciprocal: no
+// data-dependent slow path (the pad rows of a sorted block may hold any bits, and the IEEE
+// divide's slow path on their overflowing values cost a gate/up epilogue three times its time);
+// the error is a few fp32 ulps, far below the bf16 rounding of h.  For g -> -inf the divisor
+// overflows and the quotient is 0, the limit of SiLU.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.f + __expf(-g)) * u;
+}
+
 __device__ __forceinline__ void raise_error(int32_t* err, int32_t code) {
     if (err) atomicCAS(err, 0, code);
 }

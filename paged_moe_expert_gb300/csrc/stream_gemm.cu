@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) stream_gemm1_kernel(
                 const float gs = warp_sum(g[m]);
                 const float us = warp_sum(u[m]);
                 if (lane == m % 32) {
-                    const float a = gs / (1.f + expf(-gs)) * us;
+                    const float a = silu_mul(gs, us);
                     h[(int64_t)(b * MT + m) * f + n] = f32_to_bf16_bits(a);
                 }
             }

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float a = g[j] / (1.f + expf(-g[j])) * u[j];
+                        const float a = silu_mul(g[j], u[j]);
                         h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(a);
                     }
                 }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const float g = v[j], u = xch[(c0 + j) * 64 + r];
-                            h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(g / (1.f + expf(-g)) * u);
+                            h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(silu_mul(g, u));
                         }
                     }
                     asm volatile("bar.sync 1, 128;" ::: "memory");

@@ -700,8 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             if (nn[q] < 0) break;
-                            const float h0 = g[q].x / (1.f + expf(-g[q].x)) * up[q].x;
-                            const float h1 = g[q].y / (1.f + expf(-g[q].y)) * up[q].y;
+                            const float h0 = silu_mul(g[q].x, up[q].x);
+                            const float h1 = silu_mul(g[q].y, up[q].y);
                             reinterpret_cast<uint32_t*>(args.h + ((int64_t)a * BN + nn[q]) * args.f + ft * 64)[lane] =
                                 pack_bf16(h0, h1);
                         }

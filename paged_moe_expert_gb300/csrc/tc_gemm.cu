@@ -43,6 +43,28 @@ constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
 enum { kGateUp = 1, kDown = 2 };
 
+// Per-tile time stamps for performance work (compiled in only with -DPMOE_GEMM_TRACE): for each
+// tile of the last launch of each mode, [0] globaltimer when its accumulator was free, [1] when
+// its first k-block had landed, [2] after its last MMA was issued, [3] SM cycles the MMA issuer
+// waited for loads, [4] globaltimer when the epilogue released the accumulator, [5] SM id,
+// [6] globaltimer when the epilogue saw the accumulator full, [7] globaltimer when the MMA issuer
+// began waiting for the accumulator.
+#ifdef PMOE_GEMM_TRACE
+constexpr int kTraceTiles = 8192;
+constexpr int kTraceWords = 8;
+__device__ unsigned long long g_gemm_trace[2][kTraceTiles][kTraceWords];
+#define GTRACE(t, i, v) \
+    do { if ((t) < kTraceTiles) g_gemm_trace[kMode - 1][(t)][(i)] = (unsigned long long)(v); } while (0)
+#else
+#define GTRACE(t, i, v) ((void)0)
+#endif
+
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
 struct TcArgs {
     const int32_t* block_expert;
     const int32_t* meta;
@@ -201,11 +223,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int mb = block_of(t);
                 ExpertLoc l0, l1;
                 if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
+                GTRACE(t, 7, globaltimer());
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
                 tc_fence_after();
+                GTRACE(t, 0, globaltimer());
+#ifdef PMOE_GEMM_TRACE
+                long long waited = 0;
+#endif
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
+#ifdef PMOE_GEMM_TRACE
+                    const long long c0 = clock64();
+#endif
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) { ok = false; break; }
+#ifdef PMOE_GEMM_TRACE
+                    waited += clock64() - c0;
+                    if (kb == 0) GTRACE(t, 1, globaltimer());
+#endif
                     tc_fence_after();
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
                     const uint64_t adesc = smem_desc(sa);
@@ -221,6 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit(tfull_bar(acc));
+                GTRACE(t, 2, globaltimer());
+                GTRACE(t, 3, waited);
+                GTRACE(t, 5, sm_id());
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
         }
@@ -236,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
             tc_fence_after();
+            if (lane == 0 && quad == 0) GTRACE(t, 6, globaltimer());
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
             const int64_t grow = (int64_t)mb * BM + row;
             if (kMode == kGateUp) {
@@ -249,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t p[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float a0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
-                        const float a1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                        const float a0 = silu_mul(g[2 * i], u[2 * i]);
+                        const float a1 = silu_mul(g[2 * i + 1], u[2 * i + 1]);
                         p[i] = pack_bf16(a0, a1);
                     }
                     uint4* dst = reinterpret_cast<uint4*>(h + c0);
@@ -276,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0 && quad == 0) GTRACE(t, 4, globaltimer());
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
@@ -371,5 +410,17 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
         return contig ? launch_one<kGateUp, true>(maps, a, grid, s) : launch_one<kGateUp, false>(maps, a, grid, s);
     return contig ? launch_one<kDown, true>(maps, a, grid, s) : launch_one<kDown, false>(maps, a, grid, s);
 }
+
+#ifdef PMOE_GEMM_TRACE
+extern "C" int pmoe_gemm_trace_read(int mode, unsigned long long* host, int n) {
+    if (mode < 1 || mode > 2 || n > kTraceTiles * kTraceWords) return -1;
+    return (int)cudaMemcpyFromSymbol(host, g_gemm_trace, sizeof(unsigned long long) * n,
+                                     sizeof(unsigned long long) * kTraceTiles * kTraceWords * (mode - 1));
+}
+extern "C" int pmoe_gemm_trace_clear() {
+    static unsigned long long zeros[2 * kTraceTiles * kTraceWords];
+    return (int)cudaMemcpyToSymbol(g_gemm_trace, zeros, sizeof(zeros));
+}
+#endif
 
 }  // namespace pmoe

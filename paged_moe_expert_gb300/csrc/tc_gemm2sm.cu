@@ -288,8 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     uint32_t p[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float a0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
-                        const float a1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+                        const float a0 = silu_mul(g[2 * i], u[2 * i]);
+                        const float a1 = silu_mul(g[2 * i + 1], u[2 * i + 1]);
                         p[i] = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
                     }
                     uint4* dst = reinterpret_cast<uint4*>(h + c0);
