@@ -350,11 +350,12 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     int splits;
     if (path == PMOE_PATH_TC) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d, nblk,
-                                 P->num_sms, P->d_error, stream, nullptr, 0, hidp, sh), "gate/up gemm");
+        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, cap_tc, D.f, D.d,
+                                 nblk, P->num_sms, P->d_error, stream, nullptr, 0, hidp, sh),
+                  "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d, nblk,
-                                 P->num_sms, P->d_error, stream), "down gemm");
+        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, cap_tc, D.f, D.d,
+                                 nblk, P->num_sms, P->d_error, stream), "down gemm");
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC2) {
@@ -362,16 +363,16 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         const int64_t npairs_max = nblk / 2 + 1, nsingles_max = ES < nblk ? ES : nblk;
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, pair_list, meta, loc, h,
-                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream, hidp, sh),
+                                    cap_tc, D.f, D.d, npairs_max, P->num_sms, P->d_error, stream, hidp, sh),
                   "gate/up gemm (pairs)");
-        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, D.f, D.d,
+        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, cap_tc, D.f, D.d,
                                  nsingles_max, P->num_sms, P->d_error, stream, single_list,
                                  kMetaSingles, hidp, sh), "gate/up gemm (singles)");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, pair_list, meta, loc, y,
-                                    D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
+                                    cap_tc, D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
                   "down gemm (pairs)");
-        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, D.f, D.d,
+        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, cap_tc, D.f, D.d,
                                  nsingles_max, P->num_sms, P->d_error, stream, single_list,
                                  kMetaSingles), "down gemm (singles)");
         ystride = cap_tc;

@@ -204,20 +204,24 @@ __device__ __forceinline__ int shared_token_row(const SharedRows& sh, int e, int
 // Tensor-core path (tc_gemm.cu)
 bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                      int box_rows = 128);
-// mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32)
+// An fp32 row-major matrix [rows][cols] as a TMA map with 32 x 32 boxes and 128-byte swizzle
+// (the down GEMMs' epilogue stores of y).
+bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols);
+// mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32, out_rows rows)
 // list != NULL: only the blocks in list[0 .. meta[list_meta]) (single blocks of the pair path)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
-                           void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s, const int32_t* list = nullptr, int list_meta = 0,
-                           const CUtensorMap* hid = nullptr, SharedRows sh = SharedRows{});
+                           void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
+                           int32_t* err, cudaStream_t s, const int32_t* list = nullptr,
+                           int list_meta = 0, const CUtensorMap* hid = nullptr,
+                           SharedRows sh = SharedRows{});
 
 // CTA-pair tensor-core path (tc_gemm2sm.cu): pairs of consecutive 128-row blocks of one expert
 // from pair_list (count meta[kMetaPairs]); mode 1 gate/up -> h, 2 down -> y.
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
                               const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
-                              void* out, int f, int d, int64_t npairs_max, int num_sms,
+                              void* out, int64_t out_rows, int f, int d, int64_t npairs_max, int num_sms,
                               int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
                               SharedRows sh = SharedRows{});
 

@@ -90,6 +90,64 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// ---- tensor stores from shared memory (epilogues) ----
+
+// 2D tiled TMA store of a shared-memory box, tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most the most recent bulk group of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Waits until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Epilogue of an fp32 accumulator: this warp's 32 TMEM lanes (32 output rows) x 32 columns (lo:
+// the first 16, hi: the next 16) are
+// written to a 4 KB shared-memory box in the 128-byte swizzled layout (row r's 16-byte chunk j at
+// chunk j ^ (r mod 8), so the warp's stores hit every bank once per four wavefronts) and stored to
+// y[row0 .. row0+31][col0 .. col0+31] by one TMA store issued by lane 0.  `box` must be
+// 1024-byte aligned and the caller must alternate two boxes: before writing one, lane 0 waits
+// until only its latest store (from the other box) may still be reading shared memory.
+__device__ __forceinline__ void store_rows_f32x32(const CUtensorMap* ymap, uint32_t box, const float (&lo)[16],
+                                                  const float (&hi)[16], int lane, int col0, int row0) {
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+    const uint32_t rb = box + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4), lo[4 * j], lo[4 * j + 1], lo[4 * j + 2],
+                     lo[4 * j + 3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        st_shared_v4(rb + ((uint32_t)((j + 4) ^ (lane & 7)) << 4), hi[4 * j], hi[4 * j + 1],
+                     hi[4 * j + 2], hi[4 * j + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(ymap, box, col0, row0);
+        bulk_commit();
+    }
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

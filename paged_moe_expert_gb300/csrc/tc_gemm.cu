@@ -37,7 +37,11 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;          // 6 warps
 constexpr uint32_t kTmemCols = 512;    // two 256-column fp32 accumulators
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kYBox = 32 * 32 * 4;     // down epilogue: one 32-row x 32-column fp32 store box
+// ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
+// GEMM, two store boxes per epilogue warp
+template <int kMode>
+constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 1024 + (kMode == 2 ? 4 * 2 * kYBox : 0); }
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
@@ -83,6 +87,7 @@ struct TcMaps {
     CUtensorMap a;      // activations: X_sorted [cap][d] or h [cap][f]
     CUtensorMap w[3];   // weights of pool / load buffer 0 / load buffer 1
     CUtensorMap hid;    // hidden [T][d] (128-row boxes), when args.sh.direct
+    CUtensorMap y;      // down: y fp32 [cap][d], 32 x 32 boxes, 128-byte swizzle
 };
 
 template <bool kContig>
@@ -267,6 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        const uint32_t ybox = bar0 + 1024u + (uint32_t)(quad * 2 * kYBox);   // down: this warp's boxes
+        int ysel = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int mb = block_of(t), nt = (int)(t % args.n_tiles);
             ExpertLoc l0, l1;
@@ -296,19 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                 }
             } else {
-                float* y = static_cast<float*>(args.out) + grow * args.d;
+                // fp32 rows through shared memory and TMA stores: each store writes whole
+                // 128-byte lines instead of one 16-byte piece of 32 different rows
                 const int r0 = nt * BN;
+                const int yrow = mb * BM + quad * 32;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(taddr + c0, v);
+                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 32) {
+                    float lo[16], hi[16];
+                    tmem_ld16(taddr + c0, lo);
+                    tmem_ld16(taddr + c0 + 16, hi);
                     tmem_wait_ld();
-                    if (r0 + c0 < args.d) {
-                        float4* dst = reinterpret_cast<float4*>(y + r0 + c0);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    }
+                    store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                    ysel ^= 1;
                 }
             }
             tc_fence_before();
@@ -317,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && quad == 0) GTRACE(t, 4, globaltimer());
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (kMode == kDown && lane == 0) bulk_wait_all();   // stores done before the CTA exits
     }
 
     tc_fence_before();
@@ -354,11 +361,13 @@ cudaError_t launch_one(const TcMaps& maps, const TcArgs& a, int grid, cudaStream
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kMode, kContig>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_bytes<kMode>());
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_pdl(tc_gemm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), kSmemBytes, s, maps, a);
+    return launch_pdl(tc_gemm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), smem_bytes<kMode>(),
+                      s, maps, a);
 }
 
 }  // namespace
@@ -377,15 +386,31 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An fp32 row-major matrix [rows][cols] as a TMA map with 32 x 32 boxes (128-byte rows) and
+// 128-byte swizzle, for the epilogue stores of y.
+bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encoder();
+    if (!fn || !base || rows <= 0 || cols <= 0 || (cols * 4) % 16 != 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
-                           void* out, int f, int d, int64_t nblk_max, int num_sms, int32_t* err,
-                           cudaStream_t s, const int32_t* list, int list_meta,
+                           void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
+                           int32_t* err, cudaStream_t s, const int32_t* list, int list_meta,
                            const CUtensorMap* hid, SharedRows sh) {
     TcMaps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
     maps.hid = hid ? *hid : act;
+    maps.y = act;
+    if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
     TcArgs a{};
     a.block_expert = block_expert;
     a.meta = meta;

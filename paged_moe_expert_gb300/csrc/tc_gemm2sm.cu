@@ -38,7 +38,11 @@ constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int kYBox = 32 * 32 * 4;   // down epilogue: one 32-row x 32-column fp32 store box
+// ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
+// GEMM, two store boxes per epilogue warp
+template <int kMode>
+constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 1024 + (kMode == 2 ? 4 * 2 * kYBox : 0); }
 constexpr uint32_t kIdesc = idesc_bf16(256, BN);   // M = 256: 128 rows on each CTA
 
 enum { kGateUp = 1, kDown = 2 };
@@ -60,6 +64,7 @@ struct Tc2Maps {
     CUtensorMap a;      // X_sorted [cap][d] or h [cap][f], 128-row boxes
     CUtensorMap w[3];   // pool / buffer 0 / buffer 1 weight views, 128-row boxes
     CUtensorMap hid;    // hidden [T][d], 128-row boxes, when args.sh.direct
+    CUtensorMap y;      // down: y fp32 [cap][d], 32 x 32 boxes, 128-byte swizzle
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -269,6 +274,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        const uint32_t ybox = bar0 + 1024u + (uint32_t)(quad * 2 * kYBox);   // down: this warp's boxes
+        int ysel = 0;
         for (int64_t t = cid; t < ntiles; t += ncl) {
             const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
             ExpertLoc l0, l1;
@@ -297,19 +304,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                 }
             } else {
-                float* y = static_cast<float*>(args.out) + grow * args.d;
+                // fp32 rows through shared memory and TMA stores (whole 128-byte lines)
                 const int r0 = nt * BN;
+                const int yrow = (pb + (int)rank) * 128 + quad * 32;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(taddr + c0, v);
+                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 32) {
+                    float lo[16], hi[16];
+                    tmem_ld16(taddr + c0, lo);
+                    tmem_ld16(taddr + c0 + 16, hi);
                     tmem_wait_ld();
-                    if (r0 + c0 < args.d) {
-                        float4* dst = reinterpret_cast<float4*>(y + r0 + c0);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    }
+                    store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                    ysel ^= 1;
                 }
             }
             tc_fence_before();
@@ -317,6 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (kMode == kDown && lane == 0) bulk_wait_all();   // stores done before the CTA exits
     }
 
     tc_fence_before();
@@ -335,12 +341,13 @@ cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm2sm_kernel<kMode, kContig>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_bytes<kMode>());
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    return launch_pdl(tc_gemm2sm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), kSmemBytes, s,
-                      maps, a);
+    return launch_pdl(tc_gemm2sm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads),
+                      smem_bytes<kMode>(), s, maps, a);
 }
 
 }  // namespace
@@ -348,12 +355,15 @@ cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
                               const CUtensorMap* wmaps, const int32_t* block_expert,
                               const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
-                              void* out, int f, int d, int64_t npairs_max, int num_sms,
-                              int32_t* err, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
+                              void* out, int64_t out_rows, int f, int d, int64_t npairs_max,
+                              int num_sms, int32_t* err, cudaStream_t s, const CUtensorMap* hid,
+                              SharedRows sh) {
     Tc2Maps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
     maps.hid = hid ? *hid : act;
+    maps.y = act;
+    if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
     Tc2Args a{};
     a.block_expert = block_expert;
     a.pair_list = pair_list;
