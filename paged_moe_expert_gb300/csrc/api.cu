@@ -146,8 +146,7 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.meta = o;   o = align256(o + sizeof(int32_t) * kMetaCount);
     W.loc = o;    o = align256(o + sizeof(ExpertLoc) * ES * 3);
     W.part = o;   o = align256(o + align_part_bytes());
-    W.pairs = o;  o = align256(o + sizeof(int32_t) * (W.nblk_max / 2 + 1));
-    W.singles = o; o = align256(o + sizeof(int32_t) * (ES + 1));
+    W.units = o;  o = align256(o + sizeof(int32_t) * W.nblk_max);
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
@@ -306,12 +305,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
 
     const int bm = (path == PMOE_PATH_TC || path == PMOE_PATH_TC2) ? kTcBlockM
                  : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
-    int32_t* pair_list = at<int32_t>(ws, W.pairs);
-    int32_t* single_list = at<int32_t>(ws, W.singles);
-    if (path == PMOE_PATH_TC2) {
-        rs.pair_list = pair_list;
-        rs.single_list = single_list;
-    }
+    int32_t* units = at<int32_t>(ws, W.units);
+    if (path == PMOE_PATH_TC2) rs.units = units;
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
@@ -359,22 +354,22 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC2) {
-        // pairs of 128-row blocks on CTA pairs, then each expert's odd last block on one CTA
-        const int64_t npairs_max = nblk / 2 + 1, nsingles_max = ES < nblk ? ES : nblk;
+        // 256-row pairs of blocks and each expert's odd last block, all on CTA pairs in one
+        // launch per GEMM; the shared chunks' units are the last ones of the list
+        const int shared_units = (int)(D.num_shared_chunks * (((T + kTcBlockM - 1) / kTcBlockM + 1) / 2));
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, P->tm_rows_d, bexp, pair_list, meta, loc, h,
-                                    cap_tc, D.f, D.d, npairs_max, P->num_sms, P->d_error, stream, hidp, sh),
-                  "gate/up gemm (pairs)");
-        PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, cap_tc, D.f, D.d,
-                                 nsingles_max, P->num_sms, P->d_error, stream, single_list,
-                                 kMetaSingles, hidp, sh), "gate/up gemm (singles)");
+        CUtensorMap x64, h64, hid64;
+        if (!encode_rows_map(&x64, x, cap_tc, D.d, 64) || !encode_rows_map(&h64, h, cap_tc, D.f, 64) ||
+            (sh.direct && !encode_rows_map(&hid64, hidden, T, D.d, 64)))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, x64, P->tm_rows_d, P->tm_rows_d64, bexp, units,
+                                    meta, loc, h, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error,
+                                    stream, hidp, sh.direct ? &hid64 : nullptr, sh, shared_units),
+                  "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, P->tm_rows_f, bexp, pair_list, meta, loc, y,
-                                    cap_tc, D.f, D.d, npairs_max, P->num_sms, P->d_error, stream),
-                  "down gemm (pairs)");
-        PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, cap_tc, D.f, D.d,
-                                 nsingles_max, P->num_sms, P->d_error, stream, single_list,
-                                 kMetaSingles), "down gemm (singles)");
+        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, h64, P->tm_rows_f, P->tm_rows_f, bexp, units, meta,
+                                    loc, y, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error, stream,
+                                    nullptr, nullptr, SharedRows{}, shared_units), "down gemm");
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC_DECODE) {
@@ -415,8 +410,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
     P->last_kernels = ev - 1;
-    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0) +
-                       (path == PMOE_PATH_TC2 ? 2 : 0);
+    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
     return PMOE_OK;
 }
 

@@ -29,7 +29,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, part, pairs, singles, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, x, h, y, total;
     size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
@@ -139,11 +139,10 @@ struct ResolveArgs {
     int32_t contiguous;         // 1: expert e's matrix j is pool page 3e + j, tables unused
     ExpertLoc* loc;             // [E+S][3] out
     int32_t* err;
-    // optional work lists over the sorted blocks (NULL: not written): for each expert, its blocks
-    // taken two at a time (first block of each pair) and its odd last block; counts in
-    // meta[kMetaPairs], meta[kMetaSingles]
-    int32_t* pair_list;
-    int32_t* single_list;
+    // optional work units over the sorted blocks (NULL: not written): for each expert, its blocks
+    // taken two at a time, then its odd last block, each unit (first block << 1) | single; count
+    // in meta[kMetaPairs], single-block units in meta[kMetaSingles]
+    int32_t* units;
 };
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
@@ -216,14 +215,19 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
                            int list_meta = 0, const CUtensorMap* hid = nullptr,
                            SharedRows sh = SharedRows{});
 
-// CTA-pair tensor-core path (tc_gemm2sm.cu): pairs of consecutive 128-row blocks of one expert
-// from pair_list (count meta[kMetaPairs]); mode 1 gate/up -> h, 2 down -> y.
-cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
-                              const CUtensorMap* wmaps, const int32_t* block_expert,
-                              const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
-                              void* out, int64_t out_rows, int f, int d, int64_t npairs_max, int num_sms,
-                              int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
-                              SharedRows sh = SharedRows{});
+// CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units` (count meta[kMetaPairs]):
+// a pair of consecutive 128-row blocks of one expert, or an expert's odd last block;
+// mode 1 gate/up -> h, 2 down -> y (fp32, out_rows rows).  act/act64, hid/hid64: the token rows
+// with 128- and 64-row boxes; wmaps64: gate/up weight views with 64-row boxes.  shared_units:
+// how many of the last units belong to shared chunks (spread among the routed units in the work
+// order).
+cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap& act64,
+                              const CUtensorMap* wmaps, const CUtensorMap* wmaps64,
+                              const int32_t* block_expert, const int32_t* units, const int32_t* meta,
+                              const ExpertLoc* loc, void* out, int64_t out_rows, int f, int d,
+                              int64_t units_max, int num_sms, int32_t* err, cudaStream_t s,
+                              const CUtensorMap* hid = nullptr, const CUtensorMap* hid64 = nullptr,
+                              SharedRows sh = SharedRows{}, int shared_units = 0);
 
 // Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
 // tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.

@@ -50,32 +50,34 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 // ---------------------------------------------------------------------------------------------
 constexpr int kAlignWarps = 16;
 
-// One warp: the pair and single work lists of the pair path from the padded offsets.
-__device__ __forceinline__ void write_pair_lists(const int32_t* off, int ES, int block_m,
-                                                 const ResolveArgs& rs, int32_t* meta, int lane) {
+// One warp: the work units of the CTA-pair path from the padded offsets.  Per expert, in order,
+// its pairs of consecutive 128-row blocks, then its odd last block: unit = (first block << 1) |
+// (1 for a single block).  meta[kMetaPairs] = units, meta[kMetaSingles] = single-block units.
+__device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int block_m,
+                                                const ResolveArgs& rs, int32_t* meta, int lane) {
     const int per = (ES + 31) / 32;
     const int e0 = lane * per, e1 = min(ES, e0 + per);
-    int np = 0, ns = 0;
+    int nu = 0, ns = 0;
     for (int e = e0; e < e1; ++e) {
         const int nb = (off[e + 1] - off[e]) / block_m;
-        np += nb >> 1;
+        nu += (nb + 1) >> 1;
         ns += nb & 1;
     }
-    int ip = np, is = ns;
+    int iu = nu, is = ns;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, ip, o);
+        const int a = __shfl_up_sync(0xffffffffu, iu, o);
         const int b = __shfl_up_sync(0xffffffffu, is, o);
-        if (lane >= o) { ip += a; is += b; }
+        if (lane >= o) { iu += a; is += b; }
     }
-    int pp = ip - np, ss = is - ns;
+    int uu = iu - nu;
     for (int e = e0; e < e1; ++e) {
         const int b0 = off[e] / block_m, nb = (off[e + 1] - off[e]) / block_m;
-        for (int j = 0; j < (nb >> 1); ++j) rs.pair_list[pp++] = b0 + 2 * j;
-        if (nb & 1) rs.single_list[ss++] = b0 + nb - 1;
+        for (int j = 0; j < (nb >> 1); ++j) rs.units[uu++] = (b0 + 2 * j) << 1;
+        if (nb & 1) rs.units[uu++] = ((b0 + nb - 1) << 1) | 1;
     }
     if (lane == 31) {
-        meta[kMetaPairs] = ip;
+        meta[kMetaPairs] = iu;
         meta[kMetaSingles] = is;
     }
 }
@@ -167,7 +169,7 @@ __device__ __forceinline__ void align_block(
         for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
     }
     if (tid == 0) meta[kMetaNPadded] = off[ES];
-    if (w == 0 && rs.pair_list) write_pair_lists(off, ES, block_m, rs, meta, lane);
+    if (w == 0 && rs.units) write_unit_list(off, ES, block_m, rs, meta, lane);
 
     if (do_resolve) {
         for (int idx = tid; idx < ES * 3; idx += NT) {
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
         for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
     }
     if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
-    if (c == 0 && w == 0 && rs.pair_list) write_pair_lists(off, ES, block_m, rs, meta, lane);
+    if (c == 0 && w == 0 && rs.units) write_unit_list(off, ES, block_m, rs, meta, lane);
     if (do_resolve) {
         for (int idx = c * NT + tid; idx < ES * 3; idx += C * NT) {
             const int e = idx / 3, j = idx % 3;

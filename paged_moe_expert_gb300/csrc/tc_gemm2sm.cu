@@ -7,13 +7,19 @@
 // shares one B operand: each CTA stages half of it, the tensor cores of both SMs read both
 // halves, so every SM moves 32 KB per k-block instead of 48 KB and the shared-memory traffic per
 // MMA drops by a third.  A tile's 256 rows are two consecutive 128-row blocks of one expert (one
-// per CTA), taken from the sort's pair list; an expert's odd last block goes to the single-CTA
-// kernel, so no row is padded beyond 128.
+// per CTA, M = 256).  An expert's odd last block is a unit of its own in the same launch, right
+// after the expert's pairs so that it finds the expert's weights in L2: an M = 128 MMA over the
+// pair, 64 of the block's rows on each CTA.
 //
-//   gate/up: B = [128 rows of the W1 page | 128 rows of the W3 page] for output columns
+//   pair, gate/up: B = [128 rows of the W1 page | 128 rows of the W3 page] for output columns
 //            n0..n0+127: the leader CTA stages the W1 half, its peer the W3 half; every CTA's
 //            accumulator holds gate (columns 0..127) and up (128..255) for its own 128 rows.
-//   down:    B = 256 rows of the W2 page, 128 staged by each CTA.
+//   pair, down: B = 256 rows of the W2 page, 128 staged by each CTA.
+//   single block: the M = 128 accumulator of a CTA keeps its 64 rows twice over, in TMEM lanes
+//            0..63 for B rows (output columns) 0..127 and in lanes 64..127 for B rows 128..255,
+//            both at TMEM columns 0..127.  For gate/up each CTA therefore stages
+//            [64 W1 rows | 64 W3 rows] of columns n0 + 64*rank .. +63, which puts a row's gate
+//            and up values in the same lane; down is staged as for a pair.
 //
 // Protocol: both CTAs' TMA loads complete on the leader's full barrier; the leader issues the
 // MMAs and commits them to the empty and accumulator-full barriers of both CTAs (multicast);
@@ -37,19 +43,38 @@ constexpr int A_BYTES = 128 * BK * 2;  // 16 KB: this CTA's 128 rows
 constexpr int B_BYTES = 128 * BK * 2;  // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;
+constexpr int kTileRing = 4;          // tiles handed from the producer to the MMA and epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kYBox = 32 * 32 * 4;   // down epilogue: one 32-row x 32-column fp32 store box
 // ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
 // GEMM, two store boxes per epilogue warp
 template <int kMode>
 constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 1024 + (kMode == 2 ? 4 * 2 * kYBox : 0); }
-constexpr uint32_t kIdesc = idesc_bf16(256, BN);   // M = 256: 128 rows on each CTA
+constexpr uint32_t kIdesc = idesc_bf16(256, BN);      // pair of blocks: 128 rows on each CTA
+constexpr uint32_t kIdesc128 = idesc_bf16(128, BN);   // single block: 64 rows on each CTA
+constexpr int A64_BYTES = 64 * BK * 2;                // 8 KB: a single block's 64 rows per CTA
 
 enum { kGateUp = 1, kDown = 2 };
 
+// Per-tile time stamps for performance work (compiled in only with -DPMOE_GEMM_TRACE), as in the
+// single-CTA kernel: [0] accumulator free, [1] first k-block landed, [2] last MMA issued (all
+// globaltimer, the leader's MMA issuer), [3] SM cycles it waited for loads, [4] accumulator
+// released and [6] accumulator seen full (the leader's first epilogue warp), [5] SM id, [7] wait
+// for the accumulator begun.
+#ifdef PMOE_GEMM_TRACE
+constexpr int kTraceTiles = 8192;
+constexpr int kTraceWords = 8;
+__device__ unsigned long long g_gemm2_trace[2][kTraceTiles][kTraceWords];
+#define GTRACE(t, i, v) \
+    do { if ((t) < kTraceTiles) g_gemm2_trace[kMode - 1][(t)][(i)] = (unsigned long long)(v); } while (0)
+#else
+#define GTRACE(t, i, v) ((void)0)
+#endif
+
 struct Tc2Args {
     const int32_t* block_expert;   // per 128-row block
-    const int32_t* pair_list;      // first block of each pair (the pair is blocks b, b+1)
+    const int32_t* units;          // (first block << 1) | single: blocks b, b+1, or b alone
+    int shared_units;              // the last units of the list belong to shared chunks
     const int32_t* meta;
     const ExpertLoc* loc;
     void* out;
@@ -65,6 +90,9 @@ struct Tc2Maps {
     CUtensorMap w[3];   // pool / buffer 0 / buffer 1 weight views, 128-row boxes
     CUtensorMap hid;    // hidden [T][d], 128-row boxes, when args.sh.direct
     CUtensorMap y;      // down: y fp32 [cap][d], 32 x 32 boxes, 128-byte swizzle
+    CUtensorMap a64;    // the same views with 64-row boxes (single blocks: 64 rows per CTA)
+    CUtensorMap hid64;
+    CUtensorMap w64[3]; // gate/up weight views with 64-row boxes
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -95,11 +123,12 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -152,6 +181,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // tile ring: the producer hands each tile's unit and N tile to the MMA issuer and the epilogue
+    // warps, which then need no global loads of their own between tiles
+    auto mfull_bar = [&](int j) { return bar0 + 256u + 8u * j; };
+    auto mempty_bar = [&](int j) { return bar0 + 256u + 8u * (kTileRing + j); };
+    int4* tile_ring = reinterpret_cast<int4*>(sgen + STAGES * STAGE_BYTES + 256 + 16 * kTileRing);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
@@ -164,6 +198,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);    // the leader's multicast commit
             mbar_init(tempty_bar(a), 8);   // used on the leader: 4 epilogue warps x 2 CTAs
+        }
+        for (int j = 0; j < kTileRing; ++j) {
+            mbar_init(mfull_bar(j), 1);                      // this CTA's producer
+            mbar_init(mempty_bar(j), rank == 0 ? 5 : 4);     // epilogue warps (+ the MMA issuer)
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -185,9 +223,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     pdl_wait_prev();
     pdl_allow_next();
 
-    const int npairs = args.meta[kMetaPairs];
-    const int64_t ntiles = (int64_t)npairs * args.n_tiles;
+    const int nunits = args.meta[kMetaPairs];
+    const int64_t ntiles = (int64_t)nunits * args.n_tiles;
     const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+    // Work order: the shared chunks' units (weights resident in L2, tensor-bound) are spread
+    // evenly among the routed experts' units (weights streamed from HBM), so HBM streams over the
+    // whole launch; an expert's pairs and its odd block stay together and share its weights in L2.
+    const int nrouted = nunits - args.shared_units;
+    const bool mix = args.shared_units > 0 && nrouted > 0;
+    auto unit_of = [&](int64_t t, int& pb, bool& single) {
+        int i = (int)(t / args.n_tiles);
+        if (mix) {
+            const int r = (int)(((int64_t)i * nrouted) / nunits);          // routed units before i
+            const bool routed = (int)(((int64_t)(i + 1) * nrouted) / nunits) > r;
+            i = routed ? r : nrouted + (i - r);
+        }
+        const int u = args.units[i];
+        pb = u >> 1;
+        single = (u & 1) != 0;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -195,42 +249,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int pend_phase[STAGES];
             for (int s = 0; s < STAGES; ++s) pend_phase[s] = -1;
+            int mslot = 0;
+            uint32_t mphase = 0;
             bool ok = true;
+            // hands one tile (or, with pb < 0, the end of the work) to this CTA's consumers
+            auto publish = [&](int pb, bool single, int nt, int64_t t) -> bool {
+                if (!mbar_wait(mempty_bar(mslot), mphase ^ 1u, abort_flag, args.err)) return false;
+                tile_ring[mslot] = make_int4(pb < 0 ? -1 : (pb << 1) | (single ? 1 : 0), nt, (int)t, 0);
+                mbar_arrive(mfull_bar(mslot));
+                if (++mslot == kTileRing) { mslot = 0; mphase ^= 1u; }
+                return true;
+            };
             const int npad = args.meta[kMetaNPadded];
             for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
+                int pb;
+                bool single;
+                unit_of(t, pb, single);
+                const int nt = (int)(t % args.n_tiles);
                 ExpertLoc l0, l1;
                 if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
-                // this CTA's token rows: sorted rows, or hidden itself for a shared-chunk block
-                const CUtensorMap* am = &maps.a;
-                int row_a = (pb + (int)rank) * 128;
+                if (!publish(pb, single, nt, t)) { ok = false; break; }
+                // this CTA's token rows (a pair: its own block; a single block: its 64-row half):
+                // sorted rows, or hidden itself for a shared-chunk block
+                const CUtensorMap* am = single ? &maps.a64 : &maps.a;
+                int row_a = single ? pb * 128 + (int)rank * 64 : (pb + (int)rank) * 128;
                 if (kMode == kGateUp && args.sh.direct) {
                     const int e = args.block_expert[pb];
                     if (e >= args.sh.E) {
-                        am = &maps.hid;
+                        am = single ? &maps.hid64 : &maps.hid;
                         row_a = shared_token_row(args.sh, e, row_a, npad);
                     }
                 }
                 const CUtensorMap* wm;
-                int row_b;
+                const CUtensorMap* wm2 = nullptr;   // single gate/up: W3 box after the W1 box
+                int row_b, row_b2 = 0;
                 if (kMode == kGateUp) {
-                    wm = leader ? &maps.w[l0.map] : &maps.w[l1.map];
-                    row_b = (leader ? l0.page : l1.page) * args.f + nt * 128;
+                    if (single) {
+                        wm = &maps.w64[l0.map];
+                        wm2 = &maps.w64[l1.map];
+                        row_b = l0.page * args.f + nt * 128 + (int)rank * 64;
+                        row_b2 = l1.page * args.f + nt * 128 + (int)rank * 64;
+                    } else {
+                        wm = leader ? &maps.w[l0.map] : &maps.w[l1.map];
+                        row_b = (leader ? l0.page : l1.page) * args.f + nt * 128;
+                    }
                 } else {
                     wm = &maps.w[l0.map];
                     row_b = l0.page * args.d + nt * BN + (int)rank * 128;
                 }
+                const uint32_t tx = single ? 2 * (A64_BYTES + B_BYTES) : 2 * STAGE_BYTES;
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
                     const uint32_t fb_leader = map_to_rank(full_bar(stage), 0);
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
                     tma_load_2d_pair(sa, am, fb_leader, kb * BK, row_a);
-                    tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
+                    if (wm2) {
+                        tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
+                        tma_load_2d_pair(sa + A_BYTES + B_BYTES / 2, wm2, fb_leader, kb * BK, row_b2);
+                    } else {
+                        tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
+                    }
                     pend_phase[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
+            if (ok) publish(-1, false, 0, 0);
             if (!ok && leader) {
                 volatile int never = 0;
                 for (int s = 0; s < STAGES; ++s)
@@ -243,29 +327,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int mslot = 0;
+            uint32_t mphase = 0;
             bool ok = true;
-            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                const int pb = args.pair_list[t / args.n_tiles];
-                ExpertLoc l0, l1;
-                if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
+            while (ok) {
+                if (!mbar_wait(mfull_bar(mslot), mphase, abort_flag, args.err)) break;
+                const int4 m = tile_ring[mslot];
+                mbar_arrive(mempty_bar(mslot));
+                if (++mslot == kTileRing) { mslot = 0; mphase ^= 1u; }
+                if (m.x < 0) break;
+                const int t = m.z;
+                (void)t;
+                const uint32_t idesc = (m.x & 1) ? kIdesc128 : kIdesc;
+                GTRACE(t, 7, globaltimer());
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
                 tc_fence_after();
+                GTRACE(t, 0, globaltimer());
+#ifdef PMOE_GEMM_TRACE
+                long long waited = 0;
+#endif
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
+#ifdef PMOE_GEMM_TRACE
+                    const long long c0 = clock64();
+#endif
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) { ok = false; break; }
+#ifdef PMOE_GEMM_TRACE
+                    waited += clock64() - c0;
+                    if (kb == 0) GTRACE(t, 1, globaltimer());
+#endif
                     tc_fence_after();
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
                     const uint64_t adesc = smem_desc(sa);
                     const uint64_t bdesc = smem_desc(sa + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        mma_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k),
+                        mma_pair(d_tmem, adesc + (uint64_t)(2 * k), bdesc + (uint64_t)(2 * k), idesc,
                                  (kb | k) != 0 ? 1u : 0u);
                     mma_commit_pair(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit_pair(tfull_bar(acc));
+                GTRACE(t, 2, globaltimer());
+                GTRACE(t, 3, waited);
+#ifdef PMOE_GEMM_TRACE
+                {
+                    uint32_t smid;
+                    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                    GTRACE(t, 5, smid);
+                }
+#endif
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
         }
@@ -274,17 +386,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int mslot = 0;
+        uint32_t mphase = 0;
         const uint32_t ybox = bar0 + 1024u + (uint32_t)(quad * 2 * kYBox);   // down: this warp's boxes
         int ysel = 0;
-        for (int64_t t = cid; t < ntiles; t += ncl) {
-            const int pb = args.pair_list[t / args.n_tiles], nt = (int)(t % args.n_tiles);
-            ExpertLoc l0, l1;
-            if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
-            if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
+        // lane 0 waits and the warp follows its verdict, so the warp never splits before the
+        // warp-wide TMEM loads
+        auto warp_wait = [&](uint32_t bar, uint32_t par) -> bool {
+            int ok = 0;
+            if (lane == 0) ok = mbar_wait(bar, par, abort_flag, args.err) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();   // orders lane 0's acquire before the other lanes' reads
+            return ok != 0;
+        };
+        for (;;) {
+            if (!warp_wait(mfull_bar(mslot), mphase)) break;
+            const int4 m = tile_ring[mslot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mempty_bar(mslot));
+            if (++mslot == kTileRing) { mslot = 0; mphase ^= 1u; }
+            if (m.x < 0) break;
+            const int pb = m.x >> 1, nt = m.y, t = m.z;
+            const bool single = (m.x & 1) != 0;
+            (void)t;
+            if (!warp_wait(tfull_bar(acc), acc_phase)) break;
             tc_fence_after();
+            if (leader && lane == 0 && quad == 0) GTRACE(t, 6, globaltimer());
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-            const int64_t grow = (int64_t)(pb + (int)rank) * 128 + row;
-            if (kMode == kGateUp) {
+            if (single) {
+                // this warp's TMEM lanes: rows (quad & 1) * 32 + lane of the CTA's 64, and the
+                // first (quad < 2) or second half of the tile's output columns
+                const int half = quad >> 1;
+                const int64_t grow = (int64_t)pb * 128 + (int)rank * 64 + (quad & 1) * 32 + lane;
+                if (kMode == kGateUp) {
+                    // columns 0..63: gate, 64..127: up, of outputs n0 + 64*half + (0..63)
+                    uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128 + half * 64;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 64; c0 += 16) {
+                        float g[16], u[16];
+                        tmem_ld16(taddr + c0, g);
+                        tmem_ld16(taddr + 64 + c0, u);
+                        tmem_wait_ld();
+                        uint32_t p[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            p[i] = pack_bf16(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
+                        uint4* dst = reinterpret_cast<uint4*>(h + c0);
+                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    }
+                } else {
+                    const int r0 = nt * BN + half * 128;
+                    const int yrow = pb * 128 + (int)rank * 64 + (quad & 1) * 32;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < 128 && r0 + c0 < args.d; c0 += 32) {
+                        float lo[16], hi[16];
+                        tmem_ld16(taddr + c0, lo);
+                        tmem_ld16(taddr + c0 + 16, hi);
+                        tmem_wait_ld();
+                        store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                        ysel ^= 1;
+                    }
+                }
+            } else if (kMode == kGateUp) {
+                const int64_t grow = (int64_t)(pb + (int)rank) * 128 + row;
                 uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 16) {
@@ -294,11 +459,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     uint32_t p[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float a0 = silu_mul(g[2 * i], u[2 * i]);
-                        const float a1 = silu_mul(g[2 * i + 1], u[2 * i + 1]);
-                        p[i] = (uint32_t)f32_to_bf16_bits(a0) | ((uint32_t)f32_to_bf16_bits(a1) << 16);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        p[i] = pack_bf16(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
                     uint4* dst = reinterpret_cast<uint4*>(h + c0);
                     dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
@@ -320,6 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+            if (leader && lane == 0 && quad == 0) GTRACE(t, 4, globaltimer());
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (kMode == kDown && lane == 0) bulk_wait_all();   // stores done before the CTA exits
@@ -352,21 +515,28 @@ cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_
 
 }  // namespace
 
-cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
-                              const CUtensorMap* wmaps, const int32_t* block_expert,
-                              const int32_t* pair_list, const int32_t* meta, const ExpertLoc* loc,
-                              void* out, int64_t out_rows, int f, int d, int64_t npairs_max,
-                              int num_sms, int32_t* err, cudaStream_t s, const CUtensorMap* hid,
-                              SharedRows sh) {
+cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap& act64,
+                              const CUtensorMap* wmaps, const CUtensorMap* wmaps64,
+                              const int32_t* block_expert, const int32_t* units, const int32_t* meta,
+                              const ExpertLoc* loc, void* out, int64_t out_rows, int f, int d,
+                              int64_t units_max, int num_sms, int32_t* err, cudaStream_t s,
+                              const CUtensorMap* hid, const CUtensorMap* hid64, SharedRows sh,
+                              int shared_units) {
     Tc2Maps maps;
     maps.a = act;
-    for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
+    maps.a64 = act64;
+    for (int i = 0; i < 3; ++i) {
+        maps.w[i] = wmaps[i];
+        maps.w64[i] = wmaps64[i];
+    }
     maps.hid = hid ? *hid : act;
+    maps.hid64 = hid64 ? *hid64 : act64;
     maps.y = act;
     if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
     Tc2Args a{};
     a.block_expert = block_expert;
-    a.pair_list = pair_list;
+    a.units = units;
+    a.shared_units = shared_units;
     a.meta = meta;
     a.loc = loc;
     a.out = out;
@@ -381,7 +551,7 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
         a.k_blocks = f / BK;
         a.n_tiles = (d + BN - 1) / BN;
     }
-    const int64_t tiles = npairs_max * a.n_tiles;
+    const int64_t tiles = units_max * a.n_tiles;
     int64_t clusters = num_sms / 2;
     if (tiles < clusters) clusters = tiles > 0 ? tiles : 1;
     const int grid = (int)(2 * clusters);
@@ -389,5 +559,17 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act,
         return contig ? launch2<kGateUp, true>(maps, a, grid, s) : launch2<kGateUp, false>(maps, a, grid, s);
     return contig ? launch2<kDown, true>(maps, a, grid, s) : launch2<kDown, false>(maps, a, grid, s);
 }
+
+#ifdef PMOE_GEMM_TRACE
+extern "C" int pmoe_gemm2_trace_read(int mode, unsigned long long* host, int n) {
+    if (mode < 1 || mode > 2 || n > kTraceTiles * kTraceWords) return -1;
+    return (int)cudaMemcpyFromSymbol(host, g_gemm2_trace, sizeof(unsigned long long) * n,
+                                     sizeof(unsigned long long) * kTraceTiles * kTraceWords * (mode - 1));
+}
+extern "C" int pmoe_gemm2_trace_clear() {
+    static unsigned long long zeros[2 * kTraceTiles * kTraceWords];
+    return (int)cudaMemcpyToSymbol(g_gemm2_trace, zeros, sizeof(zeros));
+}
+#endif
 
 }  // namespace pmoe

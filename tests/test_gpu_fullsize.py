@@ -32,13 +32,15 @@ CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 32), ("qwen15", 128), ("qwen1
 
 
 @pytest.mark.parametrize("name,T", CASES)
-@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM, pm.PATH_TC_DECODE],
-                         ids=["auto", "stream", "tc_decode"])
+@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM, pm.PATH_TC_DECODE, pm.PATH_TC, pm.PATH_TC2],
+                         ids=["auto", "stream", "tc_decode", "tc", "tc2"])
 def test_full_size_sampled(name, T, path):
     if path == pm.PATH_STREAM and T > 16:
         pytest.skip("the weight-streaming kernels serve decode sizes")
     if path == pm.PATH_TC_DECODE and T > 32:
         pytest.skip("covered by the automatic path above 32 tokens")
+    if path in (pm.PATH_TC, pm.PATH_TC2) and T < 512:
+        pytest.skip("the 128-token-block kernels serve prefill sizes")
     cfg = syn.CONFIGS[name]
     L = setup_layer(cfg, T, weights=weights(name))
     L.plan.set_path(path)
