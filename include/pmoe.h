@@ -82,15 +82,15 @@ typedef struct pmoe_plan* pmoe_plan_t;
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
     PMOE_PATH_AUTO = 0,   /* FUSED up to 32 tokens (E <= 128) or 16 tokens (E > 128); above,
-                             by routed tokens per expert T*k/E: <= 192 TC_DECODE, < 384 TC,
-                             else TC2 */
+                             by routed tokens per expert T*k/E: <= 24 TC_DECODE, >= 64 TC2 when
+                             E <= 128, else TC */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
     PMOE_PATH_TC_DECODE = 3, /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens
                                 on N: weight streaming for small token counts */
     PMOE_PATH_TC2 = 4,      /* 128-token blocks, taken two at a time per expert by CTA pairs
                                (tcgen05 cta_group::2, 256x256 tiles); an expert's odd last
-                               block runs on one CTA */
+                               block is an M=128 tile of the same pair kernel */
     PMOE_PATH_FUSED = 5     /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
                                (one CTA per SM) whose weight streams are split evenly over the
                                SMs; see moe_paged_forward for what it requires of the caller */

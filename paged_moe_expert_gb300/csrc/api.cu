@@ -66,11 +66,13 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
 }
 
 // The automatic path, by the routed tokens per expert T*k/E (measured crossovers on GB300): up to
-// 192 the small-batch tensor-core kernels (tokens on the MMA's N side), below 384 the single-CTA
-// 128-token-block kernels, from 384 on the CTA-pair kernels, whose 256-token blocks pad little
-// there.  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
-constexpr int kSwapMaxTokensPerExpert = 192;
-constexpr int kPairMinTokensPerExpert = 384;
+// 24 the small-batch tensor-core kernels (tokens on the MMA's N side); above, the CTA-pair kernels
+// from 64 on for layers of at most 128 experts, else the single-CTA 128-token-block kernels (with
+// hundreds of small experts most experts end in an odd block, which costs a CTA pair as much as
+// a pair of blocks).  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
+constexpr int kSwapMaxTokensPerExpert = 24;
+constexpr int kPairMinTokensPerExpert = 64;
+constexpr int kPairMaxExperts = 128;
 constexpr int kPrepSmallMaxTokens = 128;
 
 static int stream_splits(const pmoe_layer_desc& D) {
@@ -208,8 +210,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         const int fused_max = D.num_experts <= 128 ? kFusedMaxTokens : 16;
         path = T <= fused_max ? PMOE_PATH_FUSED
              : routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
-             : routed < (int64_t)kPairMinTokensPerExpert * D.num_experts ? PMOE_PATH_TC
-             : PMOE_PATH_TC2;
+             : (routed >= (int64_t)kPairMinTokensPerExpert * D.num_experts &&
+                D.num_experts <= kPairMaxExperts) ? PMOE_PATH_TC2
+             : PMOE_PATH_TC;
     }
     const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE || path == PMOE_PATH_TC2 ||
                            path == PMOE_PATH_FUSED;
@@ -346,7 +349,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (path == PMOE_PATH_TC) {
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, cap_tc, D.f, D.d,
-                                 nblk, P->num_sms, P->d_error, stream, nullptr, 0, hidp, sh),
+                                 nblk, P->num_sms, P->d_error, stream, hidp, sh),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, cap_tc, D.f, D.d,

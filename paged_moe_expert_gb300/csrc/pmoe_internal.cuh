@@ -207,12 +207,10 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 // (the down GEMMs' epilogue stores of y).
 bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols);
 // mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32, out_rows rows)
-// list != NULL: only the blocks in list[0 .. meta[list_meta]) (single blocks of the pair path)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
-                           int32_t* err, cudaStream_t s, const int32_t* list = nullptr,
-                           int list_meta = 0, const CUtensorMap* hid = nullptr,
+                           int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
                            SharedRows sh = SharedRows{});
 
 // CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units` (count meta[kMetaPairs]):

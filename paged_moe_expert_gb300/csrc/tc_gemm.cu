@@ -78,8 +78,6 @@ struct TcArgs {
     int k_blocks;       // K / 64
     int n_tiles;        // N tiles per sorted block
     int32_t* err;
-    const int32_t* list;   // NULL: every block; else the blocks list[0 .. meta[list_meta])
-    int list_meta;
     SharedRows sh;         // gate/up: shared-chunk blocks straight from hidden
 };
 
@@ -157,12 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_prev();
     pdl_allow_next();
 
-    const int nblocks = args.list ? args.meta[args.list_meta] : args.meta[kMetaNPadded] / BM;
+    const int nblocks = args.meta[kMetaNPadded] / BM;
     const int64_t ntiles = (int64_t)nblocks * args.n_tiles;
-    auto block_of = [&](int64_t t) {
-        const int i = (int)(t / args.n_tiles);
-        return args.list ? args.list[i] : i;
-    };
+    auto block_of = [&](int64_t t) { return (int)(t / args.n_tiles); };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -403,8 +398,7 @@ bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
-                           int32_t* err, cudaStream_t s, const int32_t* list, int list_meta,
-                           const CUtensorMap* hid, SharedRows sh) {
+                           int32_t* err, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
     TcMaps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
@@ -419,8 +413,6 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
     a.f = f;
     a.d = d;
     a.err = err;
-    a.list = list;
-    a.list_meta = list_meta;
     a.sh = hid ? sh : SharedRows{};
     if (mode == kGateUp) {
         a.k_blocks = d / BK;

@@ -150,11 +150,10 @@ def test_invalid_arguments_rejected():
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
     # up to 32 tokens the fused decode kernel; then by T*k/E (tiny: E=8, k=2 -> T/4): small-batch
-    # kernels up to T=768, pairs from T=1536
+    # kernels up to T=96, single-CTA blocks below T=256, pairs from T=256
     for T, want in [(1, pm.PATH_FUSED), (16, pm.PATH_FUSED), (32, pm.PATH_FUSED),
-                    (33, pm.PATH_TC_DECODE), (128, pm.PATH_TC_DECODE),
-                    (768, pm.PATH_TC_DECODE), (769, pm.PATH_TC), (1535, pm.PATH_TC),
-                    (1536, pm.PATH_TC2), (4096, pm.PATH_TC2)]:
+                    (33, pm.PATH_TC_DECODE), (96, pm.PATH_TC_DECODE), (97, pm.PATH_TC),
+                    (255, pm.PATH_TC), (256, pm.PATH_TC2), (4096, pm.PATH_TC2)]:
         L = setup_layer(cfg, T)
         L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
         assert L.plan.last_run()[0] == want
