@@ -148,7 +148,8 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.meta = o;   o = align256(o + sizeof(int32_t) * kMetaCount);
     W.loc = o;    o = align256(o + sizeof(ExpertLoc) * ES * 3);
     W.part = o;   o = align256(o + align_part_bytes());
-    W.units = o;  o = align256(o + sizeof(int32_t) * W.nblk_max);
+    W.units = o;  o = align256(o + sizeof(int4) * W.nblk_max);
+    W.unit_w2 = o; o = align256(o + sizeof(int32_t) * W.nblk_max);
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
@@ -308,8 +309,12 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
 
     const int bm = (path == PMOE_PATH_TC || path == PMOE_PATH_TC2) ? kTcBlockM
                  : path == PMOE_PATH_TC_DECODE ? sw.bn : stream_block_m(D, T);
-    int32_t* units = at<int32_t>(ws, W.units);
-    if (path == PMOE_PATH_TC2) rs.units = units;
+    int4* units = at<int4>(ws, W.units);
+    int32_t* unit_w2 = at<int32_t>(ws, W.unit_w2);
+    if (path == PMOE_PATH_TC2) {
+        rs.units = units;
+        rs.unit_w2 = unit_w2;
+    }
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
@@ -365,13 +370,13 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         if (!encode_rows_map(&x64, x, cap_tc, D.d, 64) || !encode_rows_map(&h64, h, cap_tc, D.f, 64) ||
             (sh.direct && !encode_rows_map(&hid64, hidden, T, D.d, 64)))
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
-        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, x64, P->tm_rows_d, P->tm_rows_d64, bexp, units,
-                                    meta, loc, h, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error,
+        PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, x64, P->tm_rows_d, P->tm_rows_d64, units, unit_w2,
+                                    meta, h, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error,
                                     stream, hidp, sh.direct ? &hid64 : nullptr, sh, shared_units),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
-        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, h64, P->tm_rows_f, P->tm_rows_f, bexp, units, meta,
-                                    loc, y, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error, stream,
+        PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, h64, P->tm_rows_f, P->tm_rows_f, units, unit_w2,
+                                    meta, y, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error, stream,
                                     nullptr, nullptr, SharedRows{}, shared_units), "down gemm");
         ystride = cap_tc;
         splits = 1;

@@ -29,7 +29,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, x, h, y, total;
     size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
@@ -140,10 +140,21 @@ struct ResolveArgs {
     ExpertLoc* loc;             // [E+S][3] out
     int32_t* err;
     // optional work units over the sorted blocks (NULL: not written): for each expert, its blocks
-    // taken two at a time, then its odd last block, each unit (first block << 1) | single; count
-    // in meta[kMetaPairs], single-block units in meta[kMetaSingles]
-    int32_t* units;
+    // taken two at a time, then its odd last block; units[i] = {(first block << 1) | single,
+    // expert, packed location of W1, of W3} and unit_w2[i] = packed location of W2 (pack_loc);
+    // count in meta[kMetaPairs], single-block units in meta[kMetaSingles]
+    int4* units;
+    int32_t* unit_w2;
 };
+
+// An ExpertLoc in one word, (map << 29) | page, or -1 for none (pages of a pool or a buffer are
+// fewer than 2^29: a page holds at least 64 x 128 bf16).
+__host__ __device__ __forceinline__ int32_t pack_loc(ExpertLoc L) {
+    return L.map < 0 ? -1 : (int32_t)(((uint32_t)L.map << 29) | (uint32_t)L.page);
+}
+__host__ __device__ __forceinline__ ExpertLoc unpack_loc(int32_t v) {
+    return v < 0 ? ExpertLoc{-1, -1} : ExpertLoc{v >> 29, v & ((1 << 29) - 1)};
+}
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
@@ -213,17 +224,18 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
                            int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
                            SharedRows sh = SharedRows{});
 
-// CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units` (count meta[kMetaPairs]):
-// a pair of consecutive 128-row blocks of one expert, or an expert's odd last block;
+// CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units`/`unit_w2` (count
+// meta[kMetaPairs], written by the sort): a pair of consecutive 128-row blocks of one expert, or
+// an expert's odd last block, with the expert's weight locations;
 // mode 1 gate/up -> h, 2 down -> y (fp32, out_rows rows).  act/act64, hid/hid64: the token rows
 // with 128- and 64-row boxes; wmaps64: gate/up weight views with 64-row boxes.  shared_units:
 // how many of the last units belong to shared chunks (spread among the routed units in the work
 // order).
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap& act64,
                               const CUtensorMap* wmaps, const CUtensorMap* wmaps64,
-                              const int32_t* block_expert, const int32_t* units, const int32_t* meta,
-                              const ExpertLoc* loc, void* out, int64_t out_rows, int f, int d,
-                              int64_t units_max, int num_sms, int32_t* err, cudaStream_t s,
+                              const int4* units, const int32_t* unit_w2, const int32_t* meta,
+                              void* out, int64_t out_rows, int f, int d, int64_t units_max,
+                              int num_sms, int32_t* err, cudaStream_t s,
                               const CUtensorMap* hid = nullptr, const CUtensorMap* hid64 = nullptr,
                               SharedRows sh = SharedRows{}, int shared_units = 0);
 

@@ -50,10 +50,31 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
 // ---------------------------------------------------------------------------------------------
 constexpr int kAlignWarps = 16;
 
+// Where matrix j of active expert e lives for this call: (map, page) from the buffer slot or the
+// page table, with range checks (a bad entry raises the error word and yields {-1, -1}).
+__device__ __forceinline__ ExpertLoc resolve_loc(const ResolveArgs& rs, int E, int e, int j) {
+    if (rs.contiguous) return ExpertLoc{0, 3 * e + j};
+    const int bs = e < E ? rs.buf_slot[e] : -1;
+    if (bs >= 0) {
+        const int b = rs.slots_per_buffer > 0 ? bs / rs.slots_per_buffer : 2;
+        const bool have = (b == 0 && rs.have_buf0) || (b == 1 && rs.have_buf1);
+        if (b < 2 && have) return ExpertLoc{1 + b, 3 * (bs % rs.slots_per_buffer) + j};
+        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+    } else if (bs == -1) {
+        const int p = rs.page_table[e * 3 + j];
+        if (p >= 0 && p < rs.num_pages) return ExpertLoc{0, p};
+        raise_error(rs.err, PMOE_ERR_PAGE_OOB);
+    } else {
+        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
+    }
+    return ExpertLoc{-1, -1};
+}
+
 // One warp: the work units of the CTA-pair path from the padded offsets.  Per expert, in order,
-// its pairs of consecutive 128-row blocks, then its odd last block: unit = (first block << 1) |
-// (1 for a single block).  meta[kMetaPairs] = units, meta[kMetaSingles] = single-block units.
-__device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int block_m,
+// its pairs of consecutive 128-row blocks, then its odd last block, each with the expert and its
+// three weight locations, so a GEMM finds everything about a tile in one load.
+// meta[kMetaPairs] = units, meta[kMetaSingles] = single-block units.
+__device__ __forceinline__ void write_unit_list(const int32_t* off, int E, int ES, int block_m,
                                                 const ResolveArgs& rs, int32_t* meta, int lane) {
     const int per = (ES + 31) / 32;
     const int e0 = lane * per, e1 = min(ES, e0 + per);
@@ -73,8 +94,17 @@ __device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int 
     int uu = iu - nu;
     for (int e = e0; e < e1; ++e) {
         const int b0 = off[e] / block_m, nb = (off[e + 1] - off[e]) / block_m;
-        for (int j = 0; j < (nb >> 1); ++j) rs.units[uu++] = (b0 + 2 * j) << 1;
-        if (nb & 1) rs.units[uu++] = ((b0 + nb - 1) << 1) | 1;
+        if (nb == 0) continue;
+        const int p0 = pack_loc(resolve_loc(rs, E, e, 0)), p1 = pack_loc(resolve_loc(rs, E, e, 1));
+        const int p2 = pack_loc(resolve_loc(rs, E, e, 2));
+        for (int j = 0; j < (nb >> 1); ++j) {
+            rs.units[uu] = make_int4((b0 + 2 * j) << 1, e, p0, p1);
+            rs.unit_w2[uu++] = p2;
+        }
+        if (nb & 1) {
+            rs.units[uu] = make_int4(((b0 + nb - 1) << 1) | 1, e, p0, p1);
+            rs.unit_w2[uu++] = p2;
+        }
     }
     if (lane == 31) {
         meta[kMetaPairs] = iu;
@@ -169,32 +199,12 @@ __device__ __forceinline__ void align_block(
         for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
     }
     if (tid == 0) meta[kMetaNPadded] = off[ES];
-    if (w == 0 && rs.units) write_unit_list(off, ES, block_m, rs, meta, lane);
+    if (w == 0 && rs.units) write_unit_list(off, E, ES, block_m, rs, meta, lane);
 
     if (do_resolve) {
         for (int idx = tid; idx < ES * 3; idx += NT) {
             const int e = idx / 3, j = idx % 3;
-            ExpertLoc L{-1, -1};
-            if (cnt[e] > 0) {
-                if (rs.contiguous) {
-                    L = ExpertLoc{0, 3 * e + j};
-                } else {
-                    const int bs = e < E ? rs.buf_slot[e] : -1;
-                    if (bs >= 0) {
-                        const int b = rs.slots_per_buffer > 0 ? bs / rs.slots_per_buffer : 2;
-                        const bool have = (b == 0 && rs.have_buf0) || (b == 1 && rs.have_buf1);
-                        if (b < 2 && have) L = ExpertLoc{1 + b, 3 * (bs % rs.slots_per_buffer) + j};
-                        else raise_error(rs.err, PMOE_ERR_SLOT_OOB);
-                    } else if (bs == -1) {
-                        const int p = rs.page_table[e * 3 + j];
-                        if (p >= 0 && p < rs.num_pages) L = ExpertLoc{0, p};
-                        else raise_error(rs.err, PMOE_ERR_PAGE_OOB);
-                    } else {
-                        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
-                    }
-                }
-            }
-            rs.loc[idx] = L;
+            rs.loc[idx] = cnt[e] > 0 ? resolve_loc(rs, E, e, j) : ExpertLoc{-1, -1};
         }
     }
 }
@@ -339,31 +349,11 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
         for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
     }
     if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
-    if (c == 0 && w == 0 && rs.units) write_unit_list(off, ES, block_m, rs, meta, lane);
+    if (c == 0 && w == 0 && rs.units) write_unit_list(off, E, ES, block_m, rs, meta, lane);
     if (do_resolve) {
         for (int idx = c * NT + tid; idx < ES * 3; idx += C * NT) {
             const int e = idx / 3, j = idx % 3;
-            ExpertLoc L{-1, -1};
-            if (cnt[e] > 0) {
-                if (rs.contiguous) {
-                    L = ExpertLoc{0, 3 * e + j};
-                } else {
-                    const int bs = e < E ? rs.buf_slot[e] : -1;
-                    if (bs >= 0) {
-                        const int bb = rs.slots_per_buffer > 0 ? bs / rs.slots_per_buffer : 2;
-                        const bool have = (bb == 0 && rs.have_buf0) || (bb == 1 && rs.have_buf1);
-                        if (bb < 2 && have) L = ExpertLoc{1 + bb, 3 * (bs % rs.slots_per_buffer) + j};
-                        else raise_error(rs.err, PMOE_ERR_SLOT_OOB);
-                    } else if (bs == -1) {
-                        const int p = rs.page_table[e * 3 + j];
-                        if (p >= 0 && p < rs.num_pages) L = ExpertLoc{0, p};
-                        else raise_error(rs.err, PMOE_ERR_PAGE_OOB);
-                    } else {
-                        raise_error(rs.err, PMOE_ERR_SLOT_OOB);
-                    }
-                }
-            }
-            rs.loc[idx] = L;
+            rs.loc[idx] = cnt[e] > 0 ? resolve_loc(rs, E, e, j) : ExpertLoc{-1, -1};
         }
     }
 }

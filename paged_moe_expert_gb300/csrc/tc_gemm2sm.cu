@@ -72,11 +72,10 @@ __device__ unsigned long long g_gemm2_trace[2][kTraceTiles][kTraceWords];
 #endif
 
 struct Tc2Args {
-    const int32_t* block_expert;   // per 128-row block
-    const int32_t* units;          // (first block << 1) | single: blocks b, b+1, or b alone
+    const int4* units;             // {(first block << 1) | single, expert, W1 loc, W3 loc}
+    const int32_t* unit_w2;        // W2 loc of each unit (locations packed by pack_loc)
     int shared_units;              // the last units of the list belong to shared chunks
     const int32_t* meta;
-    const ExpertLoc* loc;
     void* out;
     int f, d;
     int k_blocks;
@@ -148,25 +147,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
                  : "memory");
 }
 
-template <bool kContig>
-__device__ __forceinline__ ExpertLoc loc2(const ExpertLoc* loc, int e, int j) {
-    if (kContig) return ExpertLoc{0, 3 * e + j};
-    return loc[e * 3 + j];
-}
-
-template <int kMode, bool kContig>
-__device__ __forceinline__ bool weights_of(const Tc2Args& A, int b, ExpertLoc& l0, ExpertLoc& l1) {
-    const int e = A.block_expert[b];
-    if (kMode == kGateUp) {
-        l0 = loc2<kContig>(A.loc, e, 0);
-        l1 = loc2<kContig>(A.loc, e, 1);
-        return l0.map >= 0 && l1.map >= 0;
-    }
-    l0 = loc2<kContig>(A.loc, e, 2);
-    l1 = l0;
-    return l0.map >= 0;
-}
-
 template <int kMode, bool kContig>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_gemm2sm_kernel(const __grid_constant__ Tc2Maps maps, const Tc2Args args) {
@@ -231,16 +211,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // whole launch; an expert's pairs and its odd block stay together and share its weights in L2.
     const int nrouted = nunits - args.shared_units;
     const bool mix = args.shared_units > 0 && nrouted > 0;
-    auto unit_of = [&](int64_t t, int& pb, bool& single) {
+    auto pos_of = [&](int64_t t) -> int {
         int i = (int)(t / args.n_tiles);
         if (mix) {
             const int r = (int)(((int64_t)i * nrouted) / nunits);          // routed units before i
             const bool routed = (int)(((int64_t)(i + 1) * nrouted) / nunits) > r;
             i = routed ? r : nrouted + (i - r);
         }
-        const int u = args.units[i];
-        pb = u >> 1;
-        single = (u & 1) != 0;
+        return i;
     };
 
     if (warp == 0) {
@@ -261,20 +239,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 return true;
             };
             const int npad = args.meta[kMetaNPadded];
-            for (int64_t t = cid; t < ntiles && ok; t += ncl) {
-                int pb;
-                bool single;
-                unit_of(t, pb, single);
-                const int nt = (int)(t % args.n_tiles);
+            // Everything about a tile is in its unit's record (one 16-byte load, plus the W2
+            // location for down); the next tile's record is loaded at the start of this tile,
+            // so its latency (a microsecond or two while the GEMM loads L2) hides behind this
+            // tile's copies.  A chain of dependent loads here (unit, then expert, then page
+            // location) drained the ring: the paged gate/up ran 5% behind fixed addressing.
+            struct TileMeta {
+                int pb, single, e;
                 ExpertLoc l0, l1;
-                if (!weights_of<kMode, kContig>(args, pb, l0, l1)) continue;
+            };
+            auto meta_load = [&](TileMeta& m, int64_t tt) {
+                const int i = pos_of(tt);
+                const int4 r = args.units[i];
+                const int32_t w2 = kMode == kDown && !kContig ? args.unit_w2[i] : -1;
+                m.pb = r.x >> 1;
+                m.single = r.x & 1;
+                m.e = r.y;
+                if (kContig) {
+                    m.l0 = ExpertLoc{0, 3 * r.y + (kMode == kGateUp ? 0 : 2)};
+                    m.l1 = ExpertLoc{0, 3 * r.y + (kMode == kGateUp ? 1 : 2)};
+                } else if (kMode == kGateUp) {
+                    m.l0 = unpack_loc(r.z);
+                    m.l1 = unpack_loc(r.w);
+                } else {
+                    m.l0 = unpack_loc(w2);
+                    m.l1 = m.l0;
+                }
+            };
+            auto meta_valid = [&](const TileMeta& m) {
+                return kMode == kGateUp ? (m.l0.map >= 0 && m.l1.map >= 0) : m.l0.map >= 0;
+            };
+            // the first tile from tt on with valid weights (false: none left)
+            auto find_valid = [&](int64_t& tt, TileMeta& m) -> bool {
+                for (; tt < ntiles; tt += ncl) {
+                    meta_load(m, tt);
+                    if (meta_valid(m)) return true;
+                }
+                return false;
+            };
+            int64_t t = cid;
+            TileMeta cur;
+            bool have = find_valid(t, cur);
+            while (have && ok) {
+                const int pb = cur.pb, nt = (int)(t % args.n_tiles);
+                const bool single = cur.single != 0;
+                const ExpertLoc l0 = cur.l0, l1 = cur.l1;
                 if (!publish(pb, single, nt, t)) { ok = false; break; }
                 // this CTA's token rows (a pair: its own block; a single block: its 64-row half):
                 // sorted rows, or hidden itself for a shared-chunk block
                 const CUtensorMap* am = single ? &maps.a64 : &maps.a;
                 int row_a = single ? pb * 128 + (int)rank * 64 : (pb + (int)rank) * 128;
                 if (kMode == kGateUp && args.sh.direct) {
-                    const int e = args.block_expert[pb];
+                    const int e = cur.e;
                     if (e >= args.sh.E) {
                         am = single ? &maps.hid64 : &maps.hid;
                         row_a = shared_token_row(args.sh, e, row_a, npad);
@@ -298,6 +314,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     row_b = l0.page * args.d + nt * BN + (int)rank * 128;
                 }
                 const uint32_t tx = single ? 2 * (A64_BYTES + B_BYTES) : 2 * STAGE_BYTES;
+                int64_t tn = t + ncl;
+                TileMeta nxt;
+                if (tn < ntiles) meta_load(nxt, tn);
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
                     const uint32_t fb_leader = map_to_rank(full_bar(stage), 0);
@@ -313,6 +332,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pend_phase[stage] = (int)phase;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (!ok || tn >= ntiles) break;
+                if (!meta_valid(nxt)) {
+                    tn += ncl;
+                    if (!find_valid(tn, nxt)) break;
+                }
+                t = tn;
+                cur = nxt;
             }
             if (ok) publish(-1, false, 0, 0);
             if (!ok && leader) {
@@ -517,8 +543,8 @@ cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_
 
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap& act64,
                               const CUtensorMap* wmaps, const CUtensorMap* wmaps64,
-                              const int32_t* block_expert, const int32_t* units, const int32_t* meta,
-                              const ExpertLoc* loc, void* out, int64_t out_rows, int f, int d,
+                              const int4* units, const int32_t* unit_w2, const int32_t* meta,
+                              void* out, int64_t out_rows, int f, int d,
                               int64_t units_max, int num_sms, int32_t* err, cudaStream_t s,
                               const CUtensorMap* hid, const CUtensorMap* hid64, SharedRows sh,
                               int shared_units) {
@@ -534,11 +560,10 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, con
     maps.y = act;
     if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
     Tc2Args a{};
-    a.block_expert = block_expert;
     a.units = units;
+    a.unit_w2 = unit_w2;
     a.shared_units = shared_units;
     a.meta = meta;
-    a.loc = loc;
     a.out = out;
     a.f = f;
     a.d = d;
