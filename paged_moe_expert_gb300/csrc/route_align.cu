@@ -70,12 +70,21 @@ __device__ __forceinline__ ExpertLoc resolve_loc(const ResolveArgs& rs, int E, i
     return ExpertLoc{-1, -1};
 }
 
+// The whole CTA: packed locations of every active expert's three matrices into sloc [ES][3].
+__device__ __forceinline__ void resolve_all(const ResolveArgs& rs, int E, int ES, const int32_t* cnt,
+                                            int32_t* sloc, int tid, int nt) {
+    for (int idx = tid; idx < ES * 3; idx += nt)
+        sloc[idx] = cnt[idx / 3] > 0 ? pack_loc(resolve_loc(rs, E, idx / 3, idx % 3)) : -1;
+}
+
 // One warp: the work units of the CTA-pair path from the padded offsets.  Per expert, in order,
 // its pairs of consecutive 128-row blocks, then its odd last block, each with the expert and its
-// three weight locations, so a GEMM finds everything about a tile in one load.
-// meta[kMetaPairs] = units, meta[kMetaSingles] = single-block units.
-__device__ __forceinline__ void write_unit_list(const int32_t* off, int E, int ES, int block_m,
-                                                const ResolveArgs& rs, int32_t* meta, int lane) {
+// three weight locations (sloc: packed, [ES][3], resolved by the whole CTA beforehand), so a GEMM
+// finds everything about a tile in one load.  meta[kMetaPairs] = units, meta[kMetaSingles] =
+// single-block units.
+__device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int block_m,
+                                                const ResolveArgs& rs, const int32_t* sloc,
+                                                int32_t* meta, int lane) {
     const int per = (ES + 31) / 32;
     const int e0 = lane * per, e1 = min(ES, e0 + per);
     int nu = 0, ns = 0;
@@ -95,8 +104,7 @@ __device__ __forceinline__ void write_unit_list(const int32_t* off, int E, int E
     for (int e = e0; e < e1; ++e) {
         const int b0 = off[e] / block_m, nb = (off[e + 1] - off[e]) / block_m;
         if (nb == 0) continue;
-        const int p0 = pack_loc(resolve_loc(rs, E, e, 0)), p1 = pack_loc(resolve_loc(rs, E, e, 1));
-        const int p2 = pack_loc(resolve_loc(rs, E, e, 2));
+        const int p0 = sloc[3 * e], p1 = sloc[3 * e + 1], p2 = sloc[3 * e + 2];
         for (int j = 0; j < (nb >> 1); ++j) {
             rs.units[uu] = make_int4((b0 + 2 * j) << 1, e, p0, p1);
             rs.unit_w2[uu++] = p2;
@@ -199,7 +207,12 @@ __device__ __forceinline__ void align_block(
         for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
     }
     if (tid == 0) meta[kMetaNPadded] = off[ES];
-    if (w == 0 && rs.units) write_unit_list(off, E, ES, block_m, rs, meta, lane);
+    if (rs.units) {
+        __syncthreads();   // the per-warp counters are free: they hold the locations now
+        resolve_all(rs, E, ES, cnt, cw, tid, NT);
+        __syncthreads();
+        if (w == 0) write_unit_list(off, ES, block_m, rs, cw, meta, lane);
+    }
 
     if (do_resolve) {
         for (int idx = tid; idx < ES * 3; idx += NT) {
@@ -349,7 +362,12 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
         for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
     }
     if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
-    if (c == 0 && w == 0 && rs.units) write_unit_list(off, E, ES, block_m, rs, meta, lane);
+    if (c == 0 && rs.units) {
+        __syncthreads();   // the per-warp counters are free: they hold the locations now
+        resolve_all(rs, E, ES, cnt, cw, tid, NT);
+        __syncthreads();
+        if (w == 0) write_unit_list(off, ES, block_m, rs, cw, meta, lane);
+    }
     if (do_resolve) {
         for (int idx = c * NT + tid; idx < ES * 3; idx += C * NT) {
             const int e = idx / 3, j = idx % 3;
