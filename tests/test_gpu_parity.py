@@ -228,3 +228,25 @@ def test_fused_back_to_back_calls_reuse_the_grid_barrier():
         assert np.array_equal(out_bits(o), first)
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
     assert_close(first, ref["out_bf16"])
+
+
+def test_pair_path_back_to_back_calls_are_identical():
+    """Many CTA-pair calls in a row on one workspace, with more tiles than CTA pairs and odd
+    blocks (M=128 units), stay bit-identical and match the oracle."""
+    cfg = syn.custom_config("pairs", d=256, f=384, E=12, k=3, S=2, n_buffered=3)
+    T = 700
+    L = setup_layer(cfg, T)
+    L.plan.set_path(pm.PATH_TC2)
+    ws = pm.alloc_workspace(L.desc, T)
+    outs = [torch.empty_like(L.hidden) for _ in range(8)]
+    for o in outs:
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, out=o, workspace=ws)
+    torch.cuda.synchronize()
+    assert L.plan.device_error() == 0
+    assert L.plan.last_run()[0] == pm.PATH_TC2
+    first = out_bits(outs[0])
+    for o in outs[1:]:
+        assert np.array_equal(out_bits(o), first)
+    rows = np.arange(0, T, 37)
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np[rows], L.logits_np[rows])
+    assert_close(first[rows], ref["out_bf16"])
