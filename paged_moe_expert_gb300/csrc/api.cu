@@ -413,7 +413,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
                                       stream), "gemm2");
     }
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
-    PMOE_CUDA(launch_combine(y, splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
+    const bool y_bf16 = path == PMOE_PATH_TC || path == PMOE_PATH_TC2;   // bf16 y rows, no K split
+    PMOE_CUDA(launch_combine(y, y_bf16, splits, ystride, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
                              static_cast<uint16_t*>(out), stream), "combine");
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;

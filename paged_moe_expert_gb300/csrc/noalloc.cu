@@ -159,7 +159,7 @@ extern "C" pmoe_status moe_paged_forward_noalloc(
                                  W.bm, W.nblk, h, s)) != cudaSuccess ||
         (e = launch_stream_gemm2(L, sorted, bexp, meta, loc, W.bm, W.nblk, W.splits, W.cap, h, y,
                                  s)) != cudaSuccess ||
-        (e = launch_combine(y, W.splits, W.cap, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
+        (e = launch_combine(y, false, W.splits, W.cap, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
                             static_cast<uint16_t*>(out), s)) != cudaSuccess)
         return na_fail(PMOE_ERR_CUDA, "kernel launch failed");
     return PMOE_OK;

@@ -192,7 +192,8 @@ cudaError_t launch_stream_gemm2(const LayerPtrs& L, const int32_t* sorted_ids,
                                 const int32_t* block_expert, const int32_t* meta,
                                 const ExpertLoc* loc, int block_m, int64_t nblk_max, int splits,
                                 int64_t cap, const uint16_t* h, float* y, cudaStream_t s);
-cudaError_t launch_combine(const float* y, int splits, int64_t cap, const float* w,
+// y_bf16: y holds bf16 rows (no K split); else fp32 rows, `splits` partials `cap` rows apart
+cudaError_t launch_combine(const void* y, bool y_bf16, int splits, int64_t cap, const float* w,
                            const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
                            cudaStream_t s);
 
@@ -214,10 +215,7 @@ __device__ __forceinline__ int shared_token_row(const SharedRows& sh, int e, int
 // Tensor-core path (tc_gemm.cu)
 bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                      int box_rows = 128);
-// An fp32 row-major matrix [rows][cols] as a TMA map with 32 x 32 boxes and 128-byte swizzle
-// (the down GEMMs' epilogue stores of y).
-bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols);
-// mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (fp32, out_rows rows)
+// mode 1: gate/up GEMM + SiLU-and-mul -> h (bf16); mode 2: down GEMM -> y (bf16, out_rows rows)
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
@@ -227,7 +225,7 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
 // CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units`/`unit_w2` (count
 // meta[kMetaPairs], written by the sort): a pair of consecutive 128-row blocks of one expert, or
 // an expert's odd last block, with the expert's weight locations;
-// mode 1 gate/up -> h, 2 down -> y (fp32, out_rows rows).  act/act64, hid/hid64: the token rows
+// mode 1 gate/up -> h, 2 down -> y (bf16, out_rows rows).  act/act64, hid/hid64: the token rows
 // with 128- and 64-row boxes; wmaps64: gate/up weight views with 64-row boxes.  shared_units:
 // how many of the last units belong to shared chunks (spread among the routed units in the work
 // order).

@@ -285,8 +285,10 @@ cudaError_t launch_stream_gemm2(const LayerPtrs& L, const int32_t* sorted_ids,
 
 // ---------------------------------------------------------------------------------------------
 // Combine: out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]] + sum_s y[inv[T*k + s*T + t]] ), with
-// each y the sum of its K-split partials; the order of every sum is fixed (pairs in order j, then
-// shared chunks s, each a fused multiply-add with weight 1 for the shared ones), so the output
+// each y a bf16 row (the 128-token-block and CTA-pair paths) or the fp32 sum of its K-split
+// partials (the small-batch and weight-streaming paths); the order of every sum is fixed (pairs
+// in order j, then shared chunks s, each a fused multiply-add with weight 1 for the shared
+// ones), so the output
 // does not depend on where the experts live or on scheduling.  A thread owns four columns of one
 // token and issues the loads of up to eight pairs before it adds any of them.
 // ---------------------------------------------------------------------------------------------
@@ -346,13 +348,72 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     reinterpret_cast<uint2*>(out + (int64_t)t * d)[c] = o;
 }
 
-cudaError_t launch_combine(const float* y, int splits, int64_t ystride, const float* w,
+// The same sum over bf16 y rows (the 128-token-block and CTA-pair paths, no K split): a thread owns
+// eight columns (one 16-byte load per pair row).
+__global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(
+    const uint16_t* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv,
+    int T, int d, int k, int S, uint16_t* __restrict__ out) {
+    pdl_wait_prev();
+    pdl_allow_next();
+    const int t = blockIdx.y;
+    const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // group of 8 columns
+    const int P = k + S;
+    const int64_t NR = (int64_t)T * k;
+    __shared__ int64_t s_row[64];
+    __shared__ float s_w[64];
+    for (int p = threadIdx.x; p < P; p += kCombineThreads) {
+        s_row[p] = p < k ? inv[(int64_t)t * k + p] : inv[NR + (int64_t)(p - k) * T + t];
+        s_w[p] = p < k ? w[(int64_t)t * k + p] : 1.f;
+    }
+    __syncthreads();
+    if (c >= (d >> 3)) return;
+    const uint4* y8 = reinterpret_cast<const uint4*>(y);
+    const int64_t d8 = d >> 3;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int p0 = 0; p0 < P; p0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (p0 + i < P) v[i] = __ldg(y8 + s_row[p0 + i] * d8 + c);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (p0 + i < P) {
+                const float wp = s_w[p0 + i];
+                acc[0] = fmaf(wp, bf16_lo(v[i].x), acc[0]);
+                acc[1] = fmaf(wp, bf16_hi(v[i].x), acc[1]);
+                acc[2] = fmaf(wp, bf16_lo(v[i].y), acc[2]);
+                acc[3] = fmaf(wp, bf16_hi(v[i].y), acc[3]);
+                acc[4] = fmaf(wp, bf16_lo(v[i].z), acc[4]);
+                acc[5] = fmaf(wp, bf16_hi(v[i].z), acc[5]);
+                acc[6] = fmaf(wp, bf16_lo(v[i].w), acc[6]);
+                acc[7] = fmaf(wp, bf16_hi(v[i].w), acc[7]);
+            }
+        }
+    }
+    uint4 o;
+    o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
+    o.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
+    o.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
+    reinterpret_cast<uint4*>(out + (int64_t)t * d)[c] = o;
+}
+
+cudaError_t launch_combine(const void* y, bool y_bf16, int splits, int64_t ystride, const float* w,
                            const int32_t* inv, int T, int d, int k, int S, uint16_t* out,
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
+    if (y_bf16) {
+        const dim3 grid((unsigned)((d / 8 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
+        return launch_pdl(combine_bf16_kernel, grid, dim3(kCombineThreads), 0, s,
+                          static_cast<const uint16_t*>(y), w, inv, T, d, k, S, out);
+    }
     const dim3 grid((unsigned)((d / 4 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
-    return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, y, splits, ystride, w, inv,
-                      T, d, k, S, out);
+    return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, static_cast<const float*>(y),
+                      splits, ystride, w, inv, T, d, k, S, out);
 }
 
 }  // namespace pmoe

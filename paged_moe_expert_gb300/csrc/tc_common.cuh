@@ -115,38 +115,6 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-
-// Epilogue of an fp32 accumulator: this warp's 32 TMEM lanes (32 output rows) x 32 columns (lo:
-// the first 16, hi: the next 16) are
-// written to a 4 KB shared-memory box in the 128-byte swizzled layout (row r's 16-byte chunk j at
-// chunk j ^ (r mod 8), so the warp's stores hit every bank once per four wavefronts) and stored to
-// y[row0 .. row0+31][col0 .. col0+31] by one TMA store issued by lane 0.  `box` must be
-// 1024-byte aligned and the caller must alternate two boxes: before writing one, lane 0 waits
-// until only its latest store (from the other box) may still be reading shared memory.
-__device__ __forceinline__ void store_rows_f32x32(const CUtensorMap* ymap, uint32_t box, const float (&lo)[16],
-                                                  const float (&hi)[16], int lane, int col0, int row0) {
-    if (lane == 0) bulk_wait_read_1();
-    __syncwarp();
-    const uint32_t rb = box + (uint32_t)lane * 128u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        st_shared_v4(rb + ((uint32_t)(j ^ (lane & 7)) << 4), lo[4 * j], lo[4 * j + 1], lo[4 * j + 2],
-                     lo[4 * j + 3]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        st_shared_v4(rb + ((uint32_t)((j + 4) ^ (lane & 7)) << 4), hi[4 * j], hi[4 * j + 1],
-                     hi[4 * j + 2], hi[4 * j + 3]);
-    fence_proxy_async_shared();
-    __syncwarp();
-    if (lane == 0) {
-        tma_store_2d(ymap, box, col0, row0);
-        bulk_commit();
-    }
-}
 
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -202,6 +170,47 @@ __device__ __forceinline__ void tmem_wait_ld() {
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return (uint32_t)f32_to_bf16_bits(a) | ((uint32_t)f32_to_bf16_bits(b) << 16);
+}
+
+__device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Epilogue of an fp32 accumulator to bf16: this warp's 32 TMEM lanes (32 output rows) x 64
+// columns from TMEM column address `taddr` are rounded to bf16 into a 4 KB shared-memory box in
+// the 128-byte swizzled layout (row r's 16-byte chunk j at chunk j ^ (r mod 8): the warp's stores
+// hit every bank once per four wavefronts) and stored to y[row0 .. row0+31][col0 .. col0+63] by
+// one TMA store issued by lane 0.  `box` must be 1024-byte aligned and the caller must alternate
+// two boxes: before writing one, lane 0 waits until only its latest store (from the other box)
+// may still be reading shared memory.
+__device__ __forceinline__ void store_rows_bf16x64(const CUtensorMap* ymap, uint32_t box, uint32_t taddr,
+                                                   int lane, int col0, int row0) {
+    if (lane == 0) bulk_wait_read_1();
+    __syncwarp();
+    const uint32_t rb = box + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float a[16], b[16];
+        tmem_ld16(taddr + 32u * half, a);
+        tmem_ld16(taddr + 32u * half + 16u, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            st_shared_v4u(rb + ((uint32_t)((4 * half + j) ^ (lane & 7)) << 4), pack_bf16(a[8 * j], a[8 * j + 1]),
+                          pack_bf16(a[8 * j + 2], a[8 * j + 3]), pack_bf16(a[8 * j + 4], a[8 * j + 5]),
+                          pack_bf16(a[8 * j + 6], a[8 * j + 7]));
+            st_shared_v4u(rb + ((uint32_t)((4 * half + 2 + j) ^ (lane & 7)) << 4),
+                          pack_bf16(b[8 * j], b[8 * j + 1]), pack_bf16(b[8 * j + 2], b[8 * j + 3]),
+                          pack_bf16(b[8 * j + 4], b[8 * j + 5]), pack_bf16(b[8 * j + 6], b[8 * j + 7]));
+        }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(ymap, box, col0, row0);
+        bulk_commit();
+    }
 }
 
 }  // namespace tc

@@ -37,7 +37,7 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;          // 6 warps
 constexpr uint32_t kTmemCols = 512;    // two 256-column fp32 accumulators
-constexpr int kYBox = 32 * 32 * 4;     // down epilogue: one 32-row x 32-column fp32 store box
+constexpr int kYBox = 32 * 64 * 2;     // down epilogue: one 32-row x 64-column bf16 store box
 // ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
 // GEMM, two store boxes per epilogue warp
 template <int kMode>
@@ -73,7 +73,7 @@ struct TcArgs {
     const int32_t* block_expert;
     const int32_t* meta;
     const ExpertLoc* loc;
-    void* out;          // h (bf16 [cap][f]) or y (fp32 [cap][d])
+    void* out;          // h (bf16 [cap][f]) or y (bf16 [cap][d])
     int f, d;
     int k_blocks;       // K / 64
     int n_tiles;        // N tiles per sorted block
@@ -85,7 +85,7 @@ struct TcMaps {
     CUtensorMap a;      // activations: X_sorted [cap][d] or h [cap][f]
     CUtensorMap w[3];   // weights of pool / load buffer 0 / load buffer 1
     CUtensorMap hid;    // hidden [T][d] (128-row boxes), when args.sh.direct
-    CUtensorMap y;      // down: y fp32 [cap][d], 32 x 32 boxes, 128-byte swizzle
+    CUtensorMap y;      // down: y bf16 [cap][d], 32-row x 64-column boxes, 128-byte swizzle
 };
 
 template <bool kContig>
@@ -298,17 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                 }
             } else {
-                // fp32 rows through shared memory and TMA stores: each store writes whole
+                // bf16 rows through shared memory and TMA stores: each store writes whole
                 // 128-byte lines instead of one 16-byte piece of 32 different rows
                 const int r0 = nt * BN;
                 const int yrow = mb * BM + quad * 32;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 32) {
-                    float lo[16], hi[16];
-                    tmem_ld16(taddr + c0, lo);
-                    tmem_ld16(taddr + c0 + 16, hi);
-                    tmem_wait_ld();
-                    store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 64) {
+                    store_rows_bf16x64(&maps.y, ybox + (uint32_t)(ysel * kYBox), taddr + c0, lane, r0 + c0, yrow);
                     ysel ^= 1;
                 }
             }
@@ -381,19 +377,6 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// An fp32 row-major matrix [rows][cols] as a TMA map with 32 x 32 boxes (128-byte rows) and
-// 128-byte swizzle, for the epilogue stores of y.
-bool encode_f32_rows_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
-    EncodeTiledFn fn = encoder();
-    if (!fn || !base || rows <= 0 || cols <= 0 || (cols * 4) % 16 != 0) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-    const cuuint32_t box[2] = {32, 32};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
@@ -404,7 +387,7 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
     maps.hid = hid ? *hid : act;
     maps.y = act;
-    if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
+    if (mode == kDown && !encode_rows_map(&maps.y, out, out_rows, d, 32)) return cudaErrorInvalidValue;
     TcArgs a{};
     a.block_expert = block_expert;
     a.meta = meta;

@@ -45,7 +45,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int kThreads = 192;
 constexpr int kTileRing = 4;          // tiles handed from the producer to the MMA and epilogue
 constexpr uint32_t kTmemCols = 512;
-constexpr int kYBox = 32 * 32 * 4;   // down epilogue: one 32-row x 32-column fp32 store box
+constexpr int kYBox = 32 * 64 * 2;   // down epilogue: one 32-row x 64-column bf16 store box
 // ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
 // GEMM, two store boxes per epilogue warp
 template <int kMode>
@@ -88,7 +88,7 @@ struct Tc2Maps {
     CUtensorMap a;      // X_sorted [cap][d] or h [cap][f], 128-row boxes
     CUtensorMap w[3];   // pool / buffer 0 / buffer 1 weight views, 128-row boxes
     CUtensorMap hid;    // hidden [T][d], 128-row boxes, when args.sh.direct
-    CUtensorMap y;      // down: y fp32 [cap][d], 32 x 32 boxes, 128-byte swizzle
+    CUtensorMap y;      // down: y bf16 [cap][d], 32-row x 64-column boxes, 128-byte swizzle
     CUtensorMap a64;    // the same views with 64-row boxes (single blocks: 64 rows per CTA)
     CUtensorMap hid64;
     CUtensorMap w64[3]; // gate/up weight views with 64-row boxes
@@ -465,12 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int r0 = nt * BN + half * 128;
                     const int yrow = pb * 128 + (int)rank * 64 + (quad & 1) * 32;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 128 && r0 + c0 < args.d; c0 += 32) {
-                        float lo[16], hi[16];
-                        tmem_ld16(taddr + c0, lo);
-                        tmem_ld16(taddr + c0 + 16, hi);
-                        tmem_wait_ld();
-                        store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                    for (int c0 = 0; c0 < 128 && r0 + c0 < args.d; c0 += 64) {
+                        store_rows_bf16x64(&maps.y, ybox + (uint32_t)(ysel * kYBox), taddr + c0, lane, r0 + c0, yrow);
                         ysel ^= 1;
                     }
                 }
@@ -492,16 +488,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
                 }
             } else {
-                // fp32 rows through shared memory and TMA stores (whole 128-byte lines)
+                // bf16 rows through shared memory and TMA stores (whole 128-byte lines)
                 const int r0 = nt * BN;
                 const int yrow = (pb + (int)rank) * 128 + quad * 32;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 32) {
-                    float lo[16], hi[16];
-                    tmem_ld16(taddr + c0, lo);
-                    tmem_ld16(taddr + c0 + 16, hi);
-                    tmem_wait_ld();
-                    store_rows_f32x32(&maps.y, ybox + (uint32_t)(ysel * kYBox), lo, hi, lane, r0 + c0, yrow);
+                for (int c0 = 0; c0 < BN && r0 + c0 < args.d; c0 += 64) {
+                    store_rows_bf16x64(&maps.y, ybox + (uint32_t)(ysel * kYBox), taddr + c0, lane, r0 + c0, yrow);
                     ysel ^= 1;
                 }
             }
@@ -558,7 +550,7 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, con
     maps.hid = hid ? *hid : act;
     maps.hid64 = hid64 ? *hid64 : act64;
     maps.y = act;
-    if (mode == kDown && !encode_f32_rows_map(&maps.y, out, out_rows, d)) return cudaErrorInvalidValue;
+    if (mode == kDown && !encode_rows_map(&maps.y, out, out_rows, d, 32)) return cudaErrorInvalidValue;
     Tc2Args a{};
     a.units = units;
     a.unit_w2 = unit_w2;
