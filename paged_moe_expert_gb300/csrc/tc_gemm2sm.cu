@@ -8,18 +8,19 @@
 // halves, so every SM moves 32 KB per k-block instead of 48 KB and the shared-memory traffic per
 // MMA drops by a third.  A tile's 256 rows are two consecutive 128-row blocks of one expert (one
 // per CTA, M = 256).  An expert's odd last block is a unit of its own in the same launch, right
-// after the expert's pairs so that it finds the expert's weights in L2: an M = 128 MMA over the
-// pair, 64 of the block's rows on each CTA.
+// after the expert's pairs so that it finds the expert's weights in L2, with the operands'
+// roles swapped: 256 weight rows on the MMA's M side (128 per CTA) and the block's 128 tokens on
+// N (64 staged by each CTA), so it fills the tensor cores as a pair does at half the work (an
+// M = 128 MMA, 64 token rows per CTA, ran at half rate and cost as much as a pair).
 //
 //   pair, gate/up: B = [128 rows of the W1 page | 128 rows of the W3 page] for output columns
 //            n0..n0+127: the leader CTA stages the W1 half, its peer the W3 half; every CTA's
 //            accumulator holds gate (columns 0..127) and up (128..255) for its own 128 rows.
 //   pair, down: B = 256 rows of the W2 page, 128 staged by each CTA.
-//   single block: the M = 128 accumulator of a CTA keeps its 64 rows twice over, in TMEM lanes
-//            0..63 for B rows (output columns) 0..127 and in lanes 64..127 for B rows 128..255,
-//            both at TMEM columns 0..127.  For gate/up each CTA therefore stages
-//            [64 W1 rows | 64 W3 rows] of columns n0 + 64*rank .. +63, which puts a row's gate
-//            and up values in the same lane; down is staged as for a pair.
+//   single block, gate/up: A = [64 W1 rows | 64 W3 rows] of output columns n0 + 64*rank .. +63
+//            on each CTA; TMEM lanes 0..63 hold gate, 64..127 up, columns the 128 tokens; the up
+//            lanes hand their values to the gate lanes through shared memory.
+//   single block, down: A = 128 W2 rows (output columns) on each CTA, as the pair's B halves.
 //
 // Protocol: both CTAs' TMA loads complete on the leader's full barrier; the leader issues the
 // MMAs and commits them to the empty and accumulator-full barriers of both CTAs (multicast);
@@ -46,13 +47,14 @@ constexpr int kThreads = 192;
 constexpr int kTileRing = 4;          // tiles handed from the producer to the MMA and epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kYBox = 32 * 64 * 2;   // down epilogue: one 32-row x 64-column bf16 store box
+constexpr int kXchBytes = 16 * 64 * 4;                  // single gate/up: up values of 16 tokens
 // ring, alignment slack, barriers (1 KB, keeping what follows 1024-byte aligned) and, for the down
-// GEMM, two store boxes per epilogue warp
+// GEMM, two store boxes per epilogue warp (gate/up: the single blocks' exchange buffer)
 template <int kMode>
-constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 1024 + (kMode == 2 ? 4 * 2 * kYBox : 0); }
+constexpr int smem_bytes() { return STAGES * STAGE_BYTES + 1024 + 1024 + (kMode == 2 ? 4 * 2 * kYBox : kXchBytes); }
 constexpr uint32_t kIdesc = idesc_bf16(256, BN);      // pair of blocks: 128 rows on each CTA
-constexpr uint32_t kIdesc128 = idesc_bf16(128, BN);   // single block: 64 rows on each CTA
-constexpr int A64_BYTES = 64 * BK * 2;                // 8 KB: a single block's 64 rows per CTA
+constexpr uint32_t kIdescSwap = idesc_bf16(256, 128);   // single block: weights on M, tokens on N
+constexpr int A64_BYTES = 64 * BK * 2;                  // 8 KB: 64 rows of a 64-column k-block
 
 enum { kGateUp = 1, kDown = 2 };
 
@@ -285,8 +287,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const bool single = cur.single != 0;
                 const ExpertLoc l0 = cur.l0, l1 = cur.l1;
                 if (!publish(pb, single, nt, t)) { ok = false; break; }
-                // this CTA's token rows (a pair: its own block; a single block: its 64-row half):
-                // sorted rows, or hidden itself for a shared-chunk block
+                // this CTA's token rows (a pair: its own block, the MMA's A; a single block: its
+                // 64-row half, the MMA's B): sorted rows, or hidden itself for a shared-chunk block
                 const CUtensorMap* am = single ? &maps.a64 : &maps.a;
                 int row_a = single ? pb * 128 + (int)rank * 64 : (pb + (int)rank) * 128;
                 if (kMode == kGateUp && args.sh.direct) {
@@ -297,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 const CUtensorMap* wm;
-                const CUtensorMap* wm2 = nullptr;   // single gate/up: W3 box after the W1 box
+                const CUtensorMap* wm2 = nullptr;   // single gate/up: the W3 box after the W1 box
                 int row_b, row_b2 = 0;
                 if (kMode == kGateUp) {
                     if (single) {
@@ -322,11 +324,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb_leader = map_to_rank(full_bar(stage), 0);
                     if (leader) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
-                    tma_load_2d_pair(sa, am, fb_leader, kb * BK, row_a);
-                    if (wm2) {
-                        tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
-                        tma_load_2d_pair(sa + A_BYTES + B_BYTES / 2, wm2, fb_leader, kb * BK, row_b2);
+                    if (single) {
+                        // weights into the A half of the stage, the 64 token rows into the B half
+                        tma_load_2d_pair(sa, wm, fb_leader, kb * BK, row_b);
+                        if (wm2) tma_load_2d_pair(sa + A64_BYTES, wm2, fb_leader, kb * BK, row_b2);
+                        tma_load_2d_pair(sa + A_BYTES, am, fb_leader, kb * BK, row_a);
                     } else {
+                        tma_load_2d_pair(sa, am, fb_leader, kb * BK, row_a);
                         tma_load_2d_pair(sa + A_BYTES, wm, fb_leader, kb * BK, row_b);
                     }
                     pend_phase[stage] = (int)phase;
@@ -364,7 +368,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (m.x < 0) break;
                 const int t = m.z;
                 (void)t;
-                const uint32_t idesc = (m.x & 1) ? kIdesc128 : kIdesc;
+                const uint32_t idesc = (m.x & 1) ? kIdescSwap : kIdesc;
                 GTRACE(t, 7, globaltimer());
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err)) break;
                 tc_fence_after();
@@ -440,34 +444,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (leader && lane == 0 && quad == 0) GTRACE(t, 6, globaltimer());
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
             if (single) {
-                // this warp's TMEM lanes: rows (quad & 1) * 32 + lane of the CTA's 64, and the
-                // first (quad < 2) or second half of the tile's output columns
-                const int half = quad >> 1;
-                const int64_t grow = (int64_t)pb * 128 + (int)rank * 64 + (quad & 1) * 32 + lane;
+                // TMEM lanes: this CTA's 128 weight rows; columns: the block's tokens
+                // pb*128 + 0..127 (the leader's B rows first)
                 if (kMode == kGateUp) {
-                    // columns 0..63: gate, 64..127: up, of outputs n0 + 64*half + (0..63)
-                    uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128 + half * 64;
+                    // lanes 0..63 (quads 0, 1) gate, 64..127 (quads 2, 3) up, of the outputs
+                    // n0 + 64*rank + fi; the up warps pass their values to the gate warps
+                    const int fi = (quad & 1) * 32 + lane;
+                    const bool up_half = quad >= 2;
+                    float* xch = reinterpret_cast<float*>(sgen + STAGES * STAGE_BYTES + 1024);
+                    uint16_t* hcol = static_cast<uint16_t*>(args.out) + (int64_t)pb * 128 * args.f +
+                                     nt * 128 + (int)rank * 64 + fi;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 64; c0 += 16) {
-                        float g[16], u[16];
-                        tmem_ld16(taddr + c0, g);
-                        tmem_ld16(taddr + 64 + c0, u);
+                    for (int c0 = 0; c0 < 128; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(taddr + c0, v);
                         tmem_wait_ld();
-                        uint32_t p[8];
+                        if (up_half) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            p[i] = pack_bf16(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
-                        uint4* dst = reinterpret_cast<uint4*>(h + c0);
-                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                            for (int j = 0; j < 16; ++j) xch[j * 64 + fi] = v[j];
+                        }
+                        asm volatile("bar.sync 1, 128;" ::: "memory");
+                        if (!up_half) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                hcol[(int64_t)(c0 + j) * args.f] = f32_to_bf16_bits(silu_mul(v[j], xch[j * 64 + fi]));
+                        }
+                        asm volatile("bar.sync 1, 128;" ::: "memory");
                     }
                 } else {
-                    const int r0 = nt * BN + half * 128;
-                    const int yrow = pb * 128 + (int)rank * 64 + (quad & 1) * 32;
+                    // lanes: output columns nt*256 + rank*128 + quad*32 + lane
+                    const int dcol = nt * BN + (int)rank * 128 + quad * 32 + lane;
+                    const bool in = nt * BN + (int)rank * 128 + quad * 32 < args.d;   // whole warp
+                    uint16_t* ycol = static_cast<uint16_t*>(args.out) + (int64_t)pb * 128 * args.d + dcol;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < 128 && r0 + c0 < args.d; c0 += 64) {
-                        store_rows_bf16x64(&maps.y, ybox + (uint32_t)(ysel * kYBox), taddr + c0, lane, r0 + c0, yrow);
-                        ysel ^= 1;
+                    for (int c0 = 0; c0 < 128; c0 += 16) {
+                        float v[16];
+                        tmem_ld16(taddr + c0, v);
+                        tmem_wait_ld();
+                        if (in) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) ycol[(int64_t)(c0 + j) * args.d] = f32_to_bf16_bits(v[j]);
+                        }
                     }
                 }
             } else if (kMode == kGateUp) {
