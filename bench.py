@@ -60,7 +60,7 @@ def work(cfg, T, e_act):
     total_bytes = wbytes + 4.0 * T * d + 4.0 * T * E
     g1 = {"flops": 4.0 * pairs * d * f, "bytes": 4.0 * d * f * (e_act + S) + 2.0 * pairs * (d + f)}
     g2 = {"flops": 2.0 * pairs * d * f,
-          "bytes": 2.0 * d * f * (e_act + S) + 2.0 * pairs * f + 4.0 * pairs * d}
+          "bytes": 2.0 * d * f * (e_act + S) + 2.0 * pairs * f + 2.0 * pairs * d}   # bf16 h in, y out
     return {"flops": flops, "weight_bytes": wbytes, "bytes": total_bytes, "gemm1": g1, "gemm2": g2}
 
 
