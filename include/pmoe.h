@@ -90,7 +90,8 @@ typedef enum {
                                 on N: weight streaming for small token counts */
     PMOE_PATH_TC2 = 4,      /* 128-token blocks, taken two at a time per expert by CTA pairs
                                (tcgen05 cta_group::2, 256x256 tiles); an expert's odd last
-                               block is an M=128 tile of the same pair kernel */
+                               block runs in the same pair kernel with the weights on the MMA's
+                               M side and its 128 tokens on N */
     PMOE_PATH_FUSED = 5     /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
                                (one CTA per SM) whose weight streams are split evenly over the
                                SMs; see moe_paged_forward for what it requires of the caller */
