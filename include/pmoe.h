@@ -234,6 +234,62 @@ pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, 
                        int32_t* n_padded, void* scratch, pmoe_stream_t stream);
 size_t pmoe_align_scratch_size(void);
 
+/* ---- the adjuster: which experts each layer keeps in the page pool -------------------------
+ *
+ * Host only (no device work).  Rimuru, section "The adjuster: when to evict an expert, and which
+ * one?": after the scheduler has placed the round's requests it is short of
+ * R_b expert pages or has F_b free ones, and the adjuster
+ *   - evicts ceil((R_b + 1) / 3) experts when R_b > 0,
+ *   - else evicts 1 expert when F_b < 2,
+ *   - else adds min(5, floor((F_b - 9) / 3)) experts when F_b > 9 (nothing for 2 <= F_b <= 9).
+ * Every expert takes 3 pages (W1, W3, W2).  Each layer keeps the top slice of an offline ranking
+ * of its experts by routing probability (probs[l][e], ties to the lower expert id).  To add,
+ * each layer with an uncached expert nominates the next one of its ranking and the adjuster
+ * takes the nominees with the highest probability; to evict, each layer that keeps an expert and
+ * offloads fewer than offload_limit nominates the last expert it keeps and the adjuster takes
+ * the nominees with the lowest probability; at most one per layer per round (ties to the lower
+ * layer).  An added expert gets 3 free pages at once (lowest page ids first: the reserved pages
+ * it is copied into before the page table points at them).  An evicted expert's pages stay its
+ * own until pmoe_adjuster_end_forward (the forward pass running now may still read them), then
+ * return to the free pages.  F_b counts free pages only; pages lent out (KV cache pages of the
+ * unified pool) are neither free nor an expert's.  Errors: argument checks return
+ * PMOE_ERR_INVALID_ARG with pmoe_last_error() set and leave the state unchanged; no call blocks
+ * or touches a device.  One adjuster must not be used from two threads at once. */
+typedef struct pmoe_adjuster* pmoe_adjuster_t;
+
+/* probs: host fp32 [n_layers][n_experts] routing probabilities (finite); cached: host int32
+ * [n_layers], how many top-ranked experts each layer keeps at the start (0..n_experts); they
+ * take pages 0, 1, 2, ... layer by layer in ranking order (W1, W3, W2 of each expert), the rest
+ * of the num_pages pages are free.  num_pages >= 3 * sum(cached), < 2^31.  offload_limit >= 0:
+ * a layer with n_experts - kept >= offload_limit is left out of shrinking.  The adjuster copies
+ * what it needs; the caller keeps ownership of probs and cached and destroys *out. */
+pmoe_status pmoe_adjuster_create(int32_t n_layers, int32_t n_experts, const float* probs,
+                                 int32_t offload_limit, const int32_t* cached, int64_t num_pages,
+                                 pmoe_adjuster_t* out);
+pmoe_status pmoe_adjuster_destroy(pmoe_adjuster_t adj);
+
+/* One round.  short_pages = R_b (>= 0).  Writes records of 6 int32 to changes (host):
+ * {+1 add / -1 evict, layer, expert, page of W1, page of W3, page of W2}, in the order taken
+ * (a round only adds or only evicts); *n_changes = the records written.  A round takes no more
+ * than max_changes (>= 0) changes, nor more than one per layer.  PMOE_ERR_INVALID_ARG while the
+ * evictions of the previous round still wait for pmoe_adjuster_end_forward. */
+pmoe_status pmoe_adjuster_decide(pmoe_adjuster_t adj, int32_t short_pages, int32_t max_changes,
+                                 int32_t* changes, int32_t* n_changes);
+
+/* The forward pass that ran during the round has ended: evicted experts' pages become free. */
+pmoe_status pmoe_adjuster_end_forward(pmoe_adjuster_t adj);
+
+/* Lend n free pages (lowest ids first) to the caller, e.g. for KV cache (PMOE_ERR_INVALID_ARG
+ * when fewer than n are free), and take lent pages back. */
+pmoe_status pmoe_adjuster_lend(pmoe_adjuster_t adj, int32_t n, int32_t* pages);
+pmoe_status pmoe_adjuster_give_back(pmoe_adjuster_t adj, int32_t n, const int32_t* pages);
+
+/* State: free pages (F_b), the experts each layer keeps (cached int32 [n_layers], may be NULL),
+ * and a layer's page table (int32 [n_experts][3]; -1 for an expert not kept, an evicted expert
+ * keeps its pages until pmoe_adjuster_end_forward). */
+pmoe_status pmoe_adjuster_state(pmoe_adjuster_t adj, int64_t* free_pages, int32_t* cached);
+pmoe_status pmoe_adjuster_page_table(pmoe_adjuster_t adj, int32_t layer, int32_t* page_table);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,10 +14,11 @@ import ctypes
 import torch
 
 from . import _lib
+from .adjuster import Adjuster
 from ._lib import (PATH_AUTO, PATH_FUSED, PATH_STREAM, PATH_TC, PATH_TC2, PATH_TC_DECODE, LayerDesc,
                    PmoeError)
 
-__all__ = ["LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
+__all__ = ["Adjuster", "LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
            "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
            "make_desc"]
 

@@ -50,6 +50,14 @@ SIGNATURES = {
     "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),
     "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P, P]),
     "pmoe_align_scratch_size": (SZ, []),
+    "pmoe_adjuster_create": (ctypes.c_int, [I32, I32, P, I32, P, I64, ctypes.POINTER(P)]),
+    "pmoe_adjuster_destroy": (ctypes.c_int, [P]),
+    "pmoe_adjuster_decide": (ctypes.c_int, [P, I32, I32, P, ctypes.POINTER(I32)]),
+    "pmoe_adjuster_end_forward": (ctypes.c_int, [P]),
+    "pmoe_adjuster_lend": (ctypes.c_int, [P, I32, P]),
+    "pmoe_adjuster_give_back": (ctypes.c_int, [P, I32, P]),
+    "pmoe_adjuster_state": (ctypes.c_int, [P, ctypes.POINTER(I64), P]),
+    "pmoe_adjuster_page_table": (ctypes.c_int, [P, I32, P]),
 }
 
 _lock = threading.Lock()

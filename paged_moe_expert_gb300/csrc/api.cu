@@ -20,6 +20,8 @@ static pmoe_status fail(pmoe_status s, const char* msg) {
     return s;
 }
 
+pmoe_status record_failure(pmoe_status s, const char* msg) { return fail(s, msg); }
+
 static pmoe_status cuda_fail(cudaError_t e, const char* where) {
     g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
     return PMOE_ERR_CUDA;

@@ -63,6 +63,9 @@ struct Plan {
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)
 };
 
+// Sets the text pmoe_last_error() returns and passes the status through.
+pmoe_status record_failure(pmoe_status s, const char* msg);
+
 // Device helpers ----------------------------------------------------------------------------
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
