@@ -370,6 +370,80 @@ def decode_sweep(args):
         torch.cuda.empty_cache()
 
 
+def elastic_sweep(args):
+    """24 Qwen1.5-MoE-shaped layers on ONE page pool shared with the KV cache.  A KV demand
+    trace (in expert pages) rises and falls over the rounds; each round the KV pages are taken
+    first and the adjuster evicts or adds experts by the offline ranking (routing frequencies
+    measured on a sample drawn from the same skewed router), added experts are copied into their
+    reserved pages, and offloaded experts that the step routes to stream through the two load
+    buffers.  Prints one JSON line per phase of the trace."""
+    from paged_moe_expert_gb300 import pipeline
+    import paged_moe_expert_gb300 as pm
+    torch.cuda.set_device(0)
+    cfg = syn.CONFIGS["qwen15"]
+    w = syn.make_weights(cfg)
+    L, T, E = args.layers, args.elastic_tokens, cfg.E
+    rng = np.random.default_rng(23)
+    bias = rng.standard_normal((L, E)).astype(np.float32)     # per-layer expert popularity
+
+    def draw(n):
+        return [syn.bf16_bits_to_f32(syn.to_bf16_bits(
+            rng.standard_normal((n, E)).astype(np.float32) + bias[l])) for l in range(L)]
+
+    sample = draw(4096)   # "offline" profiling sample -> routing probability per expert
+    probs = np.stack([np.bincount(np.argsort(-lg, axis=1, kind="stable")[:, :cfg.k].ravel(),
+                                  minlength=E) / (4096.0 * cfg.k) for lg in sample]).astype(np.float32)
+    limit = args.offload_limit
+    expert_pages = 3 * E * L + 3 * 4
+    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, [E] * L, limit, expert_pages)
+    peak = args.kv_peak
+    phases = [("idle, all experts resident", [0] * 5),
+              ("KV demand ramps up", [int(peak * (i + 1) / 20) for i in range(20)]),
+              ("KV demand held at peak", [peak] * 20),
+              ("KV demand ramps down", [int(peak * (19 - i) / 20) for i in range(20)]),
+              ("idle again", [0] * 25)]
+    hidden = torch.from_numpy(syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(
+        np.float32)).view(np.int16)).view(torch.bfloat16).cuda()
+    ws = pm.alloc_workspace(stack.desc, T)
+    acts = [torch.empty_like(hidden) for _ in range(2)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    page_mb = cfg.f * cfg.d * 2 / 1e6
+    for name, trace in phases:
+        rec = {"ms": [], "resident": [], "kv_pages": [], "short": [], "adds": 0, "evicts": 0,
+               "prefetched": 0}
+        for need in trace:
+            lg = draw(T)
+            f0 = stack.filled_experts
+            changes, short = stack.round(need)
+            sched = stack.schedule(lg)
+            lg_dev = [torch.from_numpy(x).cuda() for x in lg]
+            a.record()
+            stack.step(hidden, lg_dev, sched, acts, ws)
+            b.record()
+            torch.cuda.synchronize()
+            rec["ms"].append(a.elapsed_time(b))
+            rec["resident"].append(int(stack.adj.cached().sum()))
+            rec["kv_pages"].append(len(stack.kv))
+            rec["short"].append(int(short))
+            rec["adds"] += stack.filled_experts - f0
+            rec["evicts"] += int((changes[:, 0] == -1).sum()) if len(changes) else 0
+            rec["prefetched"] += sum(len(sc[0]) for sc in sched)
+        n = len(trace)
+        line = {"metric": "elastic decode: adjuster-driven 24-layer step on one pool shared with KV",
+                "config": {"workload": "%d Qwen1.5-MoE-shaped layers, %d tokens/step, %d expert "
+                           "pages (%.2f MB each), offload limit %d" % (L, T, expert_pages, page_mb, limit),
+                           "phase": name, "rounds": n, "kv_demand_pages": [trace[0], trace[-1]]},
+                "ms_per_step_median": float(np.median(rec["ms"])),
+                "ms_per_step_max": float(np.max(rec["ms"])),
+                "tokens_per_s": T / (float(np.median(rec["ms"])) * 1e-3),
+                "resident_experts": [min(rec["resident"]), max(rec["resident"])],
+                "kv_pages_held_end": rec["kv_pages"][-1], "short_pages_max": max(rec["short"]),
+                "experts_added": rec["adds"], "experts_evicted": rec["evicts"],
+                "experts_streamed_per_step": rec["prefetched"] / n,
+                "copied_mb_per_step": (rec["adds"] + rec["prefetched"]) * 3 * page_mb / n}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,9 +461,17 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--tokens-list", default="1,4,16,64,256")
     ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
+    ap.add_argument("--elastic-sweep", action="store_true",
+                    help="adjuster-driven 24-layer decode over a KV demand trace")
+    ap.add_argument("--elastic-tokens", type=int, default=16)
+    ap.add_argument("--offload-limit", type=int, default=30)
+    ap.add_argument("--kv-peak", type=int, default=1800)
     args = ap.parse_args()
     if args.decode_sweep:
         decode_sweep(args)
+        return
+    if args.elastic_sweep:
+        elastic_sweep(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

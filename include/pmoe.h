@@ -234,6 +234,17 @@ pmoe_status pmoe_align(const int32_t* ids, int32_t T, int32_t top_k, int32_t E, 
                        int32_t* n_padded, void* scratch, pmoe_stream_t stream);
 size_t pmoe_align_scratch_size(void);
 
+/* Copy experts from pinned host memory straight into pool pages (Rimuru, section "The
+ * adjuster...": an expert the adjuster adds is written into the pages it reserved for it, and
+ * the page table points at them only after the copy).  On copy_stream: wait for `after` (e.g.
+ * the end of the forward pass that last read those pages; may be NULL), then for each expert i
+ * copy matrix j (W1, W3, W2) of host_experts[i] (3*f*d bf16, back to back) into pool page
+ * pages[3*i + j] with one cudaMemcpyAsync each, then record `copy_done` (may be NULL).  pages is
+ * a host int32 array [n][3] of distinct pages in [0, num_pages) (PMOE_ERR_PAGE_OOB otherwise). */
+pmoe_status pmoe_fill_pages_async(pmoe_plan_t plan, int32_t n, const void* const* host_experts,
+                                  const int32_t* pages, pmoe_stream_t copy_stream,
+                                  pmoe_event_t after, pmoe_event_t copy_done);
+
 /* ---- the adjuster: which experts each layer keeps in the page pool -------------------------
  *
  * Host only (no device work).  Rimuru, section "The adjuster: when to evict an expert, and which

@@ -19,7 +19,7 @@ from ._lib import (PATH_AUTO, PATH_FUSED, PATH_STREAM, PATH_TC, PATH_TC2, PATH_T
                    PmoeError)
 
 __all__ = ["Adjuster", "LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
-           "prefetch_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
+           "prefetch_async", "fill_pages_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
            "make_desc"]
 
 
@@ -187,6 +187,21 @@ def prefetch_async(plan: Plan, buf: int, host_experts, slots, copy_stream, buf_f
     _lib.check(_lib.load().pmoe_prefetch_async(plan._h, int(buf), int(n), ptrs, sl,
                                                _stream(copy_stream), free,
                                                _event(copy_done, copy_stream)))
+
+
+def fill_pages_async(plan: Plan, host_experts, pages, copy_stream, after=None, copy_done=None):
+    """Copy experts (pinned host tensors of 3*f*d bf16: W1|W3|W2) into pool pages
+    (pages[i] = the three pages of expert i) on `copy_stream`, after `after` and before
+    `copy_done` (torch.cuda.Event or None)."""
+    n = len(host_experts)
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in host_experts])
+    flat = [int(p) for row in pages for p in row]
+    if len(flat) != 3 * n:
+        raise ValueError("pages must hold three pages per expert")
+    pg = (ctypes.c_int32 * max(3 * n, 1))(*flat)
+    wait = _event(after) if (after is not None and after.cuda_event != 0) else None
+    _lib.check(_lib.load().pmoe_fill_pages_async(plan._h, int(n), ptrs, pg, _stream(copy_stream),
+                                                 wait, _event(copy_done, copy_stream)))
 
 
 def wait_event(event, timeout_ms: int) -> bool:

@@ -45,6 +45,7 @@ SIGNATURES = {
     "moe_paged_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, P, I32, P,
                                                   I32, P, P, P, P, P]),
     "pmoe_prefetch_async": (ctypes.c_int, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(I32), P, P, P]),
+    "pmoe_fill_pages_async": (ctypes.c_int, [P, I32, ctypes.POINTER(P), P, P, P, P]),
     "pmoe_wait_event": (ctypes.c_int, [P, I32]),
     "pmoe_get_device_error": (ctypes.c_int, [P, I32, ctypes.POINTER(I32), P]),
     "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),

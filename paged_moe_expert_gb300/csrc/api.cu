@@ -589,6 +589,35 @@ pmoe_status pmoe_prefetch_async(pmoe_plan_t plan, int32_t buf, int32_t n,
     return PMOE_OK;
 }
 
+pmoe_status pmoe_fill_pages_async(pmoe_plan_t plan, int32_t n, const void* const* host_experts,
+                                  const int32_t* pages, pmoe_stream_t copy_stream,
+                                  pmoe_event_t after, pmoe_event_t copy_done) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P) return fail(PMOE_ERR_INVALID_ARG, "plan is NULL");
+    if (n < 0) return fail(PMOE_ERR_INVALID_ARG, "n < 0");
+    if (n > 0 && (!host_experts || !pages)) return fail(PMOE_ERR_INVALID_ARG, "NULL host arrays");
+    for (int i = 0; i < n; ++i)
+        if (!host_experts[i]) return fail(PMOE_ERR_INVALID_ARG, "NULL host expert");
+    for (int i = 0; i < 3 * n; ++i) {
+        if (pages[i] < 0 || pages[i] >= P->num_pages)
+            return fail(PMOE_ERR_PAGE_OOB, "page out of range");
+        for (int j = 0; j < i; ++j)
+            if (pages[j] == pages[i]) return fail(PMOE_ERR_INVALID_ARG, "duplicate page");
+    }
+    cudaStream_t cs = (cudaStream_t)copy_stream;
+    if (after) PMOE_CUDA(cudaStreamWaitEvent(cs, (cudaEvent_t)after, 0), "wait after");
+    const size_t page_bytes = (size_t)P->desc.f * P->desc.d * 2;
+    char* pool = static_cast<char*>(const_cast<void*>(P->pool));
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < 3; ++j)
+            PMOE_CUDA(cudaMemcpyAsync(pool + (size_t)pages[3 * i + j] * page_bytes,
+                                      static_cast<const char*>(host_experts[i]) + j * page_bytes,
+                                      page_bytes, cudaMemcpyHostToDevice, cs),
+                      "fill page copy");
+    if (copy_done) PMOE_CUDA(cudaEventRecord((cudaEvent_t)copy_done, cs), "record copy_done");
+    return PMOE_OK;
+}
+
 pmoe_status pmoe_wait_event(pmoe_event_t ev, int32_t timeout_ms) {
     if (!ev) return fail(PMOE_ERR_INVALID_ARG, "event is NULL");
     const auto t0 = std::chrono::steady_clock::now();

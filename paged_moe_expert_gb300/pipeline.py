@@ -17,6 +17,13 @@ stream one layer ahead of compute:
     iteration l:  copy stream: wait free[(l+1)%2]  -> copy layer l+1's experts -> record ready[(l+1)%2]
                   compute:     wait ready[l%2]      -> forward layer l            -> record free[l%2]
 
+`ElasticDecodeStack` puts all layers on ONE page pool shared with the KV cache and lets the
+adjuster (libpmoe's native `pmoe_adjuster_*`) decide each round which experts stay ("The
+adjuster..."): KV pages are lent out of the free pages first, a remaining shortfall R_b makes the
+adjuster evict, surplus free pages make it add; added experts are copied into their reserved
+pages on a fill stream and a layer's page table points at them only after that copy; evicted
+experts keep their pages until the round's forward pass has ended.
+
 Only host bookkeeping lives here (which experts, which slots, which events); every copy is one
 cudaMemcpyAsync issued by libpmoe and every step of the layer runs in its kernels.
 """
@@ -27,6 +34,7 @@ import torch
 
 import paged_moe_expert_gb300 as pm
 from paged_moe_expert_gb300 import pool as pl
+from paged_moe_expert_gb300.adjuster import Adjuster
 from paged_moe_expert_gb300 import synthetic as syn
 
 
@@ -122,4 +130,155 @@ class DecodeStack:
                                      workspace=ws)
             self.free[l % 2].record(cur)                     # WAR
             x = out
+        return x
+
+
+def kv_round(held: int, need: int, free: int):
+    """One round of KV cache pages in the unified pool: (pages to take from the free pages,
+    pages to give back, R_b = pages still missing).  The scheduler's KV allocation comes before
+    the adjuster, which sees the free pages left after it and the shortfall."""
+    if need <= held:
+        return 0, held - need, 0
+    take = min(free, need - held)
+    return take, 0, need - held - take
+
+
+class ElasticDecodeStack:
+    """L layers of one MoE shape over one page pool: pages [0, 3*S*L) hold the layers' shared
+    chunks (always resident), pages base + [0, expert_pages) are the adjuster's, shared between
+    routed experts and lent KV cache pages.  All layers carry the same weights (one synthetic
+    set, pinned on the host once).  probs[l][e] is the offline routing probability the ranking
+    comes from; cached[l] experts of layer l start resident."""
+
+    def __init__(self, cfg, weights, n_layers: int, probs, cached, offload_limit: int,
+                 expert_pages: int, device="cuda"):
+        E, S, f, d = cfg.E, cfg.S, cfg.f, cfg.d
+        self.cfg, self.L, self.device = cfg, n_layers, device
+        self.base = 3 * S * n_layers
+        num_pages = self.base + expert_pages
+        self.pool = pl.new_pool(num_pages, f, d, device)
+        # a layer offloads at most offload_limit experts, so each load buffer needs that many slots
+        self.slots = max(1, int(offload_limit))
+        self.desc = pm.make_desc(d, f, E, cfg.k, cfg.renormalize, S, self.slots)
+        self.bufs = pl.new_load_buffers(self.slots, f, d, device)
+        self.plan = pm.Plan(self.desc, self.pool, num_pages, self.bufs)
+        self.adj = Adjuster(probs, cached, offload_limit, expert_pages)
+        if (E - self.adj.cached() > self.slots).any():
+            raise ValueError("a layer starts with more offloaded experts than offload_limit")
+        self.host = [torch.from_numpy(pl.pack_expert(weights, e, E, f).view(np.int16)).pin_memory()
+                     for e in range(E + S)]
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.fill_stream = torch.cuda.Stream(device=device)
+        self.ready = [torch.cuda.Event() for _ in range(2)]
+        self.free = [torch.cuda.Event() for _ in range(2)]
+        self.fill_done = [torch.cuda.Event() for _ in range(n_layers)]
+        self.fwd_done = torch.cuda.Event()
+        self.kv = []                                  # pages lent to the KV cache
+        self.filling = [False] * n_layers
+        self.filled_experts = 0
+        # initial placement: shared chunks and the cached experts, straight into their pages
+        hs, pg = [], []
+        for l in range(n_layers):
+            for s_ in range(S):
+                hs.append(self.host[E + s_])
+                pg.append([3 * (l * S + s_) + j for j in range(3)])
+            pt = self.adj.page_table(l)
+            for e in np.nonzero(pt[:, 0] >= 0)[0]:
+                hs.append(self.host[int(e)])
+                pg.append((pt[e] + self.base).tolist())
+        pm.fill_pages_async(self.plan, hs, pg, self.fill_stream)
+        self.fill_stream.synchronize()
+        self.tables = [torch.empty((E + S, 3), dtype=torch.int32, device=device)
+                       for _ in range(n_layers)]
+        self.table_host = [torch.empty((E + S, 3), dtype=torch.int32).pin_memory()
+                           for _ in range(n_layers)]
+        self.uploaded = [None] * n_layers
+        self.upload_done = [torch.cuda.Event() for _ in range(n_layers)]
+        for l in range(n_layers):
+            self.tables[l].copy_(torch.from_numpy(self.table_np(l)))
+            self.uploaded[l] = self.table_np(l)
+
+    # -- bookkeeping --------------------------------------------------------------------------
+    def table_np(self, l):
+        """Layer l's page_table [E+S][3] as the kernels must see it now."""
+        E, S = self.cfg.E, self.cfg.S
+        pt = self.adj.page_table(l)
+        out = np.full((E + S, 3), -1, np.int32)
+        has = pt[:, 0] >= 0
+        out[:E][has] = pt[has] + self.base
+        for s_ in range(S):
+            out[E + s_] = [3 * (l * S + s_) + j for j in range(3)]
+        return out
+
+    def round(self, kv_need: int):
+        """The round before a step: KV pages first, then the adjuster on what is left.  Added
+        experts start copying into their reserved pages at once, after the previous forward pass
+        (whose evictions may have freed those pages).  Returns (change records, R_b)."""
+        take, back, short = kv_round(len(self.kv), int(kv_need), self.adj.free_pages())
+        if back:
+            self.adj.give_back(self.kv[-back:])
+            del self.kv[-back:]
+        if take:
+            self.kv += self.adj.lend(take).tolist()
+        changes = self.adj.decide(short)
+        self.filling = [False] * self.L
+        adds = changes[changes[:, 0] == 1]
+        for l in np.unique(adds[:, 1]) if len(adds) else []:
+            mine = adds[adds[:, 1] == l]
+            pm.fill_pages_async(self.plan, [self.host[int(e)] for e in mine[:, 2]],
+                                (mine[:, 3:6] + self.base).tolist(), self.fill_stream,
+                                after=self.fwd_done, copy_done=self.fill_done[int(l)])
+            self.filling[int(l)] = True
+            self.filled_experts += len(mine)
+        return changes, short
+
+    def resident(self, l):
+        return self.adj.page_table(l)[:, 0] >= 0
+
+    def schedule(self, logits_np):
+        """Per layer: the routed experts without pages this round, their slots in buffer l % 2
+        and the buf_slot table (device)."""
+        E = self.cfg.E
+        sched = []
+        for l in range(self.L):
+            off = np.nonzero(~self.resident(l))[0]
+            need = np.intersect1d(routed_experts(logits_np[l], self.cfg.k), off)
+            bs = np.full(E, -1, np.int32)
+            slots = np.arange(len(need), dtype=np.int32)
+            bs[need] = (l % 2) * self.slots + slots
+            sched.append((need, slots, torch.from_numpy(bs).to(self.device)))
+        return sched
+
+    def prefetch(self, l, sched_l):
+        need, slots, _ = sched_l
+        b = l % 2
+        pm.prefetch_async(self.plan, b, [self.host[int(e)] for e in need], slots,
+                          self.copy_stream, buf_free=self.free[b], copy_done=self.ready[b])
+
+    # -- one step -----------------------------------------------------------------------------
+    def step(self, x0, logits_dev, sched, acts, ws):
+        """All layers on x0 with this round's placement; ends the round's forward pass (the
+        adjuster releases evicted experts' pages, to be reused after `fwd_done`)."""
+        cur = torch.cuda.current_stream()
+        self.prefetch(0, sched[0])
+        x = x0
+        for l in range(self.L):
+            if l + 1 < self.L:
+                self.prefetch(l + 1, sched[l + 1])
+            if self.filling[l]:
+                cur.wait_event(self.fill_done[l])           # copy before the table points there
+            t = self.table_np(l)
+            if not np.array_equal(t, self.uploaded[l]):
+                self.upload_done[l].synchronize()           # the staging copy is free again
+                self.table_host[l].numpy()[:] = t
+                self.tables[l].copy_(self.table_host[l], non_blocking=True)
+                self.upload_done[l].record(cur)
+                self.uploaded[l] = t
+            cur.wait_event(self.ready[l % 2])
+            out = acts[l % 2]
+            self.plan.forward(x, logits_dev[l], self.tables[l], sched[l][2], out=out, workspace=ws)
+            self.free[l % 2].record(cur)
+            x = out
+        self.fwd_done.record(cur)
+        self.adj.end_forward()
         return x

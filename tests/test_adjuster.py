@@ -256,3 +256,40 @@ def test_native_argument_checks(lib):
     assert a.free_pages() == free + 2
     with pytest.raises(_lib.PmoeError):
         a.page_table(3)
+
+
+# ---- part 3: the round protocol around it (host bookkeeping of the elastic stack) -----------
+
+def test_kv_round():
+    from paged_moe_expert_gb300.pipeline import kv_round
+    assert kv_round(0, 0, 5) == (0, 0, 0)
+    assert kv_round(0, 10, 4) == (4, 0, 6)        # lend what is free, the rest is R_b
+    assert kv_round(10, 3, 0) == (0, 7, 0)        # demand fell: give pages back
+    assert kv_round(2, 5, 9) == (3, 0, 0)
+
+
+def test_constant_kv_demand_is_met_within_a_few_rounds():
+    """With the oracle adjuster and the round protocol (KV first, then the adjuster, pages of
+    evicted experts free after the pass), a constant demand that the evictable experts can cover
+    stops being short after a few rounds, and a demand that drops to zero lets the cache grow
+    back until fewer than 12 pages are free (below that floor((F_b - 9) / 3) adds nothing)."""
+    from paged_moe_expert_gb300.pipeline import kv_round
+    rng = np.random.default_rng(5)
+    L, E, limit = 6, 10, 6
+    probs = rng.dirichlet(np.ones(E), size=L).astype(np.float32)
+    o = AdjusterOracle(probs, [E] * L, limit, 3 * E * L + 4)
+    held, shorts = 0, []
+    for need in [60] * 12 + [0] * 30:
+        take, back, short = kv_round(held, need, o.free_pages())
+        held += take - back
+        if take:
+            o.lend(take)
+        if back:
+            lent = [p for p, own in enumerate(o.owner) if own == ("lent",)]
+            o.give_back(lent[-back:])
+        o.decide(short)
+        o.end_forward()
+        shorts.append(short)
+    assert shorts[0] > 0 and shorts[11] == 0
+    assert o.free_pages() < 12 and o.free_pages() == 4 + 3 * (E * L - sum(o.kept))
+    assert sum(o.kept) < E * L  # 4 spare pages + 2 missing experts = 10 free: inside the gap

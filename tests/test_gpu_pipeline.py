@@ -65,3 +65,48 @@ def test_schedule_points_needed_experts_at_alternating_buffers():
         assert (bs[need] // st.slots == l % 2).all()
         assert sorted((bs[need] % st.slots).tolist()) == list(range(len(need)))
         assert (bs[np.setdiff1d(np.arange(8), need)] == -1).all()
+
+
+def test_elastic_stack_follows_the_adjuster_and_equals_resident_stack():
+    """One pool for all layers and the KV cache; a KV demand trace makes the adjuster evict and
+    add experts between steps.  Every step's output equals the all-resident stack's, and after
+    every step each layer's table points at pages that hold exactly its resident experts."""
+    from paged_moe_expert_gb300 import pool as pl
+    cfg = syn.custom_config("elastic", d=256, f=256, E=8, k=2, S=1, n_buffered=0)
+    w = syn.make_weights(cfg)
+    L, T = 4, 24
+    rng = np.random.default_rng(7)
+    probs = rng.dirichlet(np.full(cfg.E, 0.5), size=L).astype(np.float32)
+    cached = [6, 5, 7, 8]
+    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, cached, offload_limit=4,
+                                        expert_pages=3 * sum(cached) + 6)
+    res = pipeline.DecodeStack(cfg, w, L, n_offload=0, layouts=1, seed=2)
+    kv_trace = [0, 9, 30, 30, 0, 0, 12, 40, 0, 0]
+    hidden_np = syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(np.float32))
+    hidden = torch.from_numpy(hidden_np.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = pm.alloc_workspace(stack.desc, T)
+    acts = [torch.empty_like(hidden) for _ in range(2)]
+    kinds = set()
+    for s, need in enumerate(kv_trace):
+        lg = [syn.bf16_bits_to_f32(syn.to_bf16_bits(rng.standard_normal((T, cfg.E)).astype(np.float32)))
+              for _ in range(L)]
+        changes, short = stack.round(need)
+        kinds |= set(changes[:, 0].tolist())
+        sched = stack.schedule(lg)
+        lg_dev = [torch.from_numpy(x).cuda() for x in lg]
+        y = stack.step(hidden, lg_dev, sched, acts, ws)
+        torch.cuda.synchronize()
+        want = run(res, hidden, [lg], T)[0]
+        assert np.array_equal(out_bits(y), want), "step %d" % s
+        for l in range(L):
+            t = stack.tables[l].cpu().numpy()
+            assert np.array_equal(t, stack.uploaded[l])
+            for e in range(cfg.E + cfg.S):
+                if t[e, 0] < 0:
+                    continue
+                got = pl.read_expert(stack.pool, stack.bufs, t, np.full(cfg.E, -1), e, cfg.f,
+                                     cfg.d, stack.slots)
+                for g, m in zip(got, pl.expert_matrices(w, e, cfg.E, cfg.f)):
+                    assert np.array_equal(g, m), (s, l, e)
+    assert kinds == {1, -1}, "the trace must make the adjuster both add and evict"
+    assert stack.filled_experts > 0
