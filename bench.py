@@ -370,6 +370,75 @@ def decode_sweep(args):
         torch.cuda.empty_cache()
 
 
+def vmm_overhead(args):
+    """The page lookup against the rival remapped view (FluxMoE's PagedTensor: physical blocks
+    mapped under stable virtual addresses with the CUDA driver's VMM calls, the contiguous kernel
+    unchanged) and against an ordinary contiguous allocation, on the layer shapes whose expert
+    page is a whole number of VMM blocks.  All experts resident, the page table a random
+    permutation of the blocks; CUDA-graph replay, L2 flushed before every timed call.  One JSON
+    line per (layer, tokens)."""
+    import paged_moe_expert_gb300 as pm
+    from paged_moe_expert_gb300 import pool as pl
+    from paged_moe_expert_gb300 import vmm as vm
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    g = vm.granularity(0)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    for cname in ("qwen3next", "mixtral", "qwen15"):
+        cfg = syn.CONFIGS[cname]
+        E, S, f, d = cfg.E, cfg.S, cfg.f, cfg.d
+        page = f * d * 2
+        if page % g:
+            print(json.dumps({"metric": "remapped view vs page lookup", "config": {"workload": cfg.name},
+                              "skipped": "expert page of %d bytes is not a multiple of the %d-byte VMM "
+                                         "granularity" % (page, g)}), flush=True)
+            continue
+        w = syn.make_weights(cfg)
+        n = 3 * (E + S)
+        v = vm.VmmView(page, n, n)
+        pt = np.random.default_rng(5).permutation(n).astype(np.int32).reshape(E + S, 3)
+        desc = pm.make_desc(d, f, E, cfg.k, cfg.renormalize, S, 1)
+        plan_b = pm.Plan(desc, v.blocks, n)
+        host = [torch.from_numpy(pl.pack_expert(w, e, E, f).view(np.int16)).pin_memory()
+                for e in range(E + S)]
+        cs = torch.cuda.Stream()
+        pm.fill_pages_async(plan_b, host, pt.tolist(), cs)
+        cs.synchronize()
+        del host
+        vm.map_experts(v, pt)
+        assert (v.lookup() >= 0).all()
+        plan_v = pm.Plan(desc, v.view, n)
+        cw = pl.contiguous_weights(cfg, w, device)
+        plan_c = pm.Plan(desc, cw, n)
+        ptd = torch.from_numpy(pt).to(device)
+        bs = torch.full((E,), -1, dtype=torch.int32, device=device)
+        for T in cfg.tokens:
+            h, lg = syn.make_tokens(cfg, T)
+            hd, ld = pl._bf16(h).to(device), torch.from_numpy(lg).to(device)
+            ws = pm.alloc_workspace(desc, T, device)
+            o = torch.empty_like(hd)
+            fp = lambda: plan_b.forward(hd, ld, ptd, bs, out=o, workspace=ws)  # noqa: E731
+            fv = lambda: plan_v.contig_forward(hd, ld, out=o, workspace=ws)  # noqa: E731
+            fc = lambda: plan_c.contig_forward(hd, ld, out=o, workspace=ws)  # noqa: E731
+            for _ in range(3):
+                fp(); fv(); fc()
+            path = plan_b.last_run()[0]
+            gp, gv, gc = capture(fp), capture(fv), capture(fc)
+            tp, tv, tc = time_iters([gp.replay, gv.replay, gc.replay], args.sweep_iters, flush)
+            assert plan_b.device_error() == 0
+            print(json.dumps({
+                "metric": "remapped view vs page lookup",
+                "config": {"workload": "%s layer forward, T=%d tokens, all experts resident, "
+                           "pages scattered over %d blocks of %d bytes" % (cfg.name, T, n, page)},
+                "path": PATH_NAMES[path], "paged_ms": tp * 1e3, "remapped_view_ms": tv * 1e3,
+                "contiguous_alloc_ms": tc * 1e3, "paged_vs_view": tp / tv - 1.0,
+                "paged_vs_alloc": tp / tc - 1.0, "view_vs_alloc": tv / tc - 1.0}), flush=True)
+            del ws, o
+        del plan_v, plan_b, plan_c, cw
+        v.close()
+        torch.cuda.empty_cache()
+
+
 def elastic_sweep(args):
     """24 Qwen1.5-MoE-shaped layers on ONE page pool shared with the KV cache.  A KV demand
     trace (in expert pages) rises and falls over the rounds; each round the KV pages are taken
@@ -461,6 +530,8 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--tokens-list", default="1,4,16,64,256")
     ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
+    ap.add_argument("--vmm-overhead", action="store_true",
+                    help="page lookup vs remapped contiguous view vs contiguous allocation")
     ap.add_argument("--elastic-sweep", action="store_true",
                     help="adjuster-driven 24-layer decode over a KV demand trace")
     ap.add_argument("--elastic-tokens", type=int, default=16)
@@ -472,6 +543,9 @@ def main():
         return
     if args.elastic_sweep:
         elastic_sweep(args)
+        return
+    if args.vmm_overhead:
+        vmm_overhead(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -245,6 +245,44 @@ pmoe_status pmoe_fill_pages_async(pmoe_plan_t plan, int32_t n, const void* const
                                   const int32_t* pages, pmoe_stream_t copy_stream,
                                   pmoe_event_t after, pmoe_event_t copy_done);
 
+/* ---- remapped contiguous view (the rival design to the page lookup) --------------------------
+ *
+ * FluxMoE (awesome-system-papers, section "核心方法", PagedTensor): instead of looking pages up
+ * inside the kernel, keep a stable virtual address range per logical weight tensor and map
+ * physical blocks under it with the CUDA driver's virtual memory calls before the kernel runs,
+ * so an unmodified contiguous kernel reads scattered physical memory.  Invariants it states:
+ * stable virtual addresses; a virtual page maps at most one physical block at a time; a block is
+ * reused only after every kernel reading it has finished; the blocks form a fixed pool.
+ *
+ * Here one block is one expert page (f*d bf16), which must be a multiple of the device's VMM
+ * granularity (pmoe_vmm_granularity; 2 MiB pages for d=2048, f=512 or d=4096, f=14336, not for
+ * d=2048, f=1408).  pmoe_vmm_create allocates n_blocks physical blocks and reserves two device
+ * address ranges: `blocks` maps block i at offset i*block_bytes (all blocks, for the page-table
+ * forward) and `view` holds n_virtual virtual pages, unmapped at first (for moe_contig_forward,
+ * expert e's matrix j at virtual page 3e+j).  Both ranges alias the same physical bytes: no
+ * copy.  Reading an unmapped virtual page faults the GPU, so a caller launches a kernel on the
+ * view only once every page that kernel can read is mapped (pmoe_vmm_lookup).  All calls are
+ * host calls; they allocate device memory only in pmoe_vmm_create and free it in
+ * pmoe_vmm_destroy. */
+typedef struct pmoe_vmm* pmoe_vmm_t;
+
+/* Smallest block size (bytes) the device's VMM maps, or 0 with a status on error. */
+pmoe_status pmoe_vmm_granularity(int32_t device, size_t* bytes);
+pmoe_status pmoe_vmm_create(int32_t device, size_t block_bytes, int64_t n_blocks, int64_t n_virtual,
+                            pmoe_vmm_t* out);
+pmoe_status pmoe_vmm_destroy(pmoe_vmm_t vmm);
+/* Device pointers of the two ranges (either may be NULL). */
+pmoe_status pmoe_vmm_pointers(pmoe_vmm_t vmm, void** blocks, void** view);
+/* Map block blocks[i] under virtual page virt[i] for i < n (PMOE_ERR_INVALID_ARG, nothing
+ * mapped, if a virtual page is already mapped, listed twice or out of range). */
+pmoe_status pmoe_vmm_map(pmoe_vmm_t vmm, int64_t n, const int64_t* virt, const int64_t* blocks);
+/* Unmap virtual pages virt[i] once `readers_done` (the last kernel reading them; may be NULL)
+ * has completed, waiting on the host for at most timeout_ms (PMOE_ERR_TIMEOUT, nothing unmapped). */
+pmoe_status pmoe_vmm_unmap(pmoe_vmm_t vmm, int64_t n, const int64_t* virt,
+                           pmoe_event_t readers_done, int32_t timeout_ms);
+/* The block under each virtual page (-1: unmapped), host int64 [n_virtual]. */
+pmoe_status pmoe_vmm_lookup(pmoe_vmm_t vmm, int64_t* block_of);
+
 /* ---- the adjuster: which experts each layer keeps in the page pool -------------------------
  *
  * Host only (no device work).  Rimuru, section "The adjuster: when to evict an expert, and which

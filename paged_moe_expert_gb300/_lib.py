@@ -51,6 +51,13 @@ SIGNATURES = {
     "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),
     "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P, P]),
     "pmoe_align_scratch_size": (SZ, []),
+    "pmoe_vmm_granularity": (ctypes.c_int, [I32, ctypes.POINTER(SZ)]),
+    "pmoe_vmm_create": (ctypes.c_int, [I32, SZ, I64, I64, ctypes.POINTER(P)]),
+    "pmoe_vmm_destroy": (ctypes.c_int, [P]),
+    "pmoe_vmm_pointers": (ctypes.c_int, [P, ctypes.POINTER(P), ctypes.POINTER(P)]),
+    "pmoe_vmm_map": (ctypes.c_int, [P, I64, P, P]),
+    "pmoe_vmm_unmap": (ctypes.c_int, [P, I64, P, P, I32]),
+    "pmoe_vmm_lookup": (ctypes.c_int, [P, P]),
     "pmoe_adjuster_create": (ctypes.c_int, [I32, I32, P, I32, P, I64, ctypes.POINTER(P)]),
     "pmoe_adjuster_destroy": (ctypes.c_int, [P]),
     "pmoe_adjuster_decide": (ctypes.c_int, [P, I32, I32, P, ctypes.POINTER(I32)]),
