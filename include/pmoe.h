@@ -283,6 +283,41 @@ pmoe_status pmoe_vmm_unmap(pmoe_vmm_t vmm, int64_t n, const int64_t* virt,
 /* The block under each virtual page (-1: unmapped), host int64 [n_virtual]. */
 pmoe_status pmoe_vmm_lookup(pmoe_vmm_t vmm, int64_t* block_of);
 
+/* ---- three tiers of pages over one pool -----------------------------------------------------
+ *
+ * Rimuru, section "One pool for data whose sizes differ by orders of magnitude": the pool is one
+ * byte range read through views with different page sizes.  Huge pages (size lcm(expert page,
+ * SSM page), or the expert page without SSM state) split on demand into middle pages (expert or
+ * SSM pages, one kind per huge page); an expert page splits into small pages (KV cache or
+ * convolution-state pages, one kind per split page).  A small page comes from, in order: a free
+ * small page of the same kind in a split page that already holds a live page of the same owner
+ * (the request: pages of one request are freed together), any free small page of that kind, a
+ * free expert page split for it, a free huge page split into expert pages first.  A huge page is
+ * never cut straight into small pages.  A middle page comes from a free page of its kind, else a
+ * split huge page.  Ties go to the lowest byte offset.  Freeing runs upward: a split expert page
+ * whose small pages are all free is an expert page again, and a huge page whose middle pages are
+ * all free returns to the huge pages.
+ *
+ * Sizes in bytes: expert_page > 0; ssm_page >= 0 (0: none); kv_page and conv_page (0: none) must
+ * divide expert_page.  pool_bytes / huge page is the number of huge pages (the rest is unused).
+ * Offsets are byte offsets into the pool; an expert page at offset o is page o / expert_page of
+ * the kernels' page pool.  Host only; the caller owns the pool memory. */
+typedef struct pmoe_tiers* pmoe_tiers_t;
+enum { PMOE_PAGE_EXPERT = 0, PMOE_PAGE_SSM = 1, PMOE_PAGE_KV = 2, PMOE_PAGE_CONV = 3 };
+
+pmoe_status pmoe_tiers_create(int64_t pool_bytes, int64_t expert_page, int64_t ssm_page,
+                              int64_t kv_page, int64_t conv_page, pmoe_tiers_t* out);
+pmoe_status pmoe_tiers_destroy(pmoe_tiers_t t);
+/* One page of `kind` for `owner` (owner matters for small pages only): *offset = its byte offset,
+ * or -1 when the pool has no room (not an error). */
+pmoe_status pmoe_tiers_alloc(pmoe_tiers_t t, int32_t kind, int64_t owner, int64_t* offset);
+/* Return a live page (PMOE_ERR_INVALID_ARG, nothing changed, if `offset` is not a live page of
+ * `kind`). */
+pmoe_status pmoe_tiers_free(pmoe_tiers_t t, int32_t kind, int64_t offset);
+/* counts[8]: huge page bytes, free huge pages, free expert pages, free SSM pages, live expert
+ * pages, live SSM pages, split expert pages, free small pages (KV + conv). */
+pmoe_status pmoe_tiers_stats(pmoe_tiers_t t, int64_t* counts);
+
 /* ---- the adjuster: which experts each layer keeps in the page pool -------------------------
  *
  * Host only (no device work).  Rimuru, section "The adjuster: when to evict an expert, and which

@@ -58,6 +58,11 @@ SIGNATURES = {
     "pmoe_vmm_map": (ctypes.c_int, [P, I64, P, P]),
     "pmoe_vmm_unmap": (ctypes.c_int, [P, I64, P, P, I32]),
     "pmoe_vmm_lookup": (ctypes.c_int, [P, P]),
+    "pmoe_tiers_create": (ctypes.c_int, [I64, I64, I64, I64, I64, ctypes.POINTER(P)]),
+    "pmoe_tiers_destroy": (ctypes.c_int, [P]),
+    "pmoe_tiers_alloc": (ctypes.c_int, [P, I32, I64, ctypes.POINTER(I64)]),
+    "pmoe_tiers_free": (ctypes.c_int, [P, I32, I64]),
+    "pmoe_tiers_stats": (ctypes.c_int, [P, P]),
     "pmoe_adjuster_create": (ctypes.c_int, [I32, I32, P, I32, P, I64, ctypes.POINTER(P)]),
     "pmoe_adjuster_destroy": (ctypes.c_int, [P]),
     "pmoe_adjuster_decide": (ctypes.c_int, [P, I32, I32, P, ctypes.POINTER(I32)]),
