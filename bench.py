@@ -439,6 +439,67 @@ def vmm_overhead(args):
         torch.cuda.empty_cache()
 
 
+def codec_bench(args):
+    """Exponent-only Huffman pages (FluxMoE's compressed GPU backend): the buffered experts of the
+    Qwen1.5-MoE-shaped layer (15 experts, 45 pages) encoded on the host, decoded on the GPU into a
+    load buffer in one launch; against copying the same pages uncompressed from pinned host
+    memory.  One JSON line."""
+    import paged_moe_expert_gb300 as pm
+    from paged_moe_expert_gb300 import expcodec as nc
+    from paged_moe_expert_gb300 import pool as pl
+    torch.cuda.set_device(0)
+    cfg = syn.CONFIGS["qwen15"]
+    w = syn.make_weights(cfg)
+    E, f, d = cfg.E, cfg.f, cfg.d
+    page = f * d
+    n_exp = cfg.n_buffered
+    mats = [m for e in range(n_exp) for m in pl.expert_matrices(w, e, E, f)]
+    t0 = time.time()
+    blobs_h = [nc.encode(m) for m in mats]
+    enc_s = time.time() - t0
+    comp = sum(b.size for b in blobs_h)
+    blobs = [torch.from_numpy(b).cuda() for b in blobs_h]
+    buf = torch.empty(len(mats) * page, dtype=torch.bfloat16, device="cuda")
+    dsts = [buf[i * page:(i + 1) * page] for i in range(len(mats))]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        nc.decode_async(blobs, page, dsts, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ok = all(np.array_equal(dsts[i].cpu().view(torch.int16).numpy().view(np.uint16), mats[i].reshape(-1))
+             for i in (0, len(mats) - 1))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    times = []
+    for _ in range(args.sweep_iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        nc.decode_async(blobs, page, dsts)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    dec = statistics.median(times)
+    host = torch.from_numpy(np.concatenate([m.reshape(-1) for m in mats]).view(np.int16)).pin_memory()
+    raw = len(mats) * page * 2
+    h2d = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        buf.view(torch.int16).copy_(host, non_blocking=True)
+        b.record()
+        b.synchronize()
+        h2d.append(a.elapsed_time(b) * 1e-3)
+    h2d_s = statistics.median(h2d)
+    print(json.dumps({
+        "metric": "exponent-only Huffman decode of bf16 expert pages",
+        "config": {"workload": "%d Qwen1.5-MoE-shaped expert pages (%d experts x W1, W3, W2), "
+                   "%d bf16 values each, one launch, L2 flushed" % (len(mats), n_exp, page)},
+        "compressed_ratio": comp / raw, "encode_host_s": enc_s,
+        "decode_ms": dec * 1e3, "decoded_gbs": raw / dec / 1e9,
+        "decode_hbm_traffic_gbs": (raw + comp) / dec / 1e9,
+        "h2d_uncompressed_ms": h2d_s * 1e3, "h2d_gbs": raw / h2d_s / 1e9, "bit_exact": ok}), flush=True)
+
+
 def elastic_sweep(args):
     """24 Qwen1.5-MoE-shaped layers on ONE page pool shared with the KV cache.  A KV demand
     trace (in expert pages) rises and falls over the rounds; each round the KV pages are taken
@@ -530,6 +591,8 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--tokens-list", default="1,4,16,64,256")
     ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
+    ap.add_argument("--codec", action="store_true",
+                    help="exponent-only Huffman decode of expert pages vs the host copy")
     ap.add_argument("--vmm-overhead", action="store_true",
                     help="page lookup vs remapped contiguous view vs contiguous allocation")
     ap.add_argument("--elastic-sweep", action="store_true",
@@ -546,6 +609,9 @@ def main():
         return
     if args.vmm_overhead:
         vmm_overhead(args)
+        return
+    if args.codec:
+        codec_bench(args)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

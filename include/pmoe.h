@@ -283,6 +283,31 @@ pmoe_status pmoe_vmm_unmap(pmoe_vmm_t vmm, int64_t n, const int64_t* virt,
 /* The block under each virtual page (-1: unmapped), host int64 [n_virtual]. */
 pmoe_status pmoe_vmm_lookup(pmoe_vmm_t vmm, int64_t* block_of);
 
+/* ---- exponent-only Huffman compression of bf16 expert pages ----------------------------------
+ *
+ * FluxMoE (awesome-system-papers, section "核心方法", observation 3 and the compressed GPU
+ * backend): bf16 expert weights keep sign and mantissa as they are and Huffman-code the 8-bit
+ * exponent, whose entropy is low; the GPU decompresses before the weights are read.  Format (the
+ * page fixes none): per page of n values, code lengths [256], n, stream bits, a 4096-entry decode
+ * table (symbol | length << 8 for the next 12 stream bits), chunk start bits (one per 256 values),
+ * the sign|mantissa bytes and the exponent stream (32-bit words, bit 31 first, two zero words
+ * after it); sections 16-byte aligned.  Codes are canonical Huffman codes of at most 12 bits.
+ * Lossless: decoding gives back every bit pattern (NaN, infinities, subnormals included). */
+
+/* Bytes pmoe_exp_encode may write for n values. */
+size_t pmoe_exp_encode_bound(int64_t n);
+/* Host encoder: values (host bf16 bit patterns) -> out (host, cap >= pmoe_exp_encode_bound(n));
+ * *bytes = the blob's size.  n * 12 must stay below 2^32. */
+pmoe_status pmoe_exp_encode(const uint16_t* values, int64_t n, void* out, size_t cap, size_t* bytes);
+/* GPU decoder: decode n_pages blobs (device, 16-byte aligned, src_bytes[i] bytes each, every one of
+ * n values) into dst[i] (device, 16-byte aligned, n bf16) on `stream`, one thread per 256 values.
+ * src, src_bytes and dst are host arrays, n_pages <= 128.  A blob whose header does not match n or
+ * its size sets *device_error (device int32, may be NULL) to PMOE_ERR_INVALID_ARG and leaves its
+ * chunks unwritten. */
+pmoe_status pmoe_exp_decode_async(int32_t n_pages, int64_t n, const void* const* src,
+                                  const int64_t* src_bytes, void* const* dst, int32_t* device_error,
+                                  pmoe_stream_t stream);
+
 /* ---- three tiers of pages over one pool -----------------------------------------------------
  *
  * Rimuru, section "One pool for data whose sizes differ by orders of magnitude": the pool is one

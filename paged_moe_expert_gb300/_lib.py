@@ -58,6 +58,9 @@ SIGNATURES = {
     "pmoe_vmm_map": (ctypes.c_int, [P, I64, P, P]),
     "pmoe_vmm_unmap": (ctypes.c_int, [P, I64, P, P, I32]),
     "pmoe_vmm_lookup": (ctypes.c_int, [P, P]),
+    "pmoe_exp_encode_bound": (SZ, [I64]),
+    "pmoe_exp_encode": (ctypes.c_int, [P, I64, P, SZ, ctypes.POINTER(SZ)]),
+    "pmoe_exp_decode_async": (ctypes.c_int, [I32, I64, ctypes.POINTER(P), P, ctypes.POINTER(P), P, P]),
     "pmoe_tiers_create": (ctypes.c_int, [I64, I64, I64, I64, I64, ctypes.POINTER(P)]),
     "pmoe_tiers_destroy": (ctypes.c_int, [P]),
     "pmoe_tiers_alloc": (ctypes.c_int, [P, I32, I64, ctypes.POINTER(I64)]),
