@@ -76,6 +76,14 @@ constexpr int kSwapMaxTokensPerExpert = 24;
 constexpr int kPairMinTokensPerExpert = 64;
 constexpr int kPairMaxExperts = 128;
 constexpr int kPrepSmallMaxTokens = 128;
+// The one-CTA prep routes every token on one SM; its routing work grows with tokens x logits per
+// lane x k.  Past this (the Qwen1.5-MoE-shaped layer at 128 tokens) the routing kernel's many CTAs
+// and a separate sort win: 512 experts top-10 at 64 tokens took 36 us in the prep.
+constexpr int64_t kPrepSmallRouteWork = 128 * 2 * 4;
+
+static bool use_prep_small(int T, int E, int k) {
+    return T <= kPrepSmallMaxTokens && (int64_t)T * ((E + 31) / 32) * k <= kPrepSmallRouteWork;
+}
 
 static int stream_splits(const pmoe_layer_desc& D) {
     return (D.f + kStreamKChunk - 1) / kStreamKChunk;
@@ -320,8 +328,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
-    const bool gather_in_prep = T <= kPrepSmallMaxTokens && tc_family && W.np * D.d * 2 <= 64 * 1024;
-    if (T <= kPrepSmallMaxTokens) {
+    const bool prep = use_prep_small(T, D.num_experts, D.top_k);
+    const bool gather_in_prep = prep && tc_family && W.np * D.d * 2 <= 64 * 1024;
+    if (prep) {
         // one CTA: routing, sort + pad + page resolution
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_prep_small(logits, T, D.num_experts, D.top_k, D.renormalize, ids, w,
@@ -421,7 +430,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
     P->last_kernels = ev - 1;
-    P->last_launches = ev - 1 + (T > kPrepSmallMaxTokens && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
+    P->last_launches = ev - 1 + (!prep && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
     return PMOE_OK;
 }
 
