@@ -160,6 +160,7 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.part = o;   o = align256(o + align_part_bytes());
     W.units = o;  o = align256(o + sizeof(int4) * W.nblk_max);
     W.unit_w2 = o; o = align256(o + sizeof(int32_t) * W.nblk_max);
+    W.brows = o;  o = align256(o + sizeof(int32_t) * W.nblk_max);
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
     const size_t y_tc = sizeof(float) * (size_t)cap_tc * D.d;
@@ -325,6 +326,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         rs.units = units;
         rs.unit_w2 = unit_w2;
     }
+    int32_t* brows = at<int32_t>(ws, W.brows);
+    if (path == PMOE_PATH_TC) rs.block_rows = brows;
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
@@ -363,13 +366,20 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     int64_t ystride;
     int splits;
     if (path == PMOE_PATH_TC) {
+        // blocks mostly padding (few tokens per expert) load only their rows, 16 at a time
+        CUtensorMap x16, h16, hid16;
+        if (!encode_rows_map(&x16, x, cap_tc, D.d, 16) || !encode_rows_map(&h16, h, cap_tc, D.f, 16) ||
+            (sh.direct && !encode_rows_map(&hid16, hidden, T, D.d, 16)))
+            return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(1, contig, xmap, P->tm_rows_d, bexp, meta, loc, h, cap_tc, D.f, D.d,
-                                 nblk, P->num_sms, P->d_error, stream, hidp, sh),
+                                 nblk, P->num_sms, P->d_error, stream, hidp, sh, brows, &x16,
+                                 sh.direct ? &hid16 : nullptr),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm(2, contig, hmap, P->tm_rows_f, bexp, meta, loc, y, cap_tc, D.f, D.d,
-                                 nblk, P->num_sms, P->d_error, stream), "down gemm");
+                                 nblk, P->num_sms, P->d_error, stream, nullptr, SharedRows{}, brows,
+                                 &h16, nullptr), "down gemm");
         ystride = cap_tc;
         splits = 1;
     } else if (path == PMOE_PATH_TC2) {

@@ -29,7 +29,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, brows, x, h, y, total;
     size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
@@ -148,6 +148,9 @@ struct ResolveArgs {
     // count in meta[kMetaPairs], single-block units in meta[kMetaSingles]
     int4* units;
     int32_t* unit_w2;
+    // optional (NULL: not written): valid rows of each sorted block, 1..block_m (the last block of
+    // an expert holds its remainder, the others are full)
+    int32_t* block_rows;
 };
 
 // An ExpertLoc in one word, (map << 29) | page, or -1 for none (pages of a pool or a buffer are
@@ -223,7 +226,8 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
                            int32_t* err, cudaStream_t s, const CUtensorMap* hid = nullptr,
-                           SharedRows sh = SharedRows{});
+                           SharedRows sh = SharedRows{}, const int32_t* block_rows = nullptr,
+                           const CUtensorMap* act16 = nullptr, const CUtensorMap* hid16 = nullptr);
 
 // CTA-pair tensor-core path (tc_gemm2sm.cu): the work units of `units`/`unit_w2` (count
 // meta[kMetaPairs], written by the sort): a pair of consecutive 128-row blocks of one expert, or

@@ -205,6 +205,9 @@ __device__ __forceinline__ void align_block(
         const int o = off[e], c = cnt[e], end = off[e + 1];
         for (int r = o + c; r < end; ++r) sorted_ids[r] = (int32_t)NP;
         for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
+        if (rs.block_rows)
+            for (int b = o / block_m; b < end / block_m; ++b)
+                rs.block_rows[b] = min(block_m, o + c - b * block_m);
     }
     if (tid == 0) meta[kMetaNPadded] = off[ES];
     if (rs.units) {
@@ -360,6 +363,9 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
         const int o = off[e], n = cnt[e], end = off[e + 1];
         for (int r = o + n; r < end; ++r) sorted_ids[r] = (int32_t)NP;
         for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
+        if (rs.block_rows)
+            for (int bb = o / block_m; bb < end / block_m; ++bb)
+                rs.block_rows[bb] = min(block_m, o + n - bb * block_m);
     }
     if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
     if (c == 0 && rs.units) {

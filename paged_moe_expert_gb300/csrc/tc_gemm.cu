@@ -79,6 +79,7 @@ struct TcArgs {
     int n_tiles;        // N tiles per sorted block
     int32_t* err;
     SharedRows sh;         // gate/up: shared-chunk blocks straight from hidden
+    const int32_t* block_rows;   // valid rows of each block (NULL: all 128)
 };
 
 struct TcMaps {
@@ -86,7 +87,14 @@ struct TcMaps {
     CUtensorMap w[3];   // weights of pool / load buffer 0 / load buffer 1
     CUtensorMap hid;    // hidden [T][d] (128-row boxes), when args.sh.direct
     CUtensorMap y;      // down: y bf16 [cap][d], 32-row x 64-column boxes, 128-byte swizzle
+    CUtensorMap a16;    // the activation views with 16-row boxes (blocks with few valid rows)
+    CUtensorMap hid16;
 };
+
+// Valid rows of block mb: the remainder of an expert's rows in its last block, 128 elsewhere.
+__device__ __forceinline__ int valid_rows(const TcArgs& A, int mb) {
+    return A.block_rows ? A.block_rows[mb] : BM;
+}
 
 template <bool kContig>
 __device__ __forceinline__ ExpertLoc tile_loc(const ExpertLoc* loc, int e, int j) {
@@ -170,20 +178,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int npad = args.meta[kMetaNPadded];
             for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const int mb = block_of(t), nt = (int)(t % args.n_tiles);
+                const int rows = valid_rows(args, mb);
                 ExpertLoc l0, l1;
                 if (!tile_weights<kMode, kContig>(args, mb, l0, l1)) continue;
                 const CUtensorMap* w0 = &maps.w[l0.map];
                 const CUtensorMap* w1 = &maps.w[l1.map];
-                // the tile's token rows: sorted rows, or hidden itself for a shared-chunk block
-                const CUtensorMap* am = &maps.a;
+                // the tile's token rows: sorted rows, or hidden itself for a shared-chunk block;
+                // a block with fewer than 113 valid rows loads only those, in 16-row boxes (the
+                // MMA's other rows hold stale data and only feed output rows nothing reads)
+                const int n16 = (rows + 15) >> 4;
+                const bool part = n16 < BM / 16;
+                const CUtensorMap* am = part ? &maps.a16 : &maps.a;
                 int arow = mb * BM;
                 if (kMode == kGateUp && args.sh.direct) {
                     const int e = args.block_expert[mb];
                     if (e >= args.sh.E) {
-                        am = &maps.hid;
+                        am = part ? &maps.hid16 : &maps.hid;
                         arow = shared_token_row(args.sh, e, mb * BM, npad);
                     }
                 }
+                const uint32_t tx = (part ? (uint32_t)n16 * 16u * BK * 2u : (uint32_t)A_BYTES) + B_BYTES;
                 int row0, row1;
                 if (kMode == kGateUp) {
                     row0 = l0.page * args.f + nt * 128;   // W1 rows of output columns n0..n0+127
@@ -195,9 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < args.k_blocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) { ok = false; break; }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, tx);
                     const uint32_t sa = sbase + stage * STAGE_BYTES;
-                    tma_load_2d(sa, am, fb, kb * BK, arow);
+                    if (part) {
+                        for (int i = 0; i < n16; ++i)
+                            tma_load_2d(sa + (uint32_t)i * 16u * BK * 2u, am, fb, kb * BK, arow + 16 * i);
+                    } else {
+                        tma_load_2d(sa, am, fb, kb * BK, arow);
+                    }
                     tma_load_2d(sa + A_BYTES, w0, fb, kb * BK, row0);
                     tma_load_2d(sa + A_BYTES + B_HALF, w1, fb, kb * BK, row1);
                     pend_phase[stage] = (int)phase;
@@ -278,7 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && quad == 0) GTRACE(t, 6, globaltimer());
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
             const int64_t grow = (int64_t)mb * BM + row;
-            if (kMode == kGateUp) {
+            const int rows = valid_rows(args, mb);
+            if (quad * 32 >= rows) {
+                // no valid row in this warp's lanes: nothing to store
+            } else if (kMode == kGateUp) {
                 uint16_t* h = static_cast<uint16_t*>(args.out) + grow * args.f + nt * 128;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 128; c0 += 16) {
@@ -293,9 +315,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float a1 = silu_mul(g[2 * i + 1], u[2 * i + 1]);
                         p[i] = pack_bf16(a0, a1);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(h + c0);
-                    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    if (row < rows) {
+                        uint4* dst = reinterpret_cast<uint4*>(h + c0);
+                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                    }
                 }
             } else {
                 // bf16 rows through shared memory and TMA stores: each store writes whole
@@ -381,11 +405,16 @@ bool encode_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t col
 cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap* wmaps,
                            const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                            void* out, int64_t out_rows, int f, int d, int64_t nblk_max, int num_sms,
-                           int32_t* err, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
+                           int32_t* err, cudaStream_t s, const CUtensorMap* hid, SharedRows sh,
+                           const int32_t* block_rows, const CUtensorMap* act16,
+                           const CUtensorMap* hid16) {
     TcMaps maps;
     maps.a = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
     maps.hid = hid ? *hid : act;
+    maps.a16 = act16 ? *act16 : act;
+    maps.hid16 = hid16 ? *hid16 : maps.hid;
+    if (block_rows && (!act16 || (hid && !hid16))) return cudaErrorInvalidValue;
     maps.y = act;
     if (mode == kDown && !encode_rows_map(&maps.y, out, out_rows, d, 32)) return cudaErrorInvalidValue;
     TcArgs a{};
@@ -397,6 +426,7 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
     a.d = d;
     a.err = err;
     a.sh = hid ? sh : SharedRows{};
+    a.block_rows = block_rows;
     if (mode == kGateUp) {
         a.k_blocks = d / BK;
         a.n_tiles = f / 128;
