@@ -327,7 +327,7 @@ def decode_sweep(args):
     resident_ms = {}
     for frac in fractions:
         n_off = int(round((1.0 - frac) * cfg.E))
-        stack = pipeline.DecodeStack(cfg, w, L, n_off, layouts=4, seed=11)
+        stack = pipeline.DecodeStack(cfg, w, L, n_off, layouts=4, seed=11, backend=args.backend)
         for T in tokens_list:
             rng = np.random.default_rng(1000 + T)
             steps = args.warmup + args.steps
@@ -353,11 +353,13 @@ def decode_sweep(args):
             ms = e0.elapsed_time(e1) / args.steps
             if n_off == 0:
                 resident_ms[T] = ms
-            copy_ms = copied / args.steps / (h2d_gbs * 1e9) * 1e3
+            copy_ms = copied / args.steps / (h2d_gbs * 1e9) * 1e3 if args.backend == "host" else 0.0
             line = {"metric": "decode sweep: 24-layer step time with double-buffered expert prefetch",
                     "config": {"workload": "%d Qwen1.5-MoE-shaped layers, %d tokens/step" % (L, T),
                                "resident_fraction": frac, "offloaded_experts_per_layer": n_off,
-                               "pool_layouts_cycled": 4},
+                               "pool_layouts_cycled": 4,
+                               "offload_backend": ("pinned host memory" if args.backend == "host" else
+                                                   "exponent-Huffman blobs in device memory")},
                     "tokens": T, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
                     "copied_mb_per_step": copied / args.steps / 1e6,
                     "h2d_gbs": h2d_gbs, "copy_ms_per_step_est": copy_ms,
@@ -591,6 +593,8 @@ def main():
     ap.add_argument("--layers", type=int, default=24)
     ap.add_argument("--tokens-list", default="1,4,16,64,256")
     ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
+    ap.add_argument("--backend", default="host", choices=["host", "compressed"],
+                    help="decode sweep: where offloaded experts live")
     ap.add_argument("--codec", action="store_true",
                     help="exponent-only Huffman decode of expert pages vs the host copy")
     ap.add_argument("--vmm-overhead", action="store_true",

@@ -46,8 +46,12 @@ def routed_experts(logits: np.ndarray, k: int) -> np.ndarray:
 
 
 class DecodeStack:
+    """backend "host": offloaded experts live in pinned host memory and are copied in;
+    "compressed": they live in device memory as exponent-Huffman blobs (FluxMoE's compressed GPU
+    backend) and are decoded into the load buffer on the copy stream instead."""
+
     def __init__(self, cfg, weights, n_layers: int, n_offload: int, layouts: int = 4,
-                 device="cuda", seed: int = 0):
+                 device="cuda", seed: int = 0, backend: str = "host"):
         E, S, f, d = cfg.E, cfg.S, cfg.f, cfg.d
         self.cfg, self.L, self.n_off, self.layouts = cfg, n_layers, n_offload, layouts
         self.device = device
@@ -85,8 +89,19 @@ class DecodeStack:
             self.tables.append(row_tables)
         del src
         # pinned host copies of every routed expert (W1 | W3 | W2), shared by all layers
-        self.host = [torch.from_numpy(pl.pack_expert(weights, e, E, f).view(np.int16)).pin_memory()
-                     for e in range(E)]
+        if backend not in ("host", "compressed"):
+            raise ValueError("backend must be 'host' or 'compressed'")
+        self.backend = backend
+        self.host = None
+        if backend == "host":
+            self.host = [torch.from_numpy(pl.pack_expert(weights, e, E, f).view(np.int16)).pin_memory()
+                         for e in range(E)]
+        self.blobs = None
+        if backend == "compressed":
+            from paged_moe_expert_gb300 import expcodec
+            self.blobs = [[torch.from_numpy(expcodec.encode(m)).to(device)
+                           for m in pl.expert_matrices(weights, e, E, f)] for e in range(E)]
+            self.compressed_bytes = sum(b.numel() for row in self.blobs for b in row)
         self.copy_stream = torch.cuda.Stream(device=device)
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
@@ -108,8 +123,22 @@ class DecodeStack:
     def prefetch(self, l, sched_l):
         need, slots, _ = sched_l
         b = l % 2
-        pm.prefetch_async(self.plans[l][0], b, [self.host[int(e)] for e in need], slots,
-                          self.copy_stream, buf_free=self.free[b], copy_done=self.ready[b])
+        if self.backend == "host":
+            pm.prefetch_async(self.plans[l][0], b, [self.host[int(e)] for e in need], slots,
+                              self.copy_stream, buf_free=self.free[b], copy_done=self.ready[b])
+            return
+        from paged_moe_expert_gb300 import expcodec
+        page = self.cfg.f * self.cfg.d
+        if self.free[b].cuda_event != 0:
+            self.copy_stream.wait_event(self.free[b])          # WAR: the buffer's last reader
+        src, dst = [], []
+        for e, s_ in zip(need, slots):
+            for j in range(3):
+                src.append(self.blobs[int(e)][j])
+                dst.append(self.bufs[b][(3 * int(s_) + j) * page:(3 * int(s_) + j + 1) * page])
+        for i in range(0, len(src), 128):
+            expcodec.decode_async(src[i:i + 128], page, dst[i:i + 128], stream=self.copy_stream)
+        self.ready[b].record(self.copy_stream)                 # RAW: compute waits for it
 
     # -- one step -----------------------------------------------------------------------------
     def step(self, x0, logits_dev, sched, step_idx, acts, ws, first_prefetched=False):

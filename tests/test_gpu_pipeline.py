@@ -52,6 +52,27 @@ def test_prefetched_stack_equals_resident_stack(T):
     assert_close(a[0], ref, "4-layer chain")
 
 
+@pytest.mark.parametrize("T", [3, 40])
+def test_compressed_backend_stack_equals_resident_stack(T):
+    """Offloaded experts decoded from exponent-Huffman blobs in device memory into the load
+    buffers, one layer ahead of compute, give the resident stack's outputs bit for bit."""
+    cfg = syn.custom_config("stackc", d=256, f=256, E=8, k=2, S=1, n_buffered=0)
+    w = syn.make_weights(cfg)
+    L, steps = 4, 3
+    rng = np.random.default_rng(50 + T)
+    hidden_np = syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(np.float32))
+    hidden = torch.from_numpy(hidden_np.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = [[syn.bf16_bits_to_f32(syn.to_bf16_bits(rng.standard_normal((T, cfg.E)).astype(np.float32)))
+               for _ in range(L)] for _ in range(steps)]
+    comp = pipeline.DecodeStack(cfg, w, L, n_offload=5, layouts=2, seed=4, backend="compressed")
+    res = pipeline.DecodeStack(cfg, w, L, n_offload=0, layouts=1, seed=2)
+    a = run(comp, hidden, logits, T)
+    b = run(res, hidden, logits, T)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert comp.compressed_bytes < 8 * 3 * cfg.f * cfg.d * 2
+
+
 def test_schedule_points_needed_experts_at_alternating_buffers():
     cfg = syn.custom_config("sched", d=128, f=128, E=8, k=2, S=0, n_buffered=0)
     w = syn.make_weights(cfg)
