@@ -25,7 +25,10 @@ Byte layout of one compressed page of n values (sections 16-byte aligned):
   [264, 272)      total bits of the exponent stream (int64)
   [272, ...)      the 4096-entry decode table, uint16 each
   then            chunk start bit offsets, uint32 [ceil(n / 256) + 1] (the last = total bits)
-  then            the sign|mantissa bytes, uint8 [n]
+  then            the sign|mantissa bytes, uint8 [256 * chunks], interleaved so that the GPU
+                  threads decoding 256 consecutive chunks read them together: value i of chunk c
+                  sits at 65536*(c // 256) + (i // 8)*8*g + 8*(c % 256) + i % 8, g being the
+                  number of chunks in c's group of 256 (bytes past the last value are zero)
   then            the exponent stream, uint32 words (big-endian bit order inside each word),
                   followed by two zero words (a decoder may read one word past its last code)
 """
@@ -50,8 +53,18 @@ def layout(n: int):
     lut = 272
     offs = _align16(lut + 2 * (1 << LUT_BITS))
     sm = _align16(offs + 4 * (n_chunks + 1))
-    bits = _align16(sm + n)
+    bits = _align16(sm + CHUNK * n_chunks)
     return lut, offs, sm, bits
+
+
+def sm_position(n: int) -> np.ndarray:
+    """Where value i's sign|mantissa byte sits in the interleaved section."""
+    i = np.arange(n, dtype=np.int64)
+    n_chunks = (n + CHUNK - 1) // CHUNK
+    c, j = i // CHUNK, i % CHUNK
+    grp = c // 256
+    g = np.minimum(256, n_chunks - 256 * grp)
+    return 65536 * grp + (j // 8) * 8 * g + 8 * (c % 256) + j % 8
 
 
 def huffman_lengths(counts) -> list[int]:
@@ -166,7 +179,9 @@ def encode(values) -> bytes:
     out[264:272] = int(bitpos).to_bytes(8, "little")
     out[lut_o:lut_o + 2 * (1 << LUT_BITS)] = decode_table(lengths).astype("<u2").tobytes()
     out[offs_o:offs_o + 4 * len(starts)] = np.asarray(starts, dtype="<u4").tobytes()
-    out[sm_o:sm_o + n] = sm.tobytes()
+    sm_sec = np.zeros(CHUNK * n_chunks, dtype=np.uint8)
+    sm_sec[sm_position(n)] = sm
+    out[sm_o:sm_o + sm_sec.size] = sm_sec.tobytes()
     out[bits_o:] = np.asarray(words, dtype="<u4").tobytes()
     return bytes(out)
 
@@ -178,7 +193,7 @@ def decode(blob: bytes) -> np.ndarray:
     codes = canonical_codes(lengths)
     by_code = {(lengths[s], codes[s]): s for s in range(256) if lengths[s]}
     lut_o, offs_o, sm_o, bits_o = layout(n)
-    sm = np.frombuffer(blob[sm_o:sm_o + n], dtype=np.uint8)
+    sm = np.frombuffer(blob[sm_o:bits_o], dtype=np.uint8)[sm_position(n)]
     words = np.frombuffer(blob[bits_o:], dtype="<u4")
     starts = np.frombuffer(blob[offs_o:offs_o + 4 * ((n + CHUNK - 1) // CHUNK + 1)], dtype="<u4")
 

@@ -14,7 +14,10 @@
 //   thread decodes one chunk; 32-bit words filled from bit 31 down, then two zero words
 //   bytes: [0,256) lengths | [256,264) n | [264,272) stream bits | [272,...) 4096-entry table
 //   (symbol | length << 8, uint16, indexed by the next 12 stream bits) | chunk start bits, uint32
-//   [chunks + 1] | sign|mantissa bytes [n] | stream words; each section 16-byte aligned.
+//   [chunks + 1] | sign|mantissa bytes [256 * chunks], interleaved for the 256 threads that
+//   decode one group of 256 chunks: value i of chunk c at 65536*(c/256) + (i/8)*8*g + 8*(c%256)
+//   + i%8 (g chunks in the group), so a warp's 8-byte loads are contiguous | stream words; each
+//   section 16-byte aligned.
 #include <algorithm>
 #include <cstring>
 #include <queue>
@@ -43,8 +46,15 @@ __host__ __device__ inline Layout layout_of(int64_t n) {
     L.lut = 272;
     L.offs = align16(L.lut + 2 * (1 << kLutBits));
     L.sm = align16(L.offs + 4 * (L.n_chunks + 1));
-    L.bits = align16(L.sm + n);
+    L.bits = align16(L.sm + (int64_t)kChunk * L.n_chunks);
     return L;
+}
+
+// Byte offset of value i's sign|mantissa byte inside the interleaved section.
+__host__ __device__ inline int64_t sm_pos(int64_t n_chunks, int64_t i) {
+    const int64_t c = i / kChunk, j = i % kChunk, grp = c / 256;
+    const int64_t g = n_chunks - 256 * grp < 256 ? n_chunks - 256 * grp : 256;
+    return 65536 * grp + (j / 8) * 8 * g + 8 * (c % 256) + j % 8;
 }
 
 // Huffman code lengths of the 256 symbols from their counts.
@@ -141,7 +151,11 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
         return;
     }
     const uint32_t* words = reinterpret_cast<const uint32_t*>(src + L.bits);
-    const uint8_t* sm = src + L.sm + chunk * kChunk;
+    // this chunk's sign|mantissa bytes: 8 at a time, the group's chunks side by side
+    const int64_t grp = chunk / 256;
+    const int64_t g = L.n_chunks - 256 * grp < 256 ? L.n_chunks - 256 * grp : 256;
+    const uint8_t* sm = src + L.sm + 65536 * grp + 8 * (chunk % 256);
+    const int64_t sm_step = 8 * g;
     uint16_t* dst = a.dst[page] + chunk * kChunk;
     int64_t wi = start >> 5;
     int pos = (int)(start & 31);
@@ -161,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
     };
     int i = 0;
     for (; i + 8 <= cnt; i += 8) {
-        const uint2 s8 = *reinterpret_cast<const uint2*>(sm + i);
+        const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + (i / 8) * sm_step));
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
         }
         *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    for (; i < cnt; ++i) dst[i] = (uint16_t)join(next_exp(), sm[i]);
+    for (; i < cnt; ++i) dst[i] = (uint16_t)join(next_exp(), sm[(i / 8) * sm_step + i % 8]);
 }
 
 }  // namespace
@@ -215,6 +229,7 @@ extern "C" pmoe_status pmoe_exp_encode(const uint16_t* values, int64_t n, void* 
     }
     uint32_t* starts = reinterpret_cast<uint32_t*>(o + L.offs);
     uint8_t* sm = o + L.sm;
+    std::memset(sm, 0, (size_t)(L.bits - L.sm));
     uint32_t* words = reinterpret_cast<uint32_t*>(o + L.bits);
     uint64_t acc = 0;
     int acc_bits = 0;
@@ -223,7 +238,7 @@ extern "C" pmoe_status pmoe_exp_encode(const uint16_t* values, int64_t n, void* 
         if (i % kChunk == 0) starts[i / kChunk] = (uint32_t)bitpos;
         const uint16_t v = values[i];
         const int s = (v >> 7) & 0xFF;
-        sm[i] = (uint8_t)(((v >> 8) & 0x80) | (v & 0x7F));
+        sm[sm_pos(L.n_chunks, i)] = (uint8_t)(((v >> 8) & 0x80) | (v & 0x7F));
         acc = (acc << lengths[s]) | codes[s];
         acc_bits += lengths[s];
         bitpos += lengths[s];
