@@ -289,10 +289,11 @@ pmoe_status pmoe_vmm_lookup(pmoe_vmm_t vmm, int64_t* block_of);
  * backend): bf16 expert weights keep sign and mantissa as they are and Huffman-code the 8-bit
  * exponent, whose entropy is low; the GPU decompresses before the weights are read.  Format (the
  * page fixes none): per page of n values, code lengths [256], n, stream bits, a 4096-entry decode
- * table (symbol | length << 8 for the next 12 stream bits), chunk start bits (one per 256 values),
- * the sign|mantissa bytes (interleaved across each group of 256 chunks so that the threads
- * decoding them load 8 bytes each from one contiguous run) and the exponent stream (32-bit words,
- * bit 31 first, two zero words after it); sections 16-byte aligned.  Codes are canonical Huffman codes of at most 12 bits.
+ * table (symbol | length << 8 for the next 12 stream bits), the start bit of each chunk of at
+ * most 256 values (within each group of 65536 values, runs of 8 values are dealt to the group's
+ * chunks in turn, so the threads decoding neighbouring chunks read and write neighbouring runs),
+ * the sign|mantissa bytes in value order and the exponent stream (32-bit words, bit 31 first,
+ * two zero words after it); sections 16-byte aligned.  Codes are canonical Huffman codes of at most 12 bits.
  * Lossless: decoding gives back every bit pattern (NaN, infinities, subnormals included). */
 
 /* Bytes pmoe_exp_encode may write for n values. */

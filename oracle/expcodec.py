@@ -14,8 +14,13 @@ fixes no format; this module is the format's definition, written as plainly as p
   nonzero count is halved (rounding up) and the tree rebuilt.
 * canonical codes (the deflate rule): codes of one length are consecutive integers in symbol
   order, and the first code of length L is (first code of length L-1 + count of length L-1) << 1.
-* the exponent stream is written code after code, most significant code bit first, into 32-bit
-  words filled from bit 31 down; it is cut into chunks of 256 symbols, and the bit offset where
+* chunks: the values are taken in groups of 65536 (the last group may be smaller); a group of v
+  values has g = ceil(v / 256) chunks, its values form runs of 8 (the last may be shorter), and
+  run R of the group belongs to chunk R mod g, as that chunk's run number R div g.  So a chunk
+  holds at most 256 values, and the GPU threads decoding the g chunks of a group side by side
+  read and write neighbouring runs.
+* the exponent stream is written chunk after chunk, each chunk's codes in its run order, most
+  significant code bit first, into 32-bit words filled from bit 31 down; the bit offset where
   each chunk starts is stored so chunks decode independently.
 * a 4096-entry table maps the next 12 bits of the stream to (symbol | length << 8).
 
@@ -25,10 +30,7 @@ Byte layout of one compressed page of n values (sections 16-byte aligned):
   [264, 272)      total bits of the exponent stream (int64)
   [272, ...)      the 4096-entry decode table, uint16 each
   then            chunk start bit offsets, uint32 [ceil(n / 256) + 1] (the last = total bits)
-  then            the sign|mantissa bytes, uint8 [256 * chunks], interleaved so that the GPU
-                  threads decoding 256 consecutive chunks read them together: value i of chunk c
-                  sits at 65536*(c // 256) + (i // 8)*8*g + 8*(c % 256) + i % 8, g being the
-                  number of chunks in c's group of 256 (bytes past the last value are zero)
+  then            the sign|mantissa bytes, uint8 [n], in value order
   then            the exponent stream, uint32 words (big-endian bit order inside each word),
                   followed by two zero words (a decoder may read one word past its last code)
 """
@@ -53,18 +55,28 @@ def layout(n: int):
     lut = 272
     offs = _align16(lut + 2 * (1 << LUT_BITS))
     sm = _align16(offs + 4 * (n_chunks + 1))
-    bits = _align16(sm + CHUNK * n_chunks)
+    bits = _align16(sm + n)
     return lut, offs, sm, bits
 
 
-def sm_position(n: int) -> np.ndarray:
-    """Where value i's sign|mantissa byte sits in the interleaved section."""
-    i = np.arange(n, dtype=np.int64)
-    n_chunks = (n + CHUNK - 1) // CHUNK
-    c, j = i // CHUNK, i % CHUNK
-    grp = c // 256
-    g = np.minimum(256, n_chunks - 256 * grp)
-    return 65536 * grp + (j // 8) * 8 * g + 8 * (c % 256) + j % 8
+GROUP = 65536
+RUN = 8
+
+
+def chunk_values(n: int) -> list[list[int]]:
+    """The value indices of every chunk, chunk by chunk, each in its coding order."""
+    chunks = []
+    for g0 in range(0, n, GROUP):
+        v = min(GROUP, n - g0)
+        g = (v + CHUNK - 1) // CHUNK
+        runs = (v + RUN - 1) // RUN
+        for c in range(g):
+            vals = []
+            for R in range(c, runs, g):
+                start = g0 + RUN * R
+                vals += list(range(start, min(start + RUN, n)))
+            chunks.append(vals)
+    return chunks
 
 
 def huffman_lengths(counts) -> list[int]:
@@ -150,23 +162,27 @@ def encode(values) -> bytes:
     exp, sm = split(v)
     lengths = huffman_lengths(np.bincount(exp, minlength=256))
     codes = canonical_codes(lengths)
-    # the exponent stream, one code at a time, and each chunk's starting bit
+    # the exponent stream, chunk by chunk in each chunk's order, and each chunk's starting bit
     n_chunks = (n + CHUNK - 1) // CHUNK
     starts = []
     bitpos = 0
     words = []
     acc, acc_bits = 0, 0            # pending bits, most significant first
-    for i, s in enumerate(exp.tolist()):
-        if i % CHUNK == 0:
-            starts.append(bitpos)
-        L = lengths[s]
-        acc = (acc << L) | codes[s]
-        acc_bits += L
-        bitpos += L
-        while acc_bits >= 32:
-            words.append((acc >> (acc_bits - 32)) & 0xFFFFFFFF)
-            acc_bits -= 32
-            acc &= (1 << acc_bits) - 1
+    chunks = chunk_values(n)
+    assert len(chunks) == n_chunks and all(len(c) <= CHUNK for c in chunks)
+    ex = exp.tolist()
+    for vals in chunks:
+        starts.append(bitpos)
+        for i in vals:
+            s = ex[i]
+            L = lengths[s]
+            acc = (acc << L) | codes[s]
+            acc_bits += L
+            bitpos += L
+            while acc_bits >= 32:
+                words.append((acc >> (acc_bits - 32)) & 0xFFFFFFFF)
+                acc_bits -= 32
+                acc &= (1 << acc_bits) - 1
     if acc_bits:
         words.append((acc << (32 - acc_bits)) & 0xFFFFFFFF)
     words += [0, 0]
@@ -179,9 +195,7 @@ def encode(values) -> bytes:
     out[264:272] = int(bitpos).to_bytes(8, "little")
     out[lut_o:lut_o + 2 * (1 << LUT_BITS)] = decode_table(lengths).astype("<u2").tobytes()
     out[offs_o:offs_o + 4 * len(starts)] = np.asarray(starts, dtype="<u4").tobytes()
-    sm_sec = np.zeros(CHUNK * n_chunks, dtype=np.uint8)
-    sm_sec[sm_position(n)] = sm
-    out[sm_o:sm_o + sm_sec.size] = sm_sec.tobytes()
+    out[sm_o:sm_o + n] = sm.tobytes()
     out[bits_o:] = np.asarray(words, dtype="<u4").tobytes()
     return bytes(out)
 
@@ -193,7 +207,7 @@ def decode(blob: bytes) -> np.ndarray:
     codes = canonical_codes(lengths)
     by_code = {(lengths[s], codes[s]): s for s in range(256) if lengths[s]}
     lut_o, offs_o, sm_o, bits_o = layout(n)
-    sm = np.frombuffer(blob[sm_o:bits_o], dtype=np.uint8)[sm_position(n)]
+    sm = np.frombuffer(blob[sm_o:sm_o + n], dtype=np.uint8)
     words = np.frombuffer(blob[bits_o:], dtype="<u4")
     starts = np.frombuffer(blob[offs_o:offs_o + 4 * ((n + CHUNK - 1) // CHUNK + 1)], dtype="<u4")
 
@@ -201,9 +215,9 @@ def decode(blob: bytes) -> np.ndarray:
         return (int(words[p >> 5]) >> (31 - (p & 31))) & 1
 
     exp = np.empty(n, dtype=np.uint8)
-    for c in range(len(starts) - 1):
+    for c, vals in enumerate(chunk_values(n)):
         p = int(starts[c])
-        for i in range(c * CHUNK, min(n, (c + 1) * CHUNK)):
+        for i in vals:
             code, L = 0, 0
             while (L, code) not in by_code:
                 code = (code << 1) | bit(p)

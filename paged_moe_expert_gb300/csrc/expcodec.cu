@@ -10,14 +10,15 @@
 //   first, ties to the node made earlier, leaves made first in symbol order; one symbol ->
 //   length 1); counts halved (rounding up) and the tree rebuilt while a code exceeds 12 bits
 //   canonical codes (consecutive within a length, in symbol order)
-//   the exponent stream cut into chunks of 256 symbols with the start bit of each chunk, so one
-//   thread decodes one chunk; 32-bit words filled from bit 31 down, then two zero words
+//   chunks of at most 256 values, one per GPU thread: values in groups of 65536, a group of v
+//   values has g = ceil(v/256) chunks, and its run R of 8 values belongs to chunk R mod g (as its
+//   run R div g), so the threads of a group read and write neighbouring runs
+//   the exponent stream chunk by chunk with the start bit of each chunk; 32-bit words filled
+//   from bit 31 down, then two zero words
 //   bytes: [0,256) lengths | [256,264) n | [264,272) stream bits | [272,...) 4096-entry table
 //   (symbol | length << 8, uint16, indexed by the next 12 stream bits) | chunk start bits, uint32
-//   [chunks + 1] | sign|mantissa bytes [256 * chunks], interleaved for the 256 threads that
-//   decode one group of 256 chunks: value i of chunk c at 65536*(c/256) + (i/8)*8*g + 8*(c%256)
-//   + i%8 (g chunks in the group), so a warp's 8-byte loads are contiguous | stream words; each
-//   section 16-byte aligned.
+//   [chunks + 1] | sign|mantissa bytes [n] in value order | stream words; each section 16-byte
+//   aligned.
 #include <algorithm>
 #include <cstring>
 #include <queue>
@@ -29,6 +30,8 @@ namespace pmoe {
 namespace {
 
 constexpr int kChunk = 256;
+constexpr int kGroup = 65536;            // values per group of 256 chunks
+constexpr int kRun = 8;                  // values per run
 constexpr int kLmax = 12;
 constexpr int kLutBits = 12;
 constexpr int kThreads = 256;             // one chunk per thread
@@ -46,15 +49,25 @@ __host__ __device__ inline Layout layout_of(int64_t n) {
     L.lut = 272;
     L.offs = align16(L.lut + 2 * (1 << kLutBits));
     L.sm = align16(L.offs + 4 * (L.n_chunks + 1));
-    L.bits = align16(L.sm + (int64_t)kChunk * L.n_chunks);
+    L.bits = align16(L.sm + n);
     return L;
 }
 
-// Byte offset of value i's sign|mantissa byte inside the interleaved section.
-__host__ __device__ inline int64_t sm_pos(int64_t n_chunks, int64_t i) {
-    const int64_t c = i / kChunk, j = i % kChunk, grp = c / 256;
-    const int64_t g = n_chunks - 256 * grp < 256 ? n_chunks - 256 * grp : 256;
-    return 65536 * grp + (j / 8) * 8 * g + 8 * (c % 256) + j % 8;
+// Chunk `chunk`'s place: its group's first value, the group's chunk count g and run count, and
+// its index c inside the group (its runs are c, c + g, c + 2g, ...).
+struct ChunkPlace {
+    int64_t g0;
+    int64_t g, runs, c;
+};
+__host__ __device__ inline ChunkPlace place_of(int64_t n, int64_t chunk) {
+    ChunkPlace P;
+    const int64_t grp = chunk / 256;
+    P.g0 = grp * kGroup;
+    const int64_t v = n - P.g0 < kGroup ? n - P.g0 : kGroup;
+    P.g = (v + kChunk - 1) / kChunk;
+    P.runs = (v + kRun - 1) / kRun;
+    P.c = chunk % 256;
+    return P;
 }
 
 // Huffman code lengths of the 256 symbols from their counts.
@@ -145,18 +158,14 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
     }
     const uint32_t* starts = reinterpret_cast<const uint32_t*>(src + L.offs);
     const int64_t start = starts[chunk];
-    const int cnt = (int)min((int64_t)kChunk, a.n - chunk * kChunk);
     if (start > total) {
         if (a.err) atomicCAS(a.err, 0, (int)PMOE_ERR_INVALID_ARG);
         return;
     }
     const uint32_t* words = reinterpret_cast<const uint32_t*>(src + L.bits);
-    // this chunk's sign|mantissa bytes: 8 at a time, the group's chunks side by side
-    const int64_t grp = chunk / 256;
-    const int64_t g = L.n_chunks - 256 * grp < 256 ? L.n_chunks - 256 * grp : 256;
-    const uint8_t* sm = src + L.sm + 65536 * grp + 8 * (chunk % 256);
-    const int64_t sm_step = 8 * g;
-    uint16_t* dst = a.dst[page] + chunk * kChunk;
+    const ChunkPlace P = place_of(a.n, chunk);
+    const uint8_t* sm = src + L.sm;
+    uint16_t* dst = a.dst[page];
     int64_t wi = start >> 5;
     int pos = (int)(start & 31);
     uint64_t cur = ((uint64_t)__ldg(words + wi) << 32) | __ldg(words + wi + 1);
@@ -173,21 +182,26 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
     auto join = [](uint32_t ex, uint32_t s) -> uint32_t {
         return ((s & 0x80u) << 8) | (ex << 7) | (s & 0x7Fu);
     };
-    int i = 0;
-    for (; i + 8 <= cnt; i += 8) {
-        const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + (i / 8) * sm_step));
-        uint32_t o[4];
+    // the chunk's runs; neighbouring threads hold neighbouring runs, so each warp's 8-byte loads
+    // and 16-byte stores cover one contiguous range
+    for (int64_t R = P.c; R < P.runs; R += P.g) {
+        const int64_t v0 = P.g0 + kRun * R;
+        if (v0 + kRun <= a.n) {
+            const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + v0));
+            uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t sw = q < 2 ? s8.x : s8.y;
-            const int sh = (q & 1) * 16;
-            const uint32_t e0 = next_exp();
-            const uint32_t e1 = next_exp();
-            o[q] = join(e0, (sw >> sh) & 0xFFu) | (join(e1, (sw >> (sh + 8)) & 0xFFu) << 16);
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t sw = q < 2 ? s8.x : s8.y;
+                const int sh = (q & 1) * 16;
+                const uint32_t e0 = next_exp();
+                const uint32_t e1 = next_exp();
+                o[q] = join(e0, (sw >> sh) & 0xFFu) | (join(e1, (sw >> (sh + 8)) & 0xFFu) << 16);
+            }
+            *reinterpret_cast<uint4*>(dst + v0) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            for (int64_t v = v0; v < a.n; ++v) dst[v] = (uint16_t)join(next_exp(), sm[v]);
         }
-        *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    for (; i < cnt; ++i) dst[i] = (uint16_t)join(next_exp(), sm[(i / 8) * sm_step + i % 8]);
 }
 
 }  // namespace
@@ -229,23 +243,27 @@ extern "C" pmoe_status pmoe_exp_encode(const uint16_t* values, int64_t n, void* 
     }
     uint32_t* starts = reinterpret_cast<uint32_t*>(o + L.offs);
     uint8_t* sm = o + L.sm;
-    std::memset(sm, 0, (size_t)(L.bits - L.sm));
+    for (int64_t i = 0; i < n; ++i) sm[i] = (uint8_t)(((values[i] >> 8) & 0x80) | (values[i] & 0x7F));
     uint32_t* words = reinterpret_cast<uint32_t*>(o + L.bits);
     uint64_t acc = 0;
     int acc_bits = 0;
     int64_t bitpos = 0, nw = 0;
-    for (int64_t i = 0; i < n; ++i) {
-        if (i % kChunk == 0) starts[i / kChunk] = (uint32_t)bitpos;
-        const uint16_t v = values[i];
-        const int s = (v >> 7) & 0xFF;
-        sm[sm_pos(L.n_chunks, i)] = (uint8_t)(((v >> 8) & 0x80) | (v & 0x7F));
-        acc = (acc << lengths[s]) | codes[s];
-        acc_bits += lengths[s];
-        bitpos += lengths[s];
-        if (acc_bits >= 32) {
-            words[nw++] = (uint32_t)(acc >> (acc_bits - 32));
-            acc_bits -= 32;
-            acc &= (acc_bits ? ((1ull << acc_bits) - 1) : 0);
+    for (int64_t chunk = 0; chunk < L.n_chunks; ++chunk) {
+        starts[chunk] = (uint32_t)bitpos;
+        const ChunkPlace P = place_of(n, chunk);
+        for (int64_t R = P.c; R < P.runs; R += P.g) {
+            const int64_t v0 = P.g0 + kRun * R;
+            for (int64_t i = v0; i < v0 + kRun && i < n; ++i) {
+                const int s = (values[i] >> 7) & 0xFF;
+                acc = (acc << lengths[s]) | codes[s];
+                acc_bits += lengths[s];
+                bitpos += lengths[s];
+                if (acc_bits >= 32) {
+                    words[nw++] = (uint32_t)(acc >> (acc_bits - 32));
+                    acc_bits -= 32;
+                    acc &= (acc_bits ? ((1ull << acc_bits) - 1) : 0);
+                }
+            }
         }
     }
     if (acc_bits) words[nw++] = (uint32_t)(acc << (32 - acc_bits));
