@@ -131,10 +131,14 @@ struct DecodeArgs {
     int32_t* err;
 };
 
-// One thread per chunk: table lookups on the next 12 bits of a 64-bit window, eight values
-// joined and stored (16 bytes) at a time.
+// One thread per chunk: lookups on the next 12 bits of a 64-bit window, eight values joined and
+// stored (16 bytes) at a time.  Each CTA first turns the page's table into a table of code pairs:
+// entry w holds the symbol and length of the code at the front of w and, when the next code also
+// fits in the 12 bits, that second symbol and the pair's length, so one lookup usually yields two
+// values (bits 0-7 first symbol, 8-15 second, 16-19 first length, 20-23 pair length, 28 pair).
 __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_constant__ DecodeArgs a) {
     __shared__ uint16_t lut[1 << kLutBits];
+    __shared__ uint32_t lut2[1 << kLutBits];
     const int page = blockIdx.x / a.ctas_per_page;
     const int64_t chunk = (int64_t)(blockIdx.x % a.ctas_per_page) * kThreads + threadIdx.x;
     const uint8_t* src = a.src[page];
@@ -143,6 +147,19 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
         const uint4* t4 = reinterpret_cast<const uint4*>(src + L.lut);
         uint4* s4 = reinterpret_cast<uint4*>(lut);
         for (int i = threadIdx.x; i < (2 << kLutBits) / 16; i += kThreads) s4[i] = t4[i];
+    }
+    __syncthreads();
+    for (int w = threadIdx.x; w < (1 << kLutBits); w += kThreads) {
+        const uint32_t e1 = lut[w];
+        const uint32_t l1 = e1 >> 8;
+        uint32_t v = (e1 & 0xFFu) | (l1 << 16) | (l1 << 20);
+        if (l1 >= 1 && l1 < (uint32_t)kLutBits) {
+            const uint32_t e2 = lut[(w << l1) & ((1 << kLutBits) - 1)];
+            const uint32_t l2 = e2 >> 8;
+            if (l2 >= 1 && l1 + l2 <= (uint32_t)kLutBits)
+                v = (e1 & 0xFFu) | ((e2 & 0xFFu) << 8) | (l1 << 16) | ((l1 + l2) << 20) | (1u << 28);
+        }
+        lut2[w] = v;
     }
     __syncthreads();
     if (chunk >= L.n_chunks) return;
@@ -169,14 +186,17 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
     int64_t wi = start >> 5;
     int pos = (int)(start & 31);
     uint64_t cur = ((uint64_t)__ldg(words + wi) << 32) | __ldg(words + wi + 1);
-    auto next_exp = [&]() -> uint32_t {
-        const uint32_t e = lut[(uint32_t)((cur << pos) >> (64 - kLutBits))];
-        pos += (int)(e >> 8);
+    auto advance = [&](int len) {
+        pos += len;
         if (pos >= 32) {
             pos -= 32;
             ++wi;
             cur = (cur << 32) | (wi + 1 < words_avail ? __ldg(words + wi + 1) : 0u);
         }
+    };
+    auto next_exp = [&]() -> uint32_t {
+        const uint32_t e = lut2[(uint32_t)((cur << pos) >> (64 - kLutBits))];
+        advance((int)((e >> 16) & 0xFu));
         return e & 0xFFu;
     };
     auto join = [](uint32_t ex, uint32_t s) -> uint32_t {
@@ -188,13 +208,22 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
         const int64_t v0 = P.g0 + kRun * R;
         if (v0 + kRun <= a.n) {
             const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + v0));
+            // the run's 8 exponents, one or two per lookup
+            uint64_t ex = 0;
+            for (int got = 0; got < kRun;) {
+                const uint32_t e = lut2[(uint32_t)((cur << pos) >> (64 - kLutBits))];
+                const bool two = ((e >> 28) & 1u) && got < kRun - 1;
+                ex |= (uint64_t)(two ? (e & 0xFFFFu) : (e & 0xFFu)) << (8 * got);
+                advance((int)(two ? (e >> 20) & 0xFu : (e >> 16) & 0xFu));
+                got += two ? 2 : 1;
+            }
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t sw = q < 2 ? s8.x : s8.y;
                 const int sh = (q & 1) * 16;
-                const uint32_t e0 = next_exp();
-                const uint32_t e1 = next_exp();
+                const uint32_t e0 = (uint32_t)(ex >> (16 * q)) & 0xFFu;
+                const uint32_t e1 = (uint32_t)(ex >> (16 * q + 8)) & 0xFFu;
                 o[q] = join(e0, (sw >> sh) & 0xFFu) | (join(e1, (sw >> (sh + 8)) & 0xFFu) << 16);
             }
             *reinterpret_cast<uint4*>(dst + v0) = make_uint4(o[0], o[1], o[2], o[3]);
