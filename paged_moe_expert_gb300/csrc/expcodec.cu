@@ -185,13 +185,17 @@ __global__ void __launch_bounds__(kThreads) exp_decode_kernel(const __grid_const
     uint16_t* dst = a.dst[page];
     int64_t wi = start >> 5;
     int pos = (int)(start & 31);
+    // the 64-bit window holds words wi and wi+1; word wi+2 is loaded one refill ahead, so the
+    // load's latency hides behind the ~12 values decoded before it is needed
     uint64_t cur = ((uint64_t)__ldg(words + wi) << 32) | __ldg(words + wi + 1);
+    uint32_t nxt = wi + 2 < words_avail ? __ldg(words + wi + 2) : 0u;
     auto advance = [&](int len) {
         pos += len;
         if (pos >= 32) {
             pos -= 32;
             ++wi;
-            cur = (cur << 32) | (wi + 1 < words_avail ? __ldg(words + wi + 1) : 0u);
+            cur = (cur << 32) | nxt;
+            nxt = wi + 2 < words_avail ? __ldg(words + wi + 2) : 0u;
         }
     };
     auto next_exp = [&]() -> uint32_t {
