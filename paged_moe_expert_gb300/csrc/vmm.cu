@@ -71,12 +71,20 @@ pmoe_status drv(CUresult r, const char* what) {
     return r == CUDA_SUCCESS ? PMOE_OK : pmoe::record_failure(PMOE_ERR_CUDA, what);
 }
 
-// Makes the runtime's context of `device` current for the driver calls that follow.
-pmoe_status use_device(int device) {
-    if (cudaSetDevice(device) != cudaSuccess || cudaFree(nullptr) != cudaSuccess)
-        return bad(PMOE_ERR_CUDA, "pmoe_vmm: cannot make the device current");
-    return PMOE_OK;
-}
+// Makes the runtime's context of `device` current for the driver calls that follow, and puts the
+// caller's current device back when it goes out of scope.
+struct DeviceScope {
+    int prev = -1;
+    pmoe_status status = PMOE_OK;
+    explicit DeviceScope(int device) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (cudaSetDevice(device) != cudaSuccess || cudaFree(nullptr) != cudaSuccess)
+            status = bad(PMOE_ERR_CUDA, "pmoe_vmm: cannot make the device current");
+    }
+    ~DeviceScope() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
 
 pmoe_status map_one(pmoe_vmm* v, CUdeviceptr at, CUmemGenericAllocationHandle h) {
     const VmmApi& A = api();
@@ -113,6 +121,8 @@ extern "C" pmoe_status pmoe_vmm_granularity(int32_t device, size_t* bytes) {
     if (!bytes) return bad(PMOE_ERR_INVALID_ARG, "pmoe_vmm_granularity: bytes is NULL");
     *bytes = 0;
     if (!api().ok) return bad(PMOE_ERR_CUDA, "pmoe_vmm: driver VMM entry points not found");
+    DeviceScope scope(device);
+    if (scope.status != PMOE_OK) return scope.status;
     const CUmemAllocationProp p = device_prop(device);
     return drv(api().granularity(bytes, &p, CU_MEM_ALLOC_GRANULARITY_MINIMUM),
                "cuMemGetAllocationGranularity failed");
@@ -124,10 +134,10 @@ extern "C" pmoe_status pmoe_vmm_create(int32_t device, size_t block_bytes, int64
     *out = nullptr;
     if (block_bytes == 0 || n_blocks < 1 || n_virtual < 1)
         return bad(PMOE_ERR_INVALID_ARG, "pmoe_vmm_create: block_bytes, n_blocks, n_virtual >= 1");
-    pmoe_status st = use_device(device);
-    if (st != PMOE_OK) return st;
+    DeviceScope scope(device);
+    if (scope.status != PMOE_OK) return scope.status;
     size_t g = 0;
-    st = pmoe_vmm_granularity(device, &g);
+    pmoe_status st = pmoe_vmm_granularity(device, &g);
     if (st != PMOE_OK) return st;
     if (block_bytes % g != 0)
         return bad(PMOE_ERR_UNSUPPORTED, "pmoe_vmm_create: block_bytes is not a multiple of the "
@@ -168,8 +178,8 @@ extern "C" pmoe_status pmoe_vmm_create(int32_t device, size_t block_bytes, int64
 
 extern "C" pmoe_status pmoe_vmm_destroy(pmoe_vmm_t v) {
     if (!v) return PMOE_OK;
-    pmoe_status st = use_device(v->device);
-    if (st != PMOE_OK) return st;
+    DeviceScope scope(v->device);
+    if (scope.status != PMOE_OK) return scope.status;
     teardown(v);
     return PMOE_OK;
 }
@@ -193,8 +203,9 @@ extern "C" pmoe_status pmoe_vmm_map(pmoe_vmm_t v, int64_t n, const int64_t* virt
             return bad(PMOE_ERR_INVALID_ARG, "pmoe_vmm_map: virtual page already mapped or listed twice");
         seen[virt[i]] = 1;
     }
-    pmoe_status st = use_device(v->device);
-    if (st != PMOE_OK) return st;
+    DeviceScope scope(v->device);
+    if (scope.status != PMOE_OK) return scope.status;
+    pmoe_status st = PMOE_OK;
     for (int64_t i = 0; i < n; ++i) {
         st = map_one(v, v->view + (CUdeviceptr)(virt[i] * v->block_bytes), v->handles[blocks[i]]);
         if (st != PMOE_OK) return st;   // the pages before i stay mapped (pmoe_vmm_lookup shows them)
@@ -214,8 +225,9 @@ extern "C" pmoe_status pmoe_vmm_unmap(pmoe_vmm_t v, int64_t n, const int64_t* vi
         pmoe_status st = pmoe_wait_event(readers_done, timeout_ms);
         if (st != PMOE_OK) return st;
     }
-    pmoe_status st = use_device(v->device);
-    if (st != PMOE_OK) return st;
+    DeviceScope scope(v->device);
+    if (scope.status != PMOE_OK) return scope.status;
+    pmoe_status st = PMOE_OK;
     for (int64_t i = 0; i < n; ++i) {
         if (v->block_of[virt[i]] < 0) continue;   // listed twice
         st = drv(api().unmap(v->view + (CUdeviceptr)(virt[i] * v->block_bytes), v->block_bytes),
