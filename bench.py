@@ -587,7 +587,7 @@ def main():
     ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc", "tc_decode", "tc2", "fused"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--sweep-iters", type=int, default=20)
+    ap.add_argument("--sweep-iters", type=int, default=50)
     ap.add_argument("--decode-sweep", action="store_true",
                     help="24-layer decode sweep with prefetch (prints one line per case)")
     ap.add_argument("--layers", type=int, default=24)
