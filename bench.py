@@ -527,7 +527,8 @@ def elastic_sweep(args):
                                   minlength=E) / (4096.0 * cfg.k) for lg in sample]).astype(np.float32)
     limit = args.offload_limit
     expert_pages = 3 * E * L + 3 * 4
-    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, [E] * L, limit, expert_pages)
+    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, [E] * L, limit, expert_pages,
+                                        backend=args.backend)
     peak = args.kv_peak
     phases = [("idle, all experts resident", [0] * 5),
               ("KV demand ramps up", [int(peak * (i + 1) / 20) for i in range(20)]),
@@ -564,7 +565,9 @@ def elastic_sweep(args):
         line = {"metric": "elastic decode: adjuster-driven 24-layer step on one pool shared with KV",
                 "config": {"workload": "%d Qwen1.5-MoE-shaped layers, %d tokens/step, %d expert "
                            "pages (%.2f MB each), offload limit %d" % (L, T, expert_pages, page_mb, limit),
-                           "phase": name, "rounds": n, "kv_demand_pages": [trace[0], trace[-1]]},
+                           "phase": name, "rounds": n, "kv_demand_pages": [trace[0], trace[-1]],
+                           "offload_backend": ("pinned host memory" if args.backend == "host" else
+                                               "exponent-Huffman blobs in device memory")},
                 "ms_per_step_median": float(np.median(rec["ms"])),
                 "ms_per_step_max": float(np.max(rec["ms"])),
                 "tokens_per_s": T / (float(np.median(rec["ms"])) * 1e-3),

@@ -180,7 +180,7 @@ class ElasticDecodeStack:
     comes from; cached[l] experts of layer l start resident."""
 
     def __init__(self, cfg, weights, n_layers: int, probs, cached, offload_limit: int,
-                 expert_pages: int, device="cuda"):
+                 expert_pages: int, device="cuda", backend: str = "host"):
         E, S, f, d = cfg.E, cfg.S, cfg.f, cfg.d
         self.cfg, self.L, self.device = cfg, n_layers, device
         self.base = 3 * S * n_layers
@@ -196,6 +196,17 @@ class ElasticDecodeStack:
             raise ValueError("a layer starts with more offloaded experts than offload_limit")
         self.host = [torch.from_numpy(pl.pack_expert(weights, e, E, f).view(np.int16)).pin_memory()
                      for e in range(E + S)]
+        # "compressed": the routed experts' pages also live in device memory as exponent-Huffman
+        # blobs, and both the streamed experts and the experts the adjuster adds are decoded from
+        # them instead of copied from the host
+        if backend not in ("host", "compressed"):
+            raise ValueError("backend must be 'host' or 'compressed'")
+        self.backend = backend
+        self.blobs = None
+        if backend == "compressed":
+            from paged_moe_expert_gb300 import expcodec
+            self.blobs = [[torch.from_numpy(expcodec.encode(m)).to(device)
+                           for m in pl.expert_matrices(weights, e, E, f)] for e in range(E)]
         self.copy_stream = torch.cuda.Stream(device=device)
         self.fill_stream = torch.cuda.Stream(device=device)
         self.ready = [torch.cuda.Event() for _ in range(2)]
@@ -254,9 +265,21 @@ class ElasticDecodeStack:
         adds = changes[changes[:, 0] == 1]
         for l in np.unique(adds[:, 1]) if len(adds) else []:
             mine = adds[adds[:, 1] == l]
-            pm.fill_pages_async(self.plan, [self.host[int(e)] for e in mine[:, 2]],
-                                (mine[:, 3:6] + self.base).tolist(), self.fill_stream,
-                                after=self.fwd_done, copy_done=self.fill_done[int(l)])
+            pages = (mine[:, 3:6] + self.base).tolist()
+            if self.backend == "host":
+                pm.fill_pages_async(self.plan, [self.host[int(e)] for e in mine[:, 2]], pages,
+                                    self.fill_stream, after=self.fwd_done,
+                                    copy_done=self.fill_done[int(l)])
+            else:
+                from paged_moe_expert_gb300 import expcodec
+                page = self.cfg.f * self.cfg.d
+                if self.fwd_done.cuda_event != 0:
+                    self.fill_stream.wait_event(self.fwd_done)   # the pages' last reader
+                src = [self.blobs[int(e)][j] for e in mine[:, 2] for j in range(3)]
+                dst = [self.pool[p * page:(p + 1) * page] for row in pages for p in row]
+                for i in range(0, len(src), 128):
+                    expcodec.decode_async(src[i:i + 128], page, dst[i:i + 128], stream=self.fill_stream)
+                self.fill_done[int(l)].record(self.fill_stream)
             self.filling[int(l)] = True
             self.filled_experts += len(mine)
         return changes, short
@@ -281,8 +304,20 @@ class ElasticDecodeStack:
     def prefetch(self, l, sched_l):
         need, slots, _ = sched_l
         b = l % 2
-        pm.prefetch_async(self.plan, b, [self.host[int(e)] for e in need], slots,
-                          self.copy_stream, buf_free=self.free[b], copy_done=self.ready[b])
+        if self.backend == "host":
+            pm.prefetch_async(self.plan, b, [self.host[int(e)] for e in need], slots,
+                              self.copy_stream, buf_free=self.free[b], copy_done=self.ready[b])
+            return
+        from paged_moe_expert_gb300 import expcodec
+        page = self.cfg.f * self.cfg.d
+        if self.free[b].cuda_event != 0:
+            self.copy_stream.wait_event(self.free[b])
+        src = [self.blobs[int(e)][j] for e in need for j in range(3)]
+        dst = [self.bufs[b][(3 * int(s_) + j) * page:(3 * int(s_) + j + 1) * page]
+               for s_ in slots for j in range(3)]
+        for i in range(0, len(src), 128):
+            expcodec.decode_async(src[i:i + 128], page, dst[i:i + 128], stream=self.copy_stream)
+        self.ready[b].record(self.copy_stream)
 
     # -- one step -----------------------------------------------------------------------------
     def step(self, x0, logits_dev, sched, acts, ws):

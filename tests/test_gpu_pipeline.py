@@ -88,7 +88,8 @@ def test_schedule_points_needed_experts_at_alternating_buffers():
         assert (bs[np.setdiff1d(np.arange(8), need)] == -1).all()
 
 
-def test_elastic_stack_follows_the_adjuster_and_equals_resident_stack():
+@pytest.mark.parametrize("backend", ["host", "compressed"])
+def test_elastic_stack_follows_the_adjuster_and_equals_resident_stack(backend):
     """One pool for all layers and the KV cache; a KV demand trace makes the adjuster evict and
     add experts between steps.  Every step's output equals the all-resident stack's, and after
     every step each layer's table points at pages that hold exactly its resident experts."""
@@ -100,7 +101,7 @@ def test_elastic_stack_follows_the_adjuster_and_equals_resident_stack():
     probs = rng.dirichlet(np.full(cfg.E, 0.5), size=L).astype(np.float32)
     cached = [6, 5, 7, 8]
     stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, cached, offload_limit=4,
-                                        expert_pages=3 * sum(cached) + 6)
+                                        expert_pages=3 * sum(cached) + 6, backend=backend)
     res = pipeline.DecodeStack(cfg, w, L, n_offload=0, layouts=1, seed=2)
     kv_trace = [0, 9, 30, 30, 0, 0, 12, 40, 0, 0]
     hidden_np = syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(np.float32))
