@@ -172,6 +172,54 @@ def kv_round(held: int, need: int, free: int):
     return take, 0, need - held - take
 
 
+class KVPages:
+    """KV cache pages of the unified pool (Rimuru, "One pool for data whose sizes differ by orders
+    of magnitude"): small pages carved by the three-tier allocator out of expert pages that the
+    adjuster lends, one request's pages kept on the same expert pages where possible; an expert
+    page whose KV pages are all free goes straight back to the adjuster.  Offsets are bytes from
+    the start of the adjuster's pages."""
+
+    def __init__(self, adj: Adjuster, expert_pages: int, page_bytes: int, kv_page_bytes: int):
+        from paged_moe_expert_gb300 import tiers
+        self._tiers = tiers
+        self.t = tiers.Tiers(expert_pages * page_bytes, page_bytes, 0, kv_page_bytes, 0)
+        # every page starts on the expert side: held by the tiers as a live expert page until the
+        # adjuster lends it
+        for p in range(expert_pages):
+            if self.t.alloc(tiers.EXPERT) != p * page_bytes:
+                raise RuntimeError("unexpected page order")
+        self.adj, self.page, self.kv = adj, page_bytes, kv_page_bytes
+        self.per_page = page_bytes // kv_page_bytes
+        self.req = {}                  # request -> its KV page offsets
+
+    def allocate(self, rid: int, n: int) -> int:
+        """n more KV pages for request rid; returns how many could not be placed."""
+        T = self._tiers
+        got = self.req.setdefault(int(rid), [])
+        for i in range(n):
+            off = self.t.alloc(T.KV, int(rid))
+            if off is None and self.adj.free_pages() > 0:
+                p = int(self.adj.lend(1)[0])            # one more expert page turns to KV
+                self.t.free(T.EXPERT, p * self.page)
+                off = self.t.alloc(T.KV, int(rid))
+            if off is None:
+                return n - i
+            got.append(off)
+        return 0
+
+    def release(self, rid: int):
+        T = self._tiers
+        for off in self.req.pop(int(rid), []):
+            self.t.free(T.KV, off)
+        c = self.t.stats()
+        for _ in range(c[1] + c[2]):                   # whole free pages back to the adjuster
+            off = self.t.alloc(T.EXPERT)
+            self.adj.give_back([off // self.page])
+
+    def live(self):
+        return {r: list(v) for r, v in self.req.items()}
+
+
 class ElasticDecodeStack:
     """L layers of one MoE shape over one page pool: pages [0, 3*S*L) hold the layers' shared
     chunks (always resident), pages base + [0, expert_pages) are the adjuster's, shared between
@@ -251,9 +299,8 @@ class ElasticDecodeStack:
         return out
 
     def round(self, kv_need: int):
-        """The round before a step: KV pages first, then the adjuster on what is left.  Added
-        experts start copying into their reserved pages at once, after the previous forward pass
-        (whose evictions may have freed those pages).  Returns (change records, R_b)."""
+        """The round before a step, KV counted in whole expert pages: KV pages first, then the
+        adjuster on what is left.  Returns (change records, R_b)."""
         take, back, short = kv_round(len(self.kv), int(kv_need), self.adj.free_pages())
         if back:
             self.adj.give_back(self.kv[-back:])
@@ -261,6 +308,29 @@ class ElasticDecodeStack:
         if take:
             self.kv += self.adj.lend(take).tolist()
         changes = self.adj.decide(short)
+        self._fill_adds(changes)
+        return changes, short
+
+    def round_requests(self, kv: "KVPages", arrivals, departures):
+        """The round before a step with KV pages per request: finished requests give their pages
+        back, then new ones ({request: KV pages}) are placed; the expert pages still missing are
+        R_b for the adjuster, and the requests that did not fit are returned to be retried."""
+        for rid in departures:
+            kv.release(rid)
+        waiting, short_kv = {}, 0
+        for rid, n in arrivals.items():
+            miss = kv.allocate(rid, n)
+            if miss:
+                waiting[rid] = miss
+                short_kv += miss
+        short = -(-short_kv // kv.per_page)                  # in expert pages
+        changes = self.adj.decide(short)
+        self._fill_adds(changes)
+        return changes, short, waiting
+
+    def _fill_adds(self, changes):
+        """Added experts start copying into their reserved pages at once, after the previous
+        forward pass (whose evictions may have freed those pages)."""
         self.filling = [False] * self.L
         adds = changes[changes[:, 0] == 1]
         for l in np.unique(adds[:, 1]) if len(adds) else []:
@@ -282,7 +352,6 @@ class ElasticDecodeStack:
                 self.fill_done[int(l)].record(self.fill_stream)
             self.filling[int(l)] = True
             self.filled_experts += len(mine)
-        return changes, short
 
     def resident(self, l):
         return self.adj.page_table(l)[:, 0] >= 0

@@ -293,3 +293,73 @@ def test_constant_kv_demand_is_met_within_a_few_rounds():
     assert shorts[0] > 0 and shorts[11] == 0
     assert o.free_pages() < 12 and o.free_pages() == 4 + 3 * (E * L - sum(o.kept))
     assert sum(o.kept) < E * L  # 4 spare pages + 2 missing experts = 10 free: inside the gap
+
+
+# ---- part 4: KV pages carved from lent expert pages (the unified pool) ----------------------
+
+def expert_pages_in_use(a, L):
+    used = set()
+    for l in range(L):
+        for row in a.page_table(l):
+            used |= {int(p) for p in row if p >= 0}
+    return used
+
+
+def test_kv_pages_live_only_on_lent_pages(lib):
+    from paged_moe_expert_gb300.pipeline import KVPages
+    rng = np.random.default_rng(8)
+    L, E, page, kvb = 3, 6, 64, 16                        # 4 KV pages per expert page
+    probs = rng.dirichlet(np.ones(E), size=L).astype(np.float32)
+    pages = 3 * E * L + 6
+    a = Adjuster(probs, [E] * L, 4, pages)
+    kv = KVPages(a, pages, page, kvb)
+    # request 1 takes 5 KV pages: two expert pages lent, the request's pages share them
+    assert kv.allocate(1, 5) == 0
+    offs = kv.live()[1]
+    assert len({o // page for o in offs}) == 2 and a.free_pages() == 4
+    # request 2 has no page yet: it takes the free KV pages already split off (request 1's
+    # second expert page) before another expert page is lent
+    assert kv.allocate(2, 2) == 0
+    assert {o // page for o in kv.live()[2]} == {max(o // page for o in offs)}
+    before = a.free_pages()
+    kv.release(1)
+    assert a.free_pages() == before + 1                    # request 1's full page came back
+    live = kv.live()[2]
+    assert all(o // page not in expert_pages_in_use(a, L) for o in live)
+
+
+def test_random_rounds_keep_kv_and_experts_apart(lib):
+    from paged_moe_expert_gb300.pipeline import KVPages
+    rng = np.random.default_rng(9)
+    L, E, page, kvb = 4, 8, 64, 16
+    probs = rng.dirichlet(np.full(E, 0.5), size=L).astype(np.float32)
+    pages = 3 * E * L + 9
+    a = Adjuster(probs, [E] * L, 5, pages)
+    kv = KVPages(a, pages, page, kvb)
+    active, nxt, waiting = {}, 0, {}
+    for rnd in range(60):
+        departures = [r for r in list(active) if rng.random() < 0.3]
+        for r in departures:
+            del active[r]
+        arrivals = dict(waiting)
+        waiting = {}
+        for _ in range(int(rng.integers(0, 4))):
+            arrivals[nxt] = int(rng.integers(1, 9))
+            nxt += 1
+        for r in departures:
+            kv.release(r)
+        short_kv = 0
+        for r, n in arrivals.items():
+            miss = kv.allocate(r, n)
+            active[r] = True
+            if miss:
+                waiting[r] = miss
+                short_kv += miss
+        a.decide(-(-short_kv // kv.per_page))
+        # experts (including the evicted ones still readable this pass) never share a page with KV
+        kv_pages = {o // page for offs in kv.live().values() for o in offs}
+        assert not kv_pages & expert_pages_in_use(a, L)
+        spans = sorted(o for offs in kv.live().values() for o in offs)
+        assert len(spans) == len(set(spans))
+        a.end_forward()
+    assert nxt > 0

@@ -132,3 +132,62 @@ def test_elastic_stack_follows_the_adjuster_and_equals_resident_stack(backend):
                     assert np.array_equal(g, m), (s, l, e)
     assert kinds == {1, -1}, "the trace must make the adjuster both add and evict"
     assert stack.filled_experts > 0
+
+
+def test_elastic_stack_with_kv_pages_keeps_kv_and_outputs_intact():
+    """KV cache pages carved from lent expert pages (the unified pool) hold what was written to
+    them through the memory view while the adjuster evicts and adds experts and the stack runs;
+    the outputs stay equal to the all-resident stack's."""
+    from paged_moe_expert_gb300 import pool as pl
+    cfg = syn.custom_config("elastic_kv", d=256, f=256, E=8, k=2, S=1, n_buffered=0)
+    w = syn.make_weights(cfg)
+    L, T = 4, 24
+    rng = np.random.default_rng(11)
+    probs = rng.dirichlet(np.full(cfg.E, 0.5), size=L).astype(np.float32)
+    cached = [6, 5, 7, 8]
+    expert_pages = 3 * sum(cached) + 6
+    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, cached, offload_limit=4,
+                                        expert_pages=expert_pages)
+    page_bytes = cfg.f * cfg.d * 2
+    kvb = page_bytes // 8
+    kv = pipeline.KVPages(stack.adj, expert_pages, page_bytes, kvb)
+    res = pipeline.DecodeStack(cfg, w, L, n_offload=0, layouts=1, seed=2)
+    base = stack.base * page_bytes
+    hidden_np = syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(np.float32))
+    hidden = torch.from_numpy(hidden_np.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = pm.alloc_workspace(stack.desc, T)
+    acts = [torch.empty_like(hidden) for _ in range(2)]
+    sig, active, waiting, nxt, kinds = {}, set(), {}, 0, set()
+
+    def view(o):
+        return pl.page_view(stack.pool, base + o, kvb, torch.int16, (kvb // 2,))
+
+    for s_ in range(10):
+        departures = [r for r in sorted(active) if rng.random() < 0.35]
+        live = kv.live()
+        for r in departures:
+            active.discard(r)
+            for o in live.get(r, []):
+                sig.pop(o, None)
+        arrivals = dict(waiting)
+        for _ in range(int(rng.integers(1, 4))):
+            arrivals[nxt] = int(rng.integers(4, 40))
+            nxt += 1
+        changes, short, waiting = stack.round_requests(kv, arrivals, departures)
+        kinds |= set(changes[:, 0].tolist())
+        for r, offs in kv.live().items():
+            active.add(r)
+            for o in offs:
+                if o not in sig:
+                    sig[o] = (r % 30000) + 1
+                    view(o).fill_(sig[o])
+        lg = [syn.bf16_bits_to_f32(syn.to_bf16_bits(rng.standard_normal((T, cfg.E)).astype(np.float32)))
+              for _ in range(L)]
+        sched = stack.schedule(lg)
+        y = stack.step(hidden, [torch.from_numpy(x).cuda() for x in lg], sched, acts, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(out_bits(y), run(res, hidden, [lg], T)[0]), "step %d" % s_
+        for o, v in sig.items():
+            t = view(o)
+            assert int(t.min()) == v and int(t.max()) == v, (s_, o)
+    assert -1 in kinds, "the KV demand must make the adjuster evict"
