@@ -138,7 +138,7 @@ def test_elastic_stack_with_kv_pages_keeps_kv_and_outputs_intact():
     """KV cache pages carved from lent expert pages (the unified pool) hold what was written to
     them through the memory view while the adjuster evicts and adds experts and the stack runs;
     the outputs stay equal to the all-resident stack's."""
-    from paged_moe_expert_gb300 import pool as pl
+    from paged_moe_expert_gb300 import tiers as tr
     cfg = syn.custom_config("elastic_kv", d=256, f=256, E=8, k=2, S=1, n_buffered=0)
     w = syn.make_weights(cfg)
     L, T = 4, 24
@@ -160,7 +160,7 @@ def test_elastic_stack_with_kv_pages_keeps_kv_and_outputs_intact():
     sig, active, waiting, nxt, kinds = {}, set(), {}, 0, set()
 
     def view(o):
-        return pl.page_view(stack.pool, base + o, kvb, torch.int16, (kvb // 2,))
+        return tr.page_view(stack.pool, base + o, kvb, torch.int16, (kvb // 2,))
 
     for s_ in range(10):
         departures = [r for r in sorted(active) if rng.random() < 0.35]
