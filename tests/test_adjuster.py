@@ -363,3 +363,66 @@ def test_random_rounds_keep_kv_and_experts_apart(lib):
         assert len(spans) == len(set(spans))
         a.end_forward()
     assert nxt > 0
+
+
+def test_kv_pages_on_native_allocators_match_the_oracles(lib):
+    """The same request rounds through KVPages (native adjuster and tiers) and through the same
+    composition over the two oracles give the same KV offsets, change lists and free counts."""
+    from oracle.tiers import EXPERT as O_EXPERT, KV as O_KV, TiersOracle
+    from paged_moe_expert_gb300.pipeline import KVPages
+
+    class OracleKV:
+        def __init__(self, adj, pages, page, kvb):
+            self.t = TiersOracle(pages * page, page, 0, kvb, 0)
+            for p in range(pages):
+                assert self.t.alloc(O_EXPERT) == p * page
+            self.adj, self.page, self.req = adj, page, {}
+
+        def allocate(self, rid, n):
+            got = self.req.setdefault(rid, [])
+            for i in range(n):
+                off = self.t.alloc(O_KV, rid)
+                if off is None and self.adj.free_pages() > 0:
+                    p = self.adj.lend(1)[0]
+                    self.t.free(O_EXPERT, p * self.page)
+                    off = self.t.alloc(O_KV, rid)
+                if off is None:
+                    return n - i
+                got.append(off)
+            return 0
+
+        def release(self, rid):
+            for off in self.req.pop(rid, []):
+                self.t.free(O_KV, off)
+            c = self.t.stats()
+            for _ in range(c[1] + c[2]):
+                off = self.t.alloc(O_EXPERT)
+                self.adj.give_back([off // self.page])
+
+    rng = np.random.default_rng(12)
+    L, E, page, kvb = 3, 8, 64, 16
+    probs = rng.dirichlet(np.full(E, 0.5), size=L).astype(np.float32)
+    pages = 3 * E * L + 7
+    a, o = Adjuster(probs, [E] * L, 5, pages), AdjusterOracle(probs, [E] * L, 5, pages)
+    kn, ko = KVPages(a, pages, page, kvb), OracleKV(o, pages, page, kvb)
+    active, nxt = set(), 0
+    for rnd in range(50):
+        departures = [r for r in sorted(active) if rng.random() < 0.3]
+        for r in departures:
+            active.discard(r)
+            kn.release(r)
+            ko.release(r)
+        short = 0
+        for _ in range(int(rng.integers(0, 4))):
+            n = int(rng.integers(1, 10))
+            mn, mo = kn.allocate(nxt, n), ko.allocate(nxt, n)
+            assert mn == mo
+            short += mn
+            active.add(nxt)
+            nxt += 1
+        assert kn.live() == {r: v for r, v in ko.req.items()}
+        R = -(-short // (page // kvb))
+        assert a.decide(R).tolist() == o.decide(R)
+        assert a.free_pages() == o.free_pages()
+        a.end_forward()
+        o.end_forward()
