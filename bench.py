@@ -502,6 +502,83 @@ def codec_bench(args):
         "h2d_uncompressed_ms": h2d_s * 1e3, "h2d_gbs": raw / h2d_s / 1e9, "bit_exact": ok}), flush=True)
 
 
+def elastic_requests(args):
+    """The elastic stack with KV cache pages in the same pool: requests arrive and leave (a
+    seeded trace whose arrival rate rises and falls), each holding KV pages of 1/8 expert page
+    carved from expert pages the adjuster lends; requests that do not fit wait for a later round.
+    24 Qwen1.5-MoE-shaped layers, 16 tokens per step.  One JSON line per phase."""
+    from paged_moe_expert_gb300 import pipeline
+    import paged_moe_expert_gb300 as pm
+    torch.cuda.set_device(0)
+    cfg = syn.CONFIGS["qwen15"]
+    w = syn.make_weights(cfg)
+    L, T, E = args.layers, args.elastic_tokens, cfg.E
+    rng = np.random.default_rng(29)
+    bias = rng.standard_normal((L, E)).astype(np.float32)
+
+    def draw(n):
+        return [syn.bf16_bits_to_f32(syn.to_bf16_bits(
+            rng.standard_normal((n, E)).astype(np.float32) + bias[l])) for l in range(L)]
+
+    sample = draw(4096)
+    probs = np.stack([np.bincount(np.argsort(-lg, axis=1, kind="stable")[:, :cfg.k].ravel(),
+                                  minlength=E) / (4096.0 * cfg.k) for lg in sample]).astype(np.float32)
+    expert_pages = 3 * E * L + 3 * 4
+    stack = pipeline.ElasticDecodeStack(cfg, w, L, probs, [E] * L, args.offload_limit, expert_pages,
+                                        backend=args.backend)
+    page_bytes = cfg.f * cfg.d * 2
+    kv = pipeline.KVPages(stack.adj, expert_pages, page_bytes, page_bytes // 8)
+    hidden = torch.from_numpy(syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(
+        np.float32)).view(np.int16)).view(torch.bfloat16).cuda()
+    ws = pm.alloc_workspace(stack.desc, T)
+    acts = [torch.empty_like(hidden) for _ in range(2)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    phases = [("quiet", 10, 0.5), ("arrivals rise", 25, 6.0), ("busy", 25, 6.0),
+              ("arrivals fall", 25, 1.0), ("quiet again", 25, 0.2)]
+    live_until, waiting, nxt, rnd = {}, {}, 0, 0
+    for name, rounds, rate in phases:
+        rec = {"ms": [], "kv_pages": [], "waiting": [], "resident": [], "adds": 0, "evicts": 0}
+        for _ in range(rounds):
+            departures = [r for r, end in live_until.items() if end <= rnd]
+            for r in departures:
+                del live_until[r]
+            arrivals = dict(waiting)
+            for _ in range(int(rng.poisson(rate))):
+                arrivals[nxt] = int(rng.integers(8, 65))
+                nxt += 1
+            f0 = stack.filled_experts
+            changes, short, waiting = stack.round_requests(kv, arrivals, departures)
+            for r in arrivals:
+                if r not in waiting:
+                    live_until[r] = rnd + int(rng.integers(3, 16))
+            lg = draw(T)
+            sched = stack.schedule(lg)
+            lg_dev = [torch.from_numpy(x).cuda() for x in lg]
+            a.record()
+            stack.step(hidden, lg_dev, sched, acts, ws)
+            b.record()
+            torch.cuda.synchronize()
+            rec["ms"].append(a.elapsed_time(b))
+            rec["kv_pages"].append(sum(len(v) for v in kv.live().values()))
+            rec["waiting"].append(len(waiting))
+            rec["resident"].append(int(stack.adj.cached().sum()))
+            rec["adds"] += stack.filled_experts - f0
+            rec["evicts"] += int((changes[:, 0] == -1).sum()) if len(changes) else 0
+            rnd += 1
+        print(json.dumps({
+            "metric": "elastic decode with KV pages in the expert pool: request-driven rounds",
+            "config": {"workload": "%d Qwen1.5-MoE-shaped layers, %d tokens/step, KV page = 1/8 "
+                       "expert page, %d expert pages, offload limit %d" % (L, T, expert_pages,
+                                                                           args.offload_limit),
+                       "phase": name, "rounds": rounds, "arrivals_per_round": rate},
+            "ms_per_step_median": float(np.median(rec["ms"])),
+            "ms_per_step_max": float(np.max(rec["ms"])),
+            "kv_pages_end": rec["kv_pages"][-1], "kv_pages_max": max(rec["kv_pages"]),
+            "requests_waiting_max": max(rec["waiting"]),
+            "resident_experts": [min(rec["resident"]), max(rec["resident"])],
+            "experts_added": rec["adds"], "experts_evicted": rec["evicts"]}), flush=True)
+
+
 def elastic_sweep(args):
     """24 Qwen1.5-MoE-shaped layers on ONE page pool shared with the KV cache.  A KV demand
     trace (in expert pages) rises and falls over the rounds; each round the KV pages are taken
@@ -604,6 +681,8 @@ def main():
                     help="page lookup vs remapped contiguous view vs contiguous allocation")
     ap.add_argument("--elastic-sweep", action="store_true",
                     help="adjuster-driven 24-layer decode over a KV demand trace")
+    ap.add_argument("--elastic-requests", action="store_true",
+                    help="elastic decode with request KV pages carved from the expert pool")
     ap.add_argument("--elastic-tokens", type=int, default=16)
     ap.add_argument("--offload-limit", type=int, default=30)
     ap.add_argument("--kv-peak", type=int, default=1800)
@@ -613,6 +692,9 @@ def main():
         return
     if args.elastic_sweep:
         elastic_sweep(args)
+        return
+    if args.elastic_requests:
+        elastic_requests(args)
         return
     if args.vmm_overhead:
         vmm_overhead(args)
