@@ -230,6 +230,24 @@ def test_fused_back_to_back_calls_reuse_the_grid_barrier():
     assert_close(first, ref["out_bf16"])
 
 
+def test_fused_calls_with_changing_token_counts_share_one_plan():
+    """One plan serves fused calls of different token counts in turn (1, 16, 5, 1, 32, 1): the
+    grid barrier's per-CTA words stay in step across them, no call times out, and each output
+    matches the oracle."""
+    cfg = syn.custom_config("mixT", d=256, f=384, E=16, k=4, S=2, n_buffered=3)
+    L = setup_layer(cfg, 32)
+    L.plan.set_path(pm.PATH_FUSED)
+    orc = oracle_layer(cfg, L.w)
+    ws = pm.alloc_workspace(L.desc, 32)
+    for T in (1, 16, 5, 1, 32, 1):
+        h, lg = syn.make_tokens(cfg, T)
+        out = L.plan.forward(pl._bf16(h).cuda(), torch.from_numpy(lg).cuda(), L.page_table,
+                             L.buf_slot, workspace=ws)
+        torch.cuda.synchronize()
+        assert L.plan.device_error() == 0, "T=%d" % T
+        assert_close(out_bits(out), orc.forward(h, lg)["out_bf16"], "T=%d" % T)
+
+
 def test_pair_path_back_to_back_calls_are_identical():
     """Many CTA-pair calls in a row on one workspace, with more tiles than CTA pairs and odd
     blocks (M=128 units), stay bit-identical and match the oracle."""
