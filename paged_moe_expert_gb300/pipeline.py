@@ -11,8 +11,9 @@ compute stream.
 
 `DecodeStack` runs L layers of one MoE shape.  Layer l keeps its resident experts in pool pages
 (cycling over a few pre-placed pool layouts, one per step, to mimic pages moving between steps);
-its offloaded experts live in pinned host memory and are copied into load buffer l % 2 on a side
-stream one layer ahead of compute:
+its offloaded experts live in pinned host memory (or, with the compressed backend, as
+exponent-Huffman blobs in device memory that libpmoe's decoder expands) and are brought into load
+buffer l % 2 on a side stream one layer ahead of compute:
 
     iteration l:  copy stream: wait free[(l+1)%2]  -> copy layer l+1's experts -> record ready[(l+1)%2]
                   compute:     wait ready[l%2]      -> forward layer l            -> record free[l%2]
@@ -22,10 +23,13 @@ adjuster (libpmoe's native `pmoe_adjuster_*`) decide each round which experts st
 adjuster..."): KV pages are lent out of the free pages first, a remaining shortfall R_b makes the
 adjuster evict, surplus free pages make it add; added experts are copied into their reserved
 pages on a fill stream and a layer's page table points at them only after that copy; evicted
-experts keep their pages until the round's forward pass has ended.
+experts keep their pages until the round's forward pass has ended.  `KVPages` gives KV cache pages
+finer than an expert page ("One pool for data whose sizes differ by orders of magnitude"): the
+three-tier allocator carves them out of expert pages the adjuster lends, and
+`ElasticDecodeStack.round_requests` runs a round with KV pages per request.
 
 Only host bookkeeping lives here (which experts, which slots, which events); every copy is one
-cudaMemcpyAsync issued by libpmoe and every step of the layer runs in its kernels.
+cudaMemcpyAsync or decode launch issued by libpmoe and every step of the layer runs in its kernels.
 """
 from __future__ import annotations
 
