@@ -852,6 +852,11 @@ def main():
             ps = lay.plan.last_run()[0]
             gp, gc = capture(fp), capture(fc)
             tp, tc = time_iters([gp.replay, gc.replay], args.sweep_iters, flush)
+            # a timing is only a timing if no kernel reported an error (a bounded wait that ran
+            # out would otherwise show up as a slow point)
+            for pl_ in (lay.plan, lay.cplan):
+                if pl_.device_error() != 0:
+                    raise RuntimeError("device error word set during the %d-token sweep point" % Ts)
             ea = lay.e_act(ls)
             wk_s = work(cfg, Ts, ea)
             frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks)
