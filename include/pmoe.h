@@ -263,7 +263,9 @@ pmoe_status pmoe_fill_pages_async(pmoe_plan_t plan, int32_t n, const void* const
  * copy.  Reading an unmapped virtual page faults the GPU, so a caller launches a kernel on the
  * view only once every page that kernel can read is mapped (pmoe_vmm_lookup).  All calls are
  * host calls; they allocate device memory only in pmoe_vmm_create and free it in
- * pmoe_vmm_destroy. */
+ * pmoe_vmm_destroy, and each makes the view's device current for its driver calls and then puts
+ * the caller's current device back.  Driver failures return PMOE_ERR_CUDA with
+ * pmoe_last_error() set. */
 typedef struct pmoe_vmm* pmoe_vmm_t;
 
 /* Smallest block size (bytes) the device's VMM maps, or 0 with a status on error. */
