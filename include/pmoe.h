@@ -161,6 +161,34 @@ pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
                               const int32_t* buf_slot, void* out, void* workspace,
                               size_t workspace_bytes, pmoe_stream_t stream);
 
+/* Where the plan's last forward call (moe_paged_forward or moe_contig_forward, with T tokens)
+ * left its routing and sort state in its workspace, so that a test can read back what the kernels
+ * of that very call computed and compare it with an independent implementation.  Each field is a
+ * byte offset into that call's workspace, or -1 when the call's kernel family does not write the
+ * array.  The contents stay valid until the workspace is reused.  PMOE_ERR_INVALID_ARG when T is
+ * not the token count of the plan's last forward call.  Host only: no device access. */
+typedef struct {
+    int32_t path;          /* pmoe_path the call ran */
+    int32_t tokens;        /* its T */
+    int32_t block_m;       /* rows per sorted block; 0 on the fused path, which sorts nothing */
+    int32_t top_k;         /* k */
+    int64_t ids;           /* int32 [T][k]: the k experts of each token, largest logit first
+                              (the fused path: CTA 0's routing, every CTA routes the same way) */
+    int64_t weights;       /* fp32 [T][k]: their routing weights */
+    int64_t sorted_ids;    /* int32 [n_padded]: the pair in each sorted row (pads hold T*(k+S)) */
+    int64_t block_expert;  /* int32 [n_padded / block_m]: the expert of each block */
+    int64_t inv;           /* int32 [T*(k+S)]: the sorted row of each pair */
+    int64_t meta;          /* int32 [16]: [0] n_padded (sorting paths), [1] work units and [2] of
+                              them single blocks (CTA-pair path), [3] active slots (fused path) */
+    int64_t block_rows;    /* int32 [n_padded / block_m]: valid rows of each block (PMOE_PATH_TC) */
+    int64_t units;         /* int32 [meta[1]][4]: CTA-pair work units {first block << 1 | single
+                              block, expert, W1 location, W3 location}, location = map << 29 | page
+                              with map 0 pool, 1 + b load buffer b (PMOE_PATH_TC2) */
+    int64_t active;        /* int32 [meta[3]]: the expert of each active slot, shared chunks
+                              E..E+S-1 first, then the routed experts in ascending id (fused path) */
+} pmoe_routing_view;
+pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_view* out);
+
 /* The contiguous twin of moe_paged_forward: the same kernels with the page lookup replaced by
  * fixed addressing, for a plan whose pool holds expert e's W1, W3, W2 as pages 3e, 3e+1, 3e+2
  * (shared chunk s as expert E+s).  It exists to measure the cost of the page lookup against
@@ -180,8 +208,11 @@ pmoe_status moe_contig_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
  * process exits; a call whose layer and T need more returns PMOE_ERR_WORKSPACE (the
  * Qwen1.5-MoE-shaped layer fits up to 16 tokens).  All calls share that array and it keeps the
  * last call's contents, so calls that overlap on the GPU (other streams, other threads) race:
- * serialise them.  device_error (device int32, may be NULL) receives a table error code and is
- * not cleared by the call.  The first call on a device looks up the array's device address
+ * serialise them.  device_error (device int32, required: PMOE_ERR_INVALID_ARG when NULL) receives
+ * a table error code (an out-of-range page or slot of a routed expert; the output is then
+ * undefined) and is not cleared by the call.  The same host checks as pmoe_plan_create apply
+ * (descriptor, supported shape, 16-byte aligned pool, load buffers, hidden and out) and run
+ * before any device work.  The first call on a device looks up the array's device address
  * (with that device current); make that first call before any stream capture. */
 pmoe_status moe_paged_forward_noalloc(const pmoe_layer_desc* desc, const void* page_pool,
                                       int64_t num_pages, const void* load_buf0,

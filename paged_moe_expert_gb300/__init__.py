@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -118,6 +119,36 @@ class Plan:
         _lib.check(_lib.load().pmoe_plan_last_run(self._h, ctypes.byref(p), ctypes.byref(n),
                                                   ctypes.byref(k)))
         return int(p.value), int(n.value), int(k.value)
+
+    def routing_state(self, workspace: torch.Tensor, T: int) -> dict:
+        """The routing and sort state the last forward call (T tokens, this workspace) left in the
+        workspace, copied to host numpy arrays (pmoe_plan_routing_view gives the offsets).  Keys:
+        path, block_m, ids [T,k], weights [T,k], meta [16], and when the call's path writes them
+        sorted_ids [n_padded], block_expert, inv, block_rows, units [n,4], active."""
+        v = _lib.RoutingView()
+        _lib.check(_lib.load().pmoe_plan_routing_view(self._h, int(T), ctypes.byref(v)))
+        torch.cuda.synchronize(workspace.device)
+        ws = workspace.cpu().numpy()
+        k, S, E = self.desc.top_k, self.desc.num_shared_chunks, self.desc.num_experts
+
+        def arr(off, n, dt=np.int32):
+            return ws[off:off + 4 * n].view(dt).copy()
+
+        meta = arr(v.meta, 16)
+        out = {"path": int(v.path), "block_m": int(v.block_m), "meta": meta,
+               "ids": arr(v.ids, T * k).reshape(T, k), "weights": arr(v.weights, T * k, np.float32).reshape(T, k)}
+        if v.sorted_ids >= 0:
+            npad = int(meta[0])
+            out["sorted_ids"] = arr(v.sorted_ids, npad)
+            out["block_expert"] = arr(v.block_expert, npad // v.block_m)
+            out["inv"] = arr(v.inv, T * (k + S))
+        if v.block_rows >= 0:
+            out["block_rows"] = arr(v.block_rows, int(meta[0]) // v.block_m)
+        if v.units >= 0:
+            out["units"] = arr(v.units, 4 * int(meta[1])).reshape(-1, 4)
+        if v.active >= 0:
+            out["active"] = arr(v.active, int(meta[3]))
+        return out
 
     def set_profile_events(self, events):
         """Record events[i] before the forward's i-th kernel (and one after the last); pass

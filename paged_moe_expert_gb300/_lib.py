@@ -29,6 +29,12 @@ class LayerDesc(ctypes.Structure):
                 ("renormalize", I32), ("num_shared_chunks", I32), ("slots_per_buffer", I32)]
 
 
+class RoutingView(ctypes.Structure):
+    _fields_ = [("path", I32), ("tokens", I32), ("block_m", I32), ("top_k", I32), ("ids", I64),
+                ("weights", I64), ("sorted_ids", I64), ("block_expert", I64), ("inv", I64),
+                ("meta", I64), ("block_rows", I64), ("units", I64), ("active", I64)]
+
+
 # name -> (restype, argtypes); mirrors include/pmoe.h
 SIGNATURES = {
     "pmoe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -42,6 +48,7 @@ SIGNATURES = {
     "pmoe_workspace_size": (SZ, [ctypes.POINTER(LayerDesc), I32]),
     "moe_paged_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, P, P, SZ, P]),
     "moe_contig_forward": (ctypes.c_int, [P, P, I32, P, I32, P, P, SZ, P]),
+    "pmoe_plan_routing_view": (ctypes.c_int, [P, I32, ctypes.POINTER(RoutingView)]),
     "moe_paged_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(LayerDesc), P, I64, P, P, P, I32, P,
                                                   I32, P, P, P, P, P]),
     "pmoe_prefetch_async": (ctypes.c_int, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(I32), P, P, P]),

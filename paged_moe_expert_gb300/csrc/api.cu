@@ -43,7 +43,7 @@ static size_t plan_words_bytes(const pmoe_layer_desc& D) {
     return 2048 + 12 * tiles;
 }
 
-static bool desc_ok(const pmoe_layer_desc* D) {
+bool desc_ok(const pmoe_layer_desc* D) {
     if (!D) return false;
     if (D->d <= 0 || D->f <= 0 || D->num_experts <= 0 || D->top_k <= 0) return false;
     if (D->top_k > D->num_experts || D->top_k > kMaxTopK) return false;
@@ -53,7 +53,7 @@ static bool desc_ok(const pmoe_layer_desc* D) {
     return true;
 }
 
-static bool shape_supported(const pmoe_layer_desc* D) {
+bool shape_supported(const pmoe_layer_desc* D) {
     return D->d % 64 == 0 && D->f % 128 == 0 && D->d <= 16384 && D->f <= 65536;
 }
 
@@ -275,6 +275,10 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         fa.ucnt = P->d_ucnt;
         fa.hflag = P->d_hflag;
         fa.err = P->d_error;
+        fa.ids_out = ids;
+        fa.w_out = w;
+        fa.active_out = sorted;
+        fa.meta_out = meta;
         fa.num_pages = P->num_pages;
         fa.p1_base1 = F.u1_shared + grid;
         // the shared chunks' gate/up (streamed before routing is known) goes to the first g0
@@ -304,6 +308,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         P->last_path = path;
         P->last_kernels = 1;
         P->last_launches = 1;
+        P->last_T = T;
+        P->last_block_m = 0;
         return PMOE_OK;
     }
 
@@ -439,6 +445,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
                              static_cast<uint16_t*>(out), stream), "combine");
     PMOE_CUDA(mark(P, ev++, stream), "profile event");
     P->last_path = path;
+    P->last_T = T;
+    P->last_block_m = bm;
     P->last_kernels = ev - 1;
     P->last_launches = ev - 1 + (!prep && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
     return PMOE_OK;
@@ -554,6 +562,34 @@ pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* e
     if (!P || n < 0 || n > 16 || (n > 0 && !events)) return fail(PMOE_ERR_INVALID_ARG, "bad profile events");
     for (int i = 0; i < n; ++i) P->prof_ev[i] = (cudaEvent_t)events[i];
     P->n_prof = n;
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_view* out) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P || !out) return fail(PMOE_ERR_INVALID_ARG, "NULL plan or view");
+    if (P->last_T <= 0 || T != P->last_T)
+        return fail(PMOE_ERR_INVALID_ARG, "T differs from the token count of the plan's last forward call");
+    const WsLayout W = layout(P->desc, T);
+    pmoe_routing_view v;
+    v.path = P->last_path;
+    v.tokens = T;
+    v.block_m = P->last_block_m;
+    v.top_k = P->desc.top_k;
+    v.ids = (int64_t)W.ids;
+    v.weights = (int64_t)W.w;
+    v.meta = (int64_t)W.meta;
+    v.sorted_ids = v.block_expert = v.inv = v.block_rows = v.units = v.active = -1;
+    if (v.path == PMOE_PATH_FUSED) {
+        v.active = (int64_t)W.sorted;
+    } else {
+        v.sorted_ids = (int64_t)W.sorted;
+        v.block_expert = (int64_t)W.bexp;
+        v.inv = (int64_t)W.inv;
+        if (v.path == PMOE_PATH_TC) v.block_rows = (int64_t)W.brows;
+        if (v.path == PMOE_PATH_TC2) v.units = (int64_t)W.units;
+    }
+    *out = v;
     return PMOE_OK;
 }
 

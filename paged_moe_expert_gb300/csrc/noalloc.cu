@@ -47,7 +47,7 @@ cudaError_t scratch_address(void** out) {
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct NoAllocLayout {
-    size_t err, ids, w, sorted, bexp, inv, meta, loc, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, h, y, total;
     int64_t np, cap, nblk;
     int bm, splits;
 };
@@ -66,7 +66,6 @@ NoAllocLayout noalloc_layout(const pmoe_layer_desc& D, int64_t T) {
     L.nblk = (L.np + bm - 1) / bm + active;
     L.splits = (D.f + kStreamKChunk - 1) / kStreamKChunk;
     size_t o = 0;
-    L.err = o;    o = up256(o + sizeof(int32_t));
     L.ids = o;    o = up256(o + sizeof(int32_t) * T * D.top_k);
     L.w = o;      o = up256(o + sizeof(float) * T * D.top_k);
     L.sorted = o; o = up256(o + sizeof(int32_t) * L.cap);
@@ -80,9 +79,6 @@ NoAllocLayout noalloc_layout(const pmoe_layer_desc& D, int64_t T) {
     return L;
 }
 
-// Failures are reported by status code alone (see pmoe_status_string).
-pmoe_status na_fail(pmoe_status s, const char*) { return s; }
-
 }  // namespace
 
 }  // namespace pmoe
@@ -94,31 +90,31 @@ extern "C" pmoe_status moe_paged_forward_noalloc(
     const void* load_buf1, const void* hidden, int32_t T, const float* router_logits,
     int32_t top_k, const int32_t* page_table, const int32_t* buf_slot, void* out,
     int32_t* device_error, pmoe_stream_t stream) {
-    if (!desc || desc->d <= 0 || desc->f <= 0 || desc->num_experts <= 0 || desc->top_k <= 0 ||
-        desc->top_k > desc->num_experts || desc->top_k > kMaxTopK || desc->num_shared_chunks < 0 ||
-        desc->slots_per_buffer < 0 || desc->num_experts + desc->num_shared_chunks > kMaxExpertsTotal ||
-        desc->top_k + desc->num_shared_chunks > kMaxPairsPerToken)
-        return na_fail(PMOE_ERR_INVALID_ARG, "bad layer descriptor");
-    if (desc->d % 64 != 0 || desc->f % 128 != 0)
-        return na_fail(PMOE_ERR_UNSUPPORTED, "d must be a multiple of 64 and f of 128");
-    if (T < 0 || top_k != desc->top_k) return na_fail(PMOE_ERR_INVALID_ARG, "bad T or top_k");
+    if (!desc_ok(desc)) return record_failure(PMOE_ERR_INVALID_ARG, "bad layer descriptor");
+    if (!shape_supported(desc))
+        return record_failure(PMOE_ERR_UNSUPPORTED, "d must be a multiple of 64 (<= 16384) and f of 128 (<= 65536)");
+    if (T < 0 || top_k != desc->top_k) return record_failure(PMOE_ERR_INVALID_ARG, "bad T or top_k");
     if (T == 0) return PMOE_OK;
     if (!page_pool || num_pages <= 0 || !hidden || !router_logits || !page_table || !buf_slot || !out)
-        return na_fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
-    if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15) || ((uintptr_t)page_pool & 15))
-        return na_fail(PMOE_ERR_INVALID_ARG, "hidden, out and the pool must be 16-byte aligned");
+        return record_failure(PMOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!device_error)
+        return record_failure(PMOE_ERR_INVALID_ARG, "device_error is NULL: table errors would go unreported");
+    if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15) || ((uintptr_t)page_pool & 15) ||
+        ((uintptr_t)load_buf0 & 15) || ((uintptr_t)load_buf1 & 15))
+        return record_failure(PMOE_ERR_INVALID_ARG,
+                              "hidden, out, the pool and the load buffers must be 16-byte aligned");
     if ((int64_t)T * (desc->top_k + desc->num_shared_chunks) > (int64_t)1 << 24)
-        return na_fail(PMOE_ERR_WORKSPACE, "too many tokens for the fixed scratch");
+        return record_failure(PMOE_ERR_WORKSPACE, "too many tokens for the fixed scratch");
     const NoAllocLayout W = noalloc_layout(*desc, T);
     if (W.total > kNoAllocScratchBytes)
-        return na_fail(PMOE_ERR_WORKSPACE, "layer and token count exceed the fixed scratch");
+        return record_failure(PMOE_ERR_WORKSPACE, "layer and token count exceed the fixed scratch");
 
     void* base = nullptr;
     cudaError_t e = scratch_address(&base);
-    if (e != cudaSuccess) return na_fail(PMOE_ERR_CUDA, "scratch address lookup failed");
+    if (e != cudaSuccess) return record_failure(PMOE_ERR_CUDA, "scratch address lookup failed");
     char* ws = static_cast<char*>(base);
     cudaStream_t s = (cudaStream_t)stream;
-    int32_t* err = device_error ? device_error : reinterpret_cast<int32_t*>(ws + W.err);
+    int32_t* err = device_error;
     int32_t* ids = reinterpret_cast<int32_t*>(ws + W.ids);
     float* w = reinterpret_cast<float*>(ws + W.w);
     int32_t* sorted = reinterpret_cast<int32_t*>(ws + W.sorted);
@@ -129,12 +125,8 @@ extern "C" pmoe_status moe_paged_forward_noalloc(
     uint16_t* h = reinterpret_cast<uint16_t*>(ws + W.h);
     float* y = reinterpret_cast<float*>(ws + W.y);
 
-    // The scratch keeps the previous call's contents.  Everything below is written before it is
-    // read, except the internal error word, which must start at zero.
-    if (!device_error) {
-        e = cudaMemsetAsync(err, 0, sizeof(int32_t), s);
-        if (e != cudaSuccess) return na_fail(PMOE_ERR_CUDA, "clearing the error word failed");
-    }
+    // The scratch keeps the previous call's contents; everything below is written before it is
+    // read.
     const pmoe_layer_desc& D = *desc;
     ResolveArgs rs{};
     rs.page_table = page_table;
@@ -161,6 +153,6 @@ extern "C" pmoe_status moe_paged_forward_noalloc(
                                  s)) != cudaSuccess ||
         (e = launch_combine(y, false, W.splits, W.cap, w, inv, T, D.d, D.top_k, D.num_shared_chunks,
                             static_cast<uint16_t*>(out), s)) != cudaSuccess)
-        return na_fail(PMOE_ERR_CUDA, "kernel launch failed");
+        return record_failure(PMOE_ERR_CUDA, "kernel launch failed");
     return PMOE_OK;
 }

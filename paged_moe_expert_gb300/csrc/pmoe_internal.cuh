@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pmoe.h"
 
 namespace pmoe {
@@ -39,7 +41,7 @@ struct WsLayout {
 };
 
 // meta[] slots
-enum { kMetaNPadded = 0, kMetaPairs = 1, kMetaSingles = 2, kMetaCount = 16 };
+enum { kMetaNPadded = 0, kMetaPairs = 1, kMetaSingles = 2, kMetaActive = 3, kMetaCount = 16 };
 
 struct Plan {
     pmoe_layer_desc desc;
@@ -57,6 +59,7 @@ struct Plan {
     cudaEvent_t prof_ev[16];   // measurement hook (pmoe_plan_set_profile_events)
     int n_prof;
     int last_path, last_kernels, last_launches;  // what the last forward ran
+    int last_T, last_block_m;                    // its token count and sorted block size
     int num_sms;
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
     CUtensorMap tm_rows_d64[3];  // the same views with 64-row boxes (stacked gate/up tiles)
@@ -65,6 +68,12 @@ struct Plan {
 
 // Sets the text pmoe_last_error() returns and passes the status through.
 pmoe_status record_failure(pmoe_status s, const char* msg);
+
+// Host checks shared by every entry point that takes a layer descriptor: sizes in range
+// (desc_ok) and a shape the kernels cover (shape_supported: d % 64, f % 128, d <= 16384,
+// f <= 65536).
+bool desc_ok(const pmoe_layer_desc* D);
+bool shape_supported(const pmoe_layer_desc* D);
 
 // Device helpers ----------------------------------------------------------------------------
 
@@ -109,6 +118,21 @@ __device__ __forceinline__ void pdl_allow_next() {
 }
 __device__ __forceinline__ void pdl_wait_prev() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`.  The attribute belongs to the current
+// device's context, so it is set once per device: `done` keeps one bit per device ordinal
+// (ordinals >= 64 set it on every call).  Racing first calls set the same value.
+inline cudaError_t raise_smem_limit(const void* kernel, int bytes,
+                                    std::atomic<unsigned long long>* done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+    if (bit && (done->load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done->fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 // Launch with the programmatic-stream-serialisation attribute.
@@ -258,6 +282,13 @@ struct FusedArgs {
     unsigned long long* ucnt;   // per gate/up tile: (epoch << 32 | pieces done) (plan-owned)
     uint32_t* hflag;            // per gate/up tile: epoch once its h is written (plan-owned)
     int32_t* err;
+    // CTA 0's routing and active-slot table, written to the workspace where the other paths keep
+    // their routing state (read back by pmoe_plan_routing_view): ids [T][k], weights [T][k],
+    // the expert of each active slot [A], and A in meta[kMetaActive]
+    int32_t* ids_out;
+    float* w_out;
+    int32_t* active_out;
+    int32_t* meta_out;
     int64_t num_pages;
     int64_t p1_base1;           // first piece slot of the routed gate/up space
     int g0;                     // CTAs that share the shared chunks' gate/up (1..grid)

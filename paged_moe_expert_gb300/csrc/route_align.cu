@@ -469,21 +469,17 @@ static size_t prep_smem_bytes(int T, int E, int k, int S) {
     return sizeof(int32_t) * ((size_t)align_words(E + S) + (size_t)T * k + E + 3 * (size_t)(E + S));
 }
 
-static cudaError_t allow_align_smem(const void* fn) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)prep_smem_bytes(128, kMaxExpertsTotal, kMaxTopK, 0));
+static cudaError_t allow_align_smem(const void* fn, std::atomic<unsigned long long>* done) {
+    return raise_smem_limit(fn, (int)prep_smem_bytes(128, kMaxExpertsTotal, kMaxTopK, 0), done);
 }
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int block_m,
                          int32_t* sorted_ids, int32_t* block_expert, int32_t* inv,
                          int32_t* meta, const ResolveArgs* resolve, cudaStream_t s) {
-    static bool attr_set = false;  // idempotent; racing first calls set the same value
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)align_smem_bytes(kMaxExpertsTotal));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(align_kernel),
+                                     (int)align_smem_bytes(kMaxExpertsTotal), &attr);
+    if (e != cudaSuccess) return e;
     ResolveArgs rs{};
     if (resolve) rs = *resolve;
     return launch_pdl(align_kernel, dim3(1), dim3(kAlignWarps * 32), align_smem_bytes(E + S), s,
@@ -511,13 +507,11 @@ cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, i
     const int ES = E + S;
     const int seg = (int)((NR + C - 1) / C);
     const size_t sm2 = sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * ES + 1);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * kMaxExpertsTotal + 1)));
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e0 = raise_smem_limit(reinterpret_cast<const void*>(align_scatter_kernel),
+                                      (int)(sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * kMaxExpertsTotal + 1)),
+                                      &attr);
+    if (e0 != cudaSuccess) return e0;
     ResolveArgs rs{};
     if (resolve) rs = *resolve;
     cudaError_t e = launch_pdl(align_count_kernel, dim3(C), dim3(kAlignWarps * 32),
@@ -542,12 +536,9 @@ static cudaError_t prep_small_epl(const float* logits, int T, int E, int k, int 
                                   int32_t* block_expert, int32_t* inv, int32_t* meta,
                                   const ResolveArgs& rs, const uint16_t* hidden, int d,
                                   uint16_t* x, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = allow_align_smem(reinterpret_cast<const void*>(prep_small_kernel<EPL>));
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = allow_align_smem(reinterpret_cast<const void*>(prep_small_kernel<EPL>), &attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(prep_small_kernel<EPL>, dim3(1), dim3(kAlignWarps * 32),
                       prep_smem_bytes(T, E, k, S), s, logits, T, E, k, renorm, ids, w, S, block_m,
                       sorted_ids, block_expert, inv, meta, rs, hidden, d, x);

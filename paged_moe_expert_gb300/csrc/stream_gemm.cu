@@ -210,20 +210,17 @@ __global__ void __launch_bounds__(kThreads) stream_gemm2_kernel(
 }
 
 template <typename K>
-cudaError_t allow_smem(K kernel) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+cudaError_t allow_smem(K kernel, std::atomic<unsigned long long>* done) {
+    return raise_smem_limit(reinterpret_cast<const void*>(kernel), 200 * 1024, done);
 }
 
 template <int MT, bool C>
 cudaError_t gemm1_mt(const LayerPtrs& L, const uint16_t* hidden, const int32_t* sorted_ids,
                      const int32_t* block_expert, const int32_t* meta, const ExpertLoc* loc,
                      int64_t nblk_max, uint16_t* h, cudaStream_t s) {
-    static bool ok = false;
-    if (!ok) {
-        cudaError_t e = allow_smem(stream_gemm1_kernel<MT, C>);
-        if (e != cudaSuccess) return e;
-        ok = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = allow_smem(stream_gemm1_kernel<MT, C>, &attr);
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(L.f / kRows1), (unsigned)nblk_max);
     const size_t smem = (size_t)MT * L.d * 2;
     return launch_pdl(stream_gemm1_kernel<MT, C>, grid, dim3(kThreads), smem, s, L, hidden, sorted_ids,
@@ -234,12 +231,9 @@ template <int MT, bool C>
 cudaError_t gemm2_mt(const LayerPtrs& L, const int32_t* sorted_ids, const int32_t* block_expert,
                      const int32_t* meta, const ExpertLoc* loc, int64_t nblk_max, int splits,
                      int64_t ystride, const uint16_t* h, float* y, cudaStream_t s) {
-    static bool ok = false;
-    if (!ok) {
-        cudaError_t e = allow_smem(stream_gemm2_kernel<MT, C>);
-        if (e != cudaSuccess) return e;
-        ok = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = allow_smem(stream_gemm2_kernel<MT, C>, &attr);
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(L.d / kRows2), (unsigned)nblk_max, (unsigned)splits);
     const size_t smem = (size_t)MT * (L.f < kStreamKChunk ? L.f : kStreamKChunk) * 2;
     return launch_pdl(stream_gemm2_kernel<MT, C>, grid, dim3(kThreads), smem, s, L, sorted_ids,

@@ -376,13 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int kMode, int BN, bool kContig>
 cudaError_t launch_swap_one(const SwapMaps& maps, const SwapArgs& a, int grid, cudaStream_t s) {
     using C = Cfg<kMode, BN>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_swap_kernel<kMode, BN, kContig>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(tc_swap_kernel<kMode, BN, kContig>),
+                                     C::SMEM, &attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(tc_swap_kernel<kMode, BN, kContig>, dim3(grid), dim3(kThreads), C::SMEM, s, maps, a);
 }
 

@@ -541,6 +541,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) TRACE(19);   // slots assigned
         const int A = S + Ar;
         const int32_t I1 = Ar * F64 * KB1, I2 = A * M2 * KB2;
+        if (cta == 0) {
+            // CTA 0's routing and slot table go to the workspace, where the other paths keep their
+            // routing state, so the call can be inspected afterwards (nothing here reads them)
+            for (int i = gi; i < T * args.k; i += kGroupThreads) {
+                const int t = i / args.k, j = i - t * args.k;
+                args.ids_out[i] = ids_s[t * kMaxTopK + j];
+                args.w_out[i] = w_s[t * kMaxTopK + j];
+            }
+            for (int a = gi; a < A; a += kGroupThreads) args.active_out[a] = slot_expert_of(a);
+            if (leader) args.meta_out[kMetaActive] = A;
+        }
         // CTA ranges: space 0 closed form (first G0 CTAs); space 1 so that spaces 0 + 1 are even
         // over all CTAs (a prefix maximum keeps the starts non-decreasing); space 2 even
         {
@@ -852,13 +863,9 @@ template <int BN>
 cudaError_t launch_bn(const Maps& maps, const FusedArgs& a, int grid, cudaStream_t s) {
     using C = FCfg<BN>;
     static_assert(C::SMEM <= kSmemMax, "shared memory budget");
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<BN>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(fused_decode_kernel<BN>), C::SMEM, &attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(fused_decode_kernel<BN>, dim3(grid), dim3(kThreads), C::SMEM, s, maps, a);
 }
 

@@ -373,14 +373,10 @@ EncodeTiledFn encoder() {
 
 template <int kMode, bool kContig>
 cudaError_t launch_one(const TcMaps& maps, const TcArgs& a, int grid, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kMode, kContig>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes<kMode>());
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(tc_gemm_kernel<kMode, kContig>),
+                                     smem_bytes<kMode>(), &attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(tc_gemm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads), smem_bytes<kMode>(),
                       s, maps, a);
 }

@@ -536,14 +536,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 template <int kMode, bool kContig>
 cudaError_t launch2(const Tc2Maps& maps, const Tc2Args& a, int grid, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm2sm_kernel<kMode, kContig>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes<kMode>());
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(tc_gemm2sm_kernel<kMode, kContig>),
+                                     smem_bytes<kMode>(), &attr);
+    if (e != cudaSuccess) return e;
     return launch_pdl(tc_gemm2sm_kernel<kMode, kContig>, dim3(grid), dim3(kThreads),
                       smem_bytes<kMode>(), s, maps, a);
 }

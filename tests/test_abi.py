@@ -75,3 +75,34 @@ def test_host_validation_statuses(lib):
     assert lib.pmoe_plan_destroy(None) == _lib.OK
     assert lib.pmoe_status_string(_lib.ERR_PAGE_OOB) == b"page index out of range"
     assert b"k" in lib.pmoe_last_error() or lib.pmoe_last_error() != b""
+
+
+def test_noalloc_refuses_bad_arguments_before_any_device_work(lib):
+    """The allocation-free forward checks its arguments on the host first: these calls pass
+    made-up device addresses and must return before touching a GPU."""
+    fn = lib.moe_paged_forward_noalloc
+    A = ctypes.c_void_p(0x100000)   # 16-byte aligned stand-ins, never dereferenced
+
+    def call(desc, T=4, buf0=A, buf1=A, err=A, top_k=None):
+        k = desc.top_k if top_k is None else top_k
+        return fn(ctypes.byref(desc), A, 32, buf0, buf1, A, T, A, k, A, A, A, err, None)
+
+    tiny = pm.make_desc(256, 128, 8, 2, True, 0, 2)
+    assert call(pm.make_desc(256, 128, 8, 9, True, 0, 2)) == _lib.ERR_INVALID_ARG       # k > E
+    assert call(pm.make_desc(100, 128, 8, 2, True, 0, 2)) == _lib.ERR_UNSUPPORTED       # d % 64
+    assert call(pm.make_desc(32768, 128, 8, 2, True, 0, 2)) == _lib.ERR_UNSUPPORTED     # d too large
+    assert call(tiny, buf0=ctypes.c_void_p(0x100008)) == _lib.ERR_INVALID_ARG           # misaligned buffer
+    assert b"aligned" in lib.pmoe_last_error()
+    assert call(tiny, buf1=ctypes.c_void_p(0x100004)) == _lib.ERR_INVALID_ARG
+    assert call(tiny, err=None) == _lib.ERR_INVALID_ARG                                 # no error word
+    assert b"device_error" in lib.pmoe_last_error()
+    assert call(tiny, top_k=1) == _lib.ERR_INVALID_ARG
+    q15 = pm.make_desc(2048, 1408, 60, 4, False, 4, 15)
+    assert call(q15, T=512) == _lib.ERR_WORKSPACE                                       # beyond the scratch
+    assert b"scratch" in lib.pmoe_last_error()
+    assert call(tiny, T=0) == _lib.OK                                                   # nothing to do
+
+
+def test_routing_view_needs_a_forward_call(lib):
+    v = _lib.RoutingView()
+    assert lib.pmoe_plan_routing_view(None, 1, ctypes.byref(v)) == _lib.ERR_INVALID_ARG
