@@ -1,14 +1,16 @@
 """Benchmark of the paged fused-MoE layer forward on GB300.
 
-One step = one forward of the Qwen1.5-MoE-shaped layer (d=2048, f=1408, 60 routed experts top-4,
-shared expert 4*1408; 45 experts in random pool pages, 15 in a load buffer) over a batch of
-T=4096 synthetic tokens, with weights, tables and activations resident in HBM.  The JSON line
-reports TFLOP/s (algorithmic: 6*T*d*(k*f + S*f)), the same through host buffers (e2e), the
-dominant kernel against its roofline, the paged-vs-contiguous overhead and a token-count sweep,
-and the CPU oracle's throughput on a bounded sample of the same workload.
+One step = one forward of the Mixtral-8x7B-shaped layer (d=4096, f=14336, 8 experts top-2; 6
+experts in random pool pages, 2 in a load buffer; logits with +1.0 on two hot experts) over a
+batch of T=8192 synthetic tokens, the largest workload of the set, with weights, tables and
+activations resident in HBM.  The JSON line reports TFLOP/s (algorithmic: 6*T*d*(k*f + S*f)),
+the same through host buffers (e2e), the dominant kernel against its roofline (the burst bf16
+peak unless the timed region lasts 2 s or more), the paged-vs-contiguous overhead, token-count
+sweeps, the CPU oracle's throughput on a bounded sample of the same workload, and the
+Qwen1.5-MoE- and Qwen3-Next-shaped layers at 4096 tokens with their sweeps as extra keys.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--config qwen15] [--tokens 4096] [--no-sweep] [--no-cpu]
+                    [--config mixtral] [--tokens 8192] [--no-sweep] [--no-cpu] [--no-extra]
 
 Under torchrun every rank runs its own replica (the path has no collective); rank 0 prints.
 """
@@ -302,7 +304,10 @@ def decode_sweep(args):
     """24 consecutive Qwen1.5-MoE-shaped layers per step, batch 1..256 tokens, resident fraction
     100% -> 50%: offloaded experts stream from pinned host memory into the two alternating load
     buffers one layer ahead of compute; the pool layout cycles over 4 pre-placed layouts per step.
-    One JSON line per (resident fraction, tokens)."""
+    With --predicted the prefetch follows a prediction (each layer's routing in the previous step)
+    instead of the actual routing, and each layer first copies in the routed experts the
+    prediction missed (pmoe_copy_in_missing), timed as its stall.  One JSON line per (resident
+    fraction, tokens)."""
     from paged_moe_expert_gb300 import pipeline
     import paged_moe_expert_gb300 as pm
     torch.cuda.set_device(0)
@@ -324,6 +329,8 @@ def decode_sweep(args):
     torch.cuda.synchronize()
     h2d_gbs = 3 * (1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9
     del hbuf, dbuf
+    if args.predicted and args.backend != "host":
+        raise SystemExit("--predicted copies missed experts from pinned host memory: use --backend host")
     resident_ms = {}
     for frac in fractions:
         n_off = int(round((1.0 - frac) * cfg.E))
@@ -334,23 +341,45 @@ def decode_sweep(args):
             logits = [[syn.bf16_bits_to_f32(syn.to_bf16_bits(
                 rng.standard_normal((T, cfg.E)).astype(np.float32))) for _ in range(L)]
                 for _ in range(steps)]
-            scheds = [stack.schedule(lg) for lg in logits]
+            n_missed = 0
+            if args.predicted:
+                # prediction for step s = each layer's routing in step s - 1 (a step before the first)
+                before = [syn.bf16_bits_to_f32(syn.to_bf16_bits(
+                    rng.standard_normal((T, cfg.E)).astype(np.float32))) for _ in range(L)]
+                preds = [[pipeline.routed_experts((logits[s_ - 1] if s_ else before)[l], cfg.k)
+                          for l in range(L)] for s_ in range(steps)]
+                scheds = [stack.schedule_predicted(p_) for p_ in preds]
+                n_missed = sum(len(np.setdiff1d(np.intersect1d(pipeline.routed_experts(logits[s_][l], cfg.k),
+                                                               stack.offloaded[l]), preds[s_][l]))
+                               for s_ in range(args.warmup, steps) for l in range(L))
+            else:
+                scheds = [stack.schedule(lg) for lg in logits]
             lg_dev = [[torch.from_numpy(x).cuda() for x in lg] for lg in logits]
+            stall = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(L)] for _ in range(args.steps)] if args.predicted else None
             hidden = torch.from_numpy(syn.to_bf16_bits(rng.standard_normal((T, cfg.d)).astype(
                 np.float32)).view(np.int16)).view(torch.bfloat16).cuda()
             ws = pm.alloc_workspace(stack.desc, T)
             acts = [torch.empty_like(hidden) for _ in range(2)]
-            copied = sum(len(sc[0]) for sched in scheds[args.warmup:] for sc in sched) * 6 * cfg.d * cfg.f
+            n_pref = sum(len(sc[0]) for sched in scheds[args.warmup:] for sc in sched)
+            copied = (n_pref + n_missed) * 6 * cfg.d * cfg.f
             for s_ in range(args.warmup):
-                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws)
+                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws, copy_in=args.predicted)
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             for s_ in range(args.warmup, steps):
-                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws)
+                stack.step(hidden, lg_dev[s_], scheds[s_], s_, acts, ws, copy_in=args.predicted,
+                           stall_events=stall[s_ - args.warmup] if stall else None)
             e1.record()
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / args.steps
+            for row in stack.plans:
+                for p_ in row:
+                    if p_.device_error() != 0:
+                        raise RuntimeError("device error word set in the decode sweep")
+            stall_ms = (sum(a_.elapsed_time(b_) for st in stall for a_, b_ in st) / args.steps
+                        if stall else None)
             if n_off == 0:
                 resident_ms[T] = ms
             copy_ms = copied / args.steps / (h2d_gbs * 1e9) * 1e3 if args.backend == "host" else 0.0
@@ -364,6 +393,11 @@ def decode_sweep(args):
                     "copied_mb_per_step": copied / args.steps / 1e6,
                     "h2d_gbs": h2d_gbs, "copy_ms_per_step_est": copy_ms,
                     "all_resident_ms": resident_ms.get(T),
+                    "prefetch": ("previous step's routing (copy-in of misses)" if args.predicted
+                                 else "actual routing"),
+                    "experts_prefetched_per_step": n_pref / args.steps,
+                    "experts_copied_in_per_step": n_missed / args.steps,
+                    "copy_in_ms_per_step": stall_ms,
                     "exposed_copy_frac": (None if T not in resident_ms or copy_ms == 0 else
                                           max(0.0, (ms - resident_ms[T])) / copy_ms)}
             print(json.dumps(line), flush=True)
@@ -656,17 +690,227 @@ def elastic_sweep(args):
         print(json.dumps(line), flush=True)
 
 
+PATH_IDS = {"auto": 0, "stream": 1, "tc": 2, "tc_decode": 3, "tc2": 4, "fused": 5}
+# a timed region at least this long runs at the power-capped (sustained) clocks; shorter ones are
+# compared with the burst peak
+SUSTAINED_REGION_S = 2.0
+
+
+def kernel_names(nk, path):
+    if nk == 6:
+        return ["route", "align", "gather", "gemm1", "gemm2", "combine"]
+    if nk == 5:
+        return (["prep", "gather"] if tc_family_path(path) else ["route", "align"]) + ["gemm1", "gemm2", "combine"]
+    if nk == 1:
+        return ["fused"]   # routing, both projections and the combine in one kernel
+    return ["prep", "gemm1", "gemm2", "combine"]
+
+
+def dominant_roofline(kwork, ksec, path, peaks, region_s):
+    """The dominant kernel against the roof that binds it.  Tensor-bound kernels take the burst
+    bf16 peak unless the timed region is long enough to run at sustained (power-capped) clocks."""
+    sustained = region_s >= SUSTAINED_REGION_S
+    tc_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    tc_family = tc_family_path(path)
+    if tc_family and kwork["flops"] / (tc_peak * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "tensor", "achieved": kwork["flops"] / ksec / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "peak_kind": "sustained" if sustained else "burst"}
+    elif not tc_family and kwork["flops"] / 80e12 > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
+        # CUDA-core fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock
+        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": kwork["flops"] / ksec / 1e12, "peak": alu_peak,
+                "unit": "TFLOP/s", "peak_kind": "fp32 FMA at max SM clock"}
+    else:
+        roof = {"bound": "hbm", "achieved": kwork["bytes"] / ksec / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_kind": "copy"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    return roof
+
+
+def workload_name(cfg, T):
+    return ("%s layer forward (d=%d f=%d E=%d top-%d shared %d), T=%d tokens, "
+            "%d pool-resident / %d buffered experts"
+            % (cfg.name, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S * cfg.f, T, cfg.E - cfg.n_buffered,
+               cfg.n_buffered))
+
+
+def measure(lay, cfg_key, T, path_name, steps, warmup, device, dist, world, peaks, e2e=True):
+    """One workload: K timed steps back to back (max over ranks), the dominant kernel bracketed
+    by events in a second pass of K steps, and optionally K end-to-end steps with host copies."""
+    pm, cfg = lay.pm, lay.cfg
+    lay.plan.set_path(PATH_IDS[path_name])
+    if lay.cplan is not None:
+        lay.cplan.set_path(PATH_IDS[path_name])
+    h_np, lg_np, hidden, logits = lay.tokens(T)
+    e_act = lay.e_act(logits)
+    wk = work(cfg, T, e_act)
+    ws = pm.alloc_workspace(lay.desc, T, device)
+    out = torch.empty_like(hidden)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lay.plan.forward(hidden, logits, lay.page_table, lay.buf_slot, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    path, nk, n_launch = lay.plan.last_run()
+    assert lay.plan.device_error() == 0
+
+    # which kernel dominates: one untimed pass with an event before every kernel
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+    lay.plan.set_profile_events(probe)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    lay.plan.set_profile_events(None)
+    probe_ms = [probe[j].elapsed_time(probe[j + 1]) for j in range(nk)]
+    dom = int(np.argmax(probe_ms))
+
+    # timed region: K steps back to back, with the dominant kernel bracketed by events on the
+    # launching stream in every step (an event between two kernels keeps the second from starting
+    # before the first ends, which costs the programmatic overlap at those two boundaries only)
+    prof = []
+    for _ in range(steps):
+        evs = [None] * (nk + 1)
+        evs[dom] = torch.cuda.Event(enable_timing=True)
+        evs[dom + 1] = torch.cuda.Event(enable_timing=True)
+        evs[dom].record(stream)        # created now, not inside the timed region
+        evs[dom + 1].record(stream)
+        prof.append(evs)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        lay.plan.set_profile_events(prof[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    lay.plan.set_profile_events(None)
+    if dist:
+        dist.barrier()
+    region_s = t_start.elapsed_time(t_end) * 1e-3
+    sec = max_over_ranks(region_s / steps, dist, device)
+    dom_sec = float(np.mean([prof[i][dom].elapsed_time(prof[i][dom + 1]) for i in range(steps)])) * 1e-3
+    assert lay.plan.device_error() == 0
+
+    names = kernel_names(nk, path)
+    kname = names[dom]
+    wk["fused"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
+    roof = dominant_roofline(wk.get(kname, {"flops": 0.0, "bytes": 0.0}), dom_sec, path, peaks, region_s)
+    roof["traffic"] = measured_traffic(cfg_key, T, PATH_NAMES[path], kname)
+    roof["kernel"] = kname
+    roof["kernel_ms"] = dom_sec * 1e3
+    roof["peak_source"] = peaks["source"]
+    res = {"cfg": cfg, "T": T, "path": path, "sec": sec, "region_s": region_s, "wk": wk,
+           "e_act": e_act, "roofline": roof, "kernels_ms": {n: float(t) for n, t in zip(names, probe_ms)},
+           "gpu_launches": int(n_launch * steps), "h_np": h_np, "lg_np": lg_np,
+           "h2d": int(hidden.numel() * 2 + logits.numel() * 4), "d2h": int(out.numel() * 2)}
+    if not e2e:
+        return res
+
+    # e2e: every step copies its inputs from pinned host memory and its result back, inside the
+    # timed region.  Device buffers are double-buffered so step i+1's host->device copy and step
+    # i-1's device->host copy (on their own streams) overlap step i's forward, ordered by events.
+    h_host = hidden.cpu().pin_memory()
+    l_host = logits.cpu().pin_memory()
+    o_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    hid_d = [hidden, torch.empty_like(hidden)]
+    lg_d = [logits, torch.empty_like(logits)]
+    out_d = [out, torch.empty_like(out)]
+    cp_in, cp_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    read_done = [torch.cuda.Event() for _ in range(2)]   # the forward of this slot finished
+    out_done = [torch.cuda.Event() for _ in range(2)]    # the result of this slot is on the host
+    for b in range(2):
+        read_done[b].record(stream)
+        out_done[b].record(stream)
+
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(cp_in):
+            cp_in.wait_event(read_done[b])           # the slot's previous forward has read it
+            hid_d[b].copy_(h_host, non_blocking=True)
+            lg_d[b].copy_(l_host, non_blocking=True)
+            in_ready[b].record(cp_in)
+        stream.wait_event(in_ready[b])
+        stream.wait_event(out_done[b])               # the slot's previous result has left
+        lay.plan.forward(hid_d[b], lg_d[b], lay.page_table, lay.buf_slot, out=out_d[b], workspace=ws)
+        read_done[b].record(stream)
+        with torch.cuda.stream(cp_out):
+            cp_out.wait_event(read_done[b])
+            o_host[b].copy_(out_d[b], non_blocking=True)
+            out_done[b].record(cp_out)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cp_in.wait_event(e0)
+    for i in range(steps):
+        e2e_step(i)
+    stream.wait_event(out_done[(steps - 1) % 2])   # the last result is on the host
+    e1.record(stream)
+    torch.cuda.synchronize()
+    res["e2e_sec"] = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / steps, dist, device)
+    return res
+
+
+def token_sweep(lay, iters, peaks, device):
+    """Every token count of the workload: paged and contiguous forward replayed from CUDA graphs,
+    interleaved, L2 flushed before every timed call (short bursts: the burst bf16 peak)."""
+    pm, cfg = lay.pm, lay.cfg
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    sweep = []
+    lay.plan.set_path(pm.PATH_AUTO)
+    lay.cplan.set_path(pm.PATH_AUTO)
+    for Ts in cfg.tokens:
+        _, _, hs, ls = lay.tokens(Ts)
+        wss = pm.alloc_workspace(lay.desc, Ts, device)
+        os_ = torch.empty_like(hs)
+        fp = lambda: lay.plan.forward(hs, ls, lay.page_table, lay.buf_slot, out=os_, workspace=wss)  # noqa: E731
+        fc = lambda: lay.cplan.contig_forward(hs, ls, out=os_, workspace=wss)  # noqa: E731
+        for _ in range(3):
+            fp(); fc()
+        ps = lay.plan.last_run()[0]
+        gp, gc = capture(fp), capture(fc)
+        tp, tc = time_iters([gp.replay, gc.replay], iters, flush)
+        # a timing is only a timing if no kernel reported an error (a bounded wait that ran
+        # out would otherwise show up as a slow point)
+        for pl_ in (lay.plan, lay.cplan):
+            if pl_.device_error() != 0:
+                raise RuntimeError("device error word set during the %d-token sweep point" % Ts)
+        ea = lay.e_act(ls)
+        wk_s = work(cfg, Ts, ea)
+        frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks, sustained=False)
+        sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "launch": "cuda_graph", "ms": tp * 1e3,
+                      "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
+                      "tflops": wk_s["flops"] / tp / 1e12,
+                      "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
+                      "tokens_per_s": Ts / tp, "experts_active": ea,
+                      "binding_roof": bound, "roof_frac": frac})
+        del wss, gp, gc
+    return sweep
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="qwen15", choices=sorted(syn.CONFIGS))
+    ap.add_argument("--config", default="mixtral", choices=sorted(syn.CONFIGS))
     ap.add_argument("--tokens", type=int, default=0)
-    ap.add_argument("--path", default="auto", choices=["auto", "stream", "tc", "tc_decode", "tc2", "fused"])
+    ap.add_argument("--path", default="auto", choices=sorted(PATH_IDS))
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other layer shapes (headline workload only)")
     ap.add_argument("--sweep-iters", type=int, default=50)
     ap.add_argument("--decode-sweep", action="store_true",
                     help="24-layer decode sweep with prefetch (prints one line per case)")
@@ -675,6 +919,9 @@ def main():
     ap.add_argument("--fractions", default="1.0,0.875,0.75,0.625,0.5")
     ap.add_argument("--backend", default="host", choices=["host", "compressed"],
                     help="decode sweep: where offloaded experts live")
+    ap.add_argument("--predicted", action="store_true",
+                    help="decode sweep: prefetch from the previous step's routing and copy in "
+                         "the experts it missed")
     ap.add_argument("--codec", action="store_true",
                     help="exponent-only Huffman decode of expert pages vs the host copy")
     ap.add_argument("--vmm-overhead", action="store_true",
@@ -719,219 +966,76 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
 
-    import paged_moe_expert_gb300 as pm
     peaks = load_peaks()
     cfg = syn.CONFIGS[args.config]
     T = args.tokens or cfg.tokens[-1]
     lay = Layer(cfg, device, contiguous=not args.no_sweep)
-    if args.path != "auto":
-        p = {"stream": pm.PATH_STREAM, "tc": pm.PATH_TC, "tc_decode": pm.PATH_TC_DECODE, "tc2": pm.PATH_TC2,
-             "fused": pm.PATH_FUSED}[args.path]
-        lay.plan.set_path(p)
-        if lay.cplan is not None:
-            lay.cplan.set_path(p)
-    h_np, lg_np, hidden, logits = lay.tokens(T)
-    e_act = lay.e_act(logits)
-    wk = work(cfg, T, e_act)
-    ws = pm.alloc_workspace(lay.desc, T, device)
-    out = torch.empty_like(hidden)
-    stream = torch.cuda.current_stream()
 
-    def step():
-        lay.plan.forward(hidden, logits, lay.page_table, lay.buf_slot, out=out, workspace=ws)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    path, nk, n_launch = lay.plan.last_run()
-    assert lay.plan.device_error() == 0
-
-    # which kernel dominates: one untimed pass with an event before every kernel
-    probe = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-    lay.plan.set_profile_events(probe)
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    lay.plan.set_profile_events(None)
-    probe_ms = [probe[j].elapsed_time(probe[j + 1]) for j in range(nk)]
-    dom = int(np.argmax(probe_ms))
-
-    # timed region: K steps back to back (events for the dominant kernel are made here and used
-    # in a second pass below)
-    prof = []
-    for _ in range(args.steps):
-        evs = [None] * (nk + 1)
-        evs[dom] = torch.cuda.Event(enable_timing=True)
-        evs[dom + 1] = torch.cuda.Event(enable_timing=True)
-        prof.append(evs)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    sec = max_over_ranks(t_start.elapsed_time(t_end) * 1e-3 / args.steps, dist, device)
-    # the same K steps again with the dominant kernel bracketed by events on the launching stream
-    # (an event between two kernels keeps the second from starting early, so these steps are not
-    # the ones `value` is taken from)
-    for i in range(args.steps):
-        lay.plan.set_profile_events(prof[i])
-        step()
-    torch.cuda.synchronize()
-    lay.plan.set_profile_events(None)
-    dom_sec = float(np.mean([prof[i][dom].elapsed_time(prof[i][dom + 1]) for i in range(args.steps)])) * 1e-3
-
-    # e2e: every step copies its inputs from pinned host memory and its result back, inside the
-    # timed region.  Device buffers are double-buffered so step i+1's host->device copy and step
-    # i-1's device->host copy (on their own streams) overlap step i's forward, ordered by events.
-    h_host = hidden.cpu().pin_memory()
-    l_host = logits.cpu().pin_memory()
-    o_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-    hid_d = [hidden, torch.empty_like(hidden)]
-    lg_d = [logits, torch.empty_like(logits)]
-    out_d = [out, torch.empty_like(out)]
-    cp_in, cp_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    read_done = [torch.cuda.Event() for _ in range(2)]   # the forward of this slot finished
-    out_done = [torch.cuda.Event() for _ in range(2)]    # the result of this slot is on the host
-    for b in range(2):
-        read_done[b].record(stream)
-        out_done[b].record(stream)
-
-    def e2e_step(i):
-        b = i % 2
-        with torch.cuda.stream(cp_in):
-            cp_in.wait_event(read_done[b])           # the slot's previous forward has read it
-            hid_d[b].copy_(h_host, non_blocking=True)
-            lg_d[b].copy_(l_host, non_blocking=True)
-            in_ready[b].record(cp_in)
-        stream.wait_event(in_ready[b])
-        stream.wait_event(out_done[b])               # the slot's previous result has left
-        lay.plan.forward(hid_d[b], lg_d[b], lay.page_table, lay.buf_slot, out=out_d[b], workspace=ws)
-        read_done[b].record(stream)
-        with torch.cuda.stream(cp_out):
-            cp_out.wait_event(read_done[b])
-            o_host[b].copy_(out_d[b], non_blocking=True)
-            out_done[b].record(cp_out)
-
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    cp_in.wait_event(e0)
-    for i in range(args.steps):
-        e2e_step(i)
-    stream.wait_event(out_done[(args.steps - 1) % 2])   # the last result is on the host
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_sec = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / args.steps, dist, device)
-
-    # token-count sweep with the contiguous twin (L2 flushed before every timed call)
-    sweep = []
+    r = measure(lay, args.config, T, args.path, args.steps, args.warmup, device, dist, world, peaks)
+    sweeps = {}
     if not args.no_sweep and rank == 0:
-        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
-        for Ts in cfg.tokens:
-            _, _, hs, ls = lay.tokens(Ts)
-            wss = pm.alloc_workspace(lay.desc, Ts, device)
-            os_ = torch.empty_like(hs)
-            fp = lambda: lay.plan.forward(hs, ls, lay.page_table, lay.buf_slot, out=os_, workspace=wss)  # noqa: E731
-            fc = lambda: lay.cplan.contig_forward(hs, ls, out=os_, workspace=wss)  # noqa: E731
-            for _ in range(3):
-                fp(); fc()
-            ps = lay.plan.last_run()[0]
-            gp, gc = capture(fp), capture(fc)
-            tp, tc = time_iters([gp.replay, gc.replay], args.sweep_iters, flush)
-            # a timing is only a timing if no kernel reported an error (a bounded wait that ran
-            # out would otherwise show up as a slow point)
-            for pl_ in (lay.plan, lay.cplan):
-                if pl_.device_error() != 0:
-                    raise RuntimeError("device error word set during the %d-token sweep point" % Ts)
-            ea = lay.e_act(ls)
-            wk_s = work(cfg, Ts, ea)
-            frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks)
-            sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "launch": "cuda_graph", "ms": tp * 1e3,
-                          "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
-                          "tflops": wk_s["flops"] / tp / 1e12,
-                          "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
-                          "tokens_per_s": Ts / tp, "experts_active": ea,
-                          "binding_roof": bound, "roof_frac": frac})
-            del wss
+        sweeps[args.config] = token_sweep(lay, args.sweep_iters, peaks, device)
     clk = clocks.stop()
-
-    # dominant kernel against its roofline
-    if nk == 6:
-        names = ["route", "align", "gather", "gemm1", "gemm2", "combine"]
-    elif nk == 5:
-        names = (["prep", "gather"] if tc_family_path(path) else ["route", "align"]) + ["gemm1", "gemm2", "combine"]
-    elif nk == 1:
-        names = ["fused"]   # routing, both projections and the combine in one kernel
-    else:
-        names = ["prep", "gemm1", "gemm2", "combine"]
-    kname = names[dom]
-    wk["fused"] = {"flops": wk["flops"], "bytes": wk["bytes"]}
-    kwork = wk.get(kname, {"flops": 0.0, "bytes": 0.0})
-    ksec = dom_sec
-    tc_family = path in (pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED)
-    if tc_family and kwork["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
-        roof = {"bound": "tensor", "achieved": kwork["flops"] / ksec / 1e12,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
-    elif not tc_family and kwork["flops"] / 80e12 > kwork["bytes"] / (peaks["hbm_gbs"] * 1e9):
-        # CUDA-core fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock
-        alu_peak = 152 * 128 * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": kwork["flops"] / ksec / 1e12, "peak": alu_peak,
-                "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": kwork["bytes"] / ksec / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(args.config, T, PATH_NAMES[path], kname)
-    roof["kernel"] = kname
-    roof["peak_source"] = peaks["source"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = oracle_throughput(cfg, lay.w, h_np, lg_np, 15.0, T)
+        cpu = oracle_throughput(cfg, lay.w, r["h_np"], r["lg_np"], 15.0, T)
 
-    overhead = None
-    for s_ in sweep:
-        if s_["tokens"] == T:
-            overhead = s_["overhead_vs_contig"]
+    # the other layer shapes at their largest token count, and their token sweeps (rank 0 only)
+    extra = []
+    if not args.no_extra and rank == 0 and world == 1:
+        del lay
+        torch.cuda.empty_cache()
+        for key in ("qwen15", "qwen3next"):
+            if key == args.config:
+                continue
+            c2 = syn.CONFIGS[key]
+            lay2 = Layer(c2, device, contiguous=not args.no_sweep)
+            r2 = measure(lay2, key, c2.tokens[-1], "auto", args.steps, args.warmup, device, None, 1,
+                         peaks, e2e=False)
+            ov = None
+            if not args.no_sweep:
+                sweeps[key] = token_sweep(lay2, args.sweep_iters, peaks, device)
+                ov = next((p["overhead_vs_contig"] for p in sweeps[key] if p["tokens"] == c2.tokens[-1]), None)
+            extra.append({"workload": workload_name(c2, c2.tokens[-1]), "tokens": c2.tokens[-1],
+                          "path": PATH_NAMES[r2["path"]], "tflops": r2["wk"]["flops"] / r2["sec"] / 1e12,
+                          "ms_per_step": r2["sec"] * 1e3, "experts_active": r2["e_act"],
+                          "weight_gbs": r2["wk"]["weight_bytes"] / r2["sec"] / 1e9,
+                          "roofline": r2["roofline"], "kernels_ms": r2["kernels_ms"],
+                          "overhead_vs_contig": ov})
+            del lay2
+            torch.cuda.empty_cache()
+
+    sweep = sweeps.get(args.config, [])
+    overhead = next((s_["overhead_vs_contig"] for s_ in sweep if s_["tokens"] == T), None)
+    wk, sec = r["wk"], r["sec"]
     value = job_throughput(wk["flops"], world, sec) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s layer forward (d=%d f=%d E=%d top-%d shared %d), T=%d tokens, "
-                               "%d pool-resident / %d buffered experts"
-                               % (cfg.name, cfg.d, cfg.f, cfg.E, cfg.k, cfg.S * cfg.f, T,
-                                  cfg.E - cfg.n_buffered, cfg.n_buffered),
-                   "tokens": T, "path": PATH_NAMES[path], "experts_active": e_act,
+        "config": {"workload": workload_name(cfg, T),
+                   "tokens": T, "path": PATH_NAMES[r["path"]], "experts_active": r["e_act"],
                    "weight_gbs": job_throughput(wk["weight_bytes"], world, sec) / 1e9,
                    "tokens_per_s": job_throughput(T, world, sec),
-                   "l2": "inputs larger than L2 (%.0f MB of expert weights per step); sweep flushes L2"
+                   "l2": "inputs larger than L2 (%.0f MB of expert weights per step); sweeps flush L2"
                          % (wk["weight_bytes"] / 1e6),
+                   "timed_region_s": r["region_s"],
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roof,
+        "roofline": r["roofline"],
         "cpu_baseline": cpu and {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
-        "e2e": {"value": job_throughput(wk["flops"], world, e2e_sec) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": int(hidden.numel() * 2 + logits.numel() * 4),
-                "d2h_bytes_per_step": int(out.numel() * 2)},
-        "gpu_launches": int(n_launch * args.steps),
+        "e2e": {"value": job_throughput(wk["flops"], world, r["e2e_sec"]) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["gpu_launches"],
         "clocks": clk,
-        "kernels_ms": {n: float(t) for n, t in zip(names, probe_ms)},
+        "kernels_ms": r["kernels_ms"],
         "overhead_vs_contig": overhead,
         "sweep": sweep,
+        "extra_workloads": extra,
+        "sweeps_other": {k: v for k, v in sweeps.items() if k != args.config},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

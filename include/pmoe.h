@@ -25,7 +25,8 @@
  *   page_table int32 [E + S][3] (device): pages of W1, W3, W2 for each routed expert e < E and
  *              each shared-expert chunk E + s (s < S; always pool-resident).
  *   buf_slot   int32 [E] (device): -1 = pool-resident (use page_table[e]); otherwise
- *              b * slots_per_buffer + s = slot s of load buffer b (b in {0, 1}).
+ *              b * slots_per_buffer + s = slot s of load buffer b (b in {0, 1}); -2 = absent
+ *              (see pmoe_copy_in_missing; an error if a token routes to it).
  *   shared     the shared expert of intermediate size S*f is split into S chunks of width f;
  *              chunk s is the expert E + s with weight 1 on every token.
  *   ownership  the caller owns every buffer: pool, load buffers, tables, activations, outputs,
@@ -233,6 +234,39 @@ pmoe_status pmoe_prefetch_async(pmoe_plan_t plan, int32_t buf, int32_t n,
                                 const void* const* host_experts, const int32_t* slots,
                                 pmoe_stream_t copy_stream, pmoe_event_t buf_free,
                                 pmoe_event_t copy_done);
+
+/* Copy-in of routed experts that are not on the device (Rimuru, section "The pipeline: what
+ * happens in one scheduling round": the manager prefetches the experts it predicts a layer needs,
+ * the layer's actual routing decides, and an expert the routing picks that is neither cached nor
+ * prefetched is copied in before the layer computes).  buf_slot[e] == -2 marks routed expert e as
+ * absent: in neither the pool nor a load buffer (a forward call that routes a token to an absent
+ * expert sets PMOE_ERR_SLOT_OOB; absent experts no token routes to are never read).  On `stream`,
+ * for the T tokens of router_logits (fp32 [T][E], the same top-k rule as the forward): every
+ * absent expert some token routes to, in ascending id, takes the next free slot of load buffer
+ * `buf` in ascending order (a slot that no buf_slot entry points at), buf_slot[e] (device, updated
+ * in place) becomes buf * slots_per_buffer + slot, and its W1 | W3 | W2 are copied from
+ * host_experts[e] into the slot.  missed (device int32 [1 + 2E]) receives the count, the experts
+ * and their slots: missed[0] = n, missed[1..n] experts, missed[1+E .. 1+E+n) slots.
+ *   host_experts  DEVICE array [E] of device-readable pointers (pmoe_device_pointers turns
+ *                 pinned host pointers into them), each to 3*f*d bf16 (W1, W3, W2 back to back),
+ *                 16-byte aligned; NULL for an expert that has no copy.
+ * Run it right before the layer's forward call on the same stream: its kernels let no later
+ * kernel start early, so the forward sees the new table entries and the copied bytes.  Nothing
+ * else may write load buffer `buf` meanwhile (after a prefetch into it, order the copy-in after
+ * that prefetch's copy_done).  Errors in the error word: PMOE_ERR_SLOT_OOB when free slots run
+ * out (the experts left over stay absent), PMOE_ERR_INVALID_ARG for an absent routed expert
+ * whose host_experts entry is NULL.  Uses plan-owned words, so copy-in and forward calls of one
+ * plan must not overlap on the GPU.  T = 0 only sets missed[0] = 0. */
+pmoe_status pmoe_copy_in_missing(pmoe_plan_t plan, const float* router_logits, int32_t T,
+                                 int32_t* buf_slot, int32_t buf, const void* const* host_experts,
+                                 int32_t* missed, pmoe_stream_t stream);
+
+/* The device-side address of each host allocation host[i] (NULL stays NULL), for kernels that
+ * read host memory directly (pmoe_copy_in_missing), from cudaHostGetDevicePointer: pinned host
+ * memory, and on systems whose GPU reads pageable memory through the host's page tables
+ * (Grace-based GB300) pageable memory too.  PMOE_ERR_INVALID_ARG if the runtime gives no device
+ * address for one or it is not 16-byte aligned.  Host arrays of n entries. */
+pmoe_status pmoe_device_pointers(int32_t n, const void* const* host, void** device);
 
 /* Host-side wait on an event with a timeout (polls cudaEventQuery; never a device spin).
  * PMOE_OK when the event completed, PMOE_ERR_TIMEOUT after timeout_ms milliseconds. */

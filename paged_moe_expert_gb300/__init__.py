@@ -20,7 +20,7 @@ from ._lib import (PATH_AUTO, PATH_FUSED, PATH_STREAM, PATH_TC, PATH_TC2, PATH_T
                    PmoeError)
 
 __all__ = ["Adjuster", "LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
-           "prefetch_async", "fill_pages_async", "wait_event", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
+           "prefetch_async", "fill_pages_async", "wait_event", "copy_in_missing", "device_pointers", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
            "make_desc"]
 
 
@@ -233,6 +233,25 @@ def fill_pages_async(plan: Plan, host_experts, pages, copy_stream, after=None, c
     wait = _event(after) if (after is not None and after.cuda_event != 0) else None
     _lib.check(_lib.load().pmoe_fill_pages_async(plan._h, int(n), ptrs, pg, _stream(copy_stream),
                                                  wait, _event(copy_done, copy_stream)))
+
+
+def device_pointers(host_tensors) -> torch.Tensor:
+    """Device-readable addresses of pinned host tensors (None stays 0), as an int64 tensor on
+    the current device: the host_experts table of copy_in_missing."""
+    n = len(host_tensors)
+    src = (ctypes.c_void_p * max(n, 1))(*[(t.data_ptr() if t is not None else None) for t in host_tensors])
+    dst = (ctypes.c_void_p * max(n, 1))()
+    _lib.check(_lib.load().pmoe_device_pointers(int(n), src, dst))
+    return torch.tensor([int(p or 0) for p in dst[:n]], dtype=torch.int64, device="cuda")
+
+
+def copy_in_missing(plan: Plan, logits, buf_slot, buf: int, host_table, missed, stream=None):
+    """Bring the routed experts marked absent (buf_slot == -2) into free slots of load buffer
+    `buf` on `stream` (pmoe_copy_in_missing); buf_slot (device int32 [E]) is updated in place and
+    missed (device int32 [1 + 2E]) lists what was copied."""
+    _lib.check(_lib.load().pmoe_copy_in_missing(plan._h, _ptr(logits), int(logits.shape[0]),
+                                                _ptr(buf_slot), int(buf), _ptr(host_table),
+                                                _ptr(missed), _stream(stream)))
 
 
 def wait_event(event, timeout_ms: int) -> bool:

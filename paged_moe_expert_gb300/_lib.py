@@ -54,6 +54,8 @@ SIGNATURES = {
     "pmoe_prefetch_async": (ctypes.c_int, [P, I32, I32, ctypes.POINTER(P), ctypes.POINTER(I32), P, P, P]),
     "pmoe_fill_pages_async": (ctypes.c_int, [P, I32, ctypes.POINTER(P), P, P, P, P]),
     "pmoe_wait_event": (ctypes.c_int, [P, I32]),
+    "pmoe_copy_in_missing": (ctypes.c_int, [P, P, I32, P, I32, P, P, P]),
+    "pmoe_device_pointers": (ctypes.c_int, [I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
     "pmoe_get_device_error": (ctypes.c_int, [P, I32, ctypes.POINTER(I32), P]),
     "pmoe_route": (ctypes.c_int, [P, I32, I32, I32, I32, P, P, P]),
     "pmoe_align": (ctypes.c_int, [P, I32, I32, I32, I32, I32, P, P, P, P, P, P]),

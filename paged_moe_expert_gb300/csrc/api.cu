@@ -160,6 +160,7 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
     W.part = o;   o = align256(o + align_part_bytes());
     W.units = o;  o = align256(o + sizeof(int4) * W.nblk_max);
     W.unit_w2 = o; o = align256(o + sizeof(int32_t) * W.nblk_max);
+    W.ugroup = o; o = align256(o + sizeof(int2) * W.nblk_max);
     W.brows = o;  o = align256(o + sizeof(int32_t) * W.nblk_max);
     W.x = o;      o = align256(o + 2 * (size_t)cap_tc * D.d);
     W.h = o;      o = align256(o + 2 * (size_t)W.cap * D.f);
@@ -331,6 +332,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (path == PMOE_PATH_TC2) {
         rs.units = units;
         rs.unit_w2 = unit_w2;
+        rs.unit_group = at<int2>(ws, W.ugroup);
     }
     int32_t* brows = at<int32_t>(ws, W.brows);
     if (path == PMOE_PATH_TC) rs.block_rows = brows;
@@ -397,13 +399,14 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         if (!encode_rows_map(&x64, x, cap_tc, D.d, 64) || !encode_rows_map(&h64, h, cap_tc, D.f, 64) ||
             (sh.direct && !encode_rows_map(&hid64, hidden, T, D.d, 64)))
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+        const int2* ugroup = at<int2>(ws, W.ugroup);
         PMOE_CUDA(launch_tc_gemm2sm(1, contig, xmap, x64, P->tm_rows_d, P->tm_rows_d64, units, unit_w2,
-                                    meta, h, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error,
+                                    ugroup, meta, h, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error,
                                     stream, hidp, sh.direct ? &hid64 : nullptr, sh, shared_units),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_gemm2sm(2, contig, hmap, h64, P->tm_rows_f, P->tm_rows_f, units, unit_w2,
-                                    meta, y, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error, stream,
+                                    ugroup, meta, y, cap_tc, D.f, D.d, nblk, P->num_sms, P->d_error, stream,
                                     nullptr, nullptr, SharedRows{}, shared_units), "down gemm");
         ystride = cap_tc;
         splits = 1;
@@ -670,6 +673,47 @@ pmoe_status pmoe_fill_pages_async(pmoe_plan_t plan, int32_t n, const void* const
                                       page_bytes, cudaMemcpyHostToDevice, cs),
                       "fill page copy");
     if (copy_done) PMOE_CUDA(cudaEventRecord((cudaEvent_t)copy_done, cs), "record copy_done");
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_copy_in_missing(pmoe_plan_t plan, const float* router_logits, int32_t T,
+                                 int32_t* buf_slot, int32_t buf, const void* const* host_experts,
+                                 int32_t* missed, pmoe_stream_t stream) {
+    Plan* P = reinterpret_cast<Plan*>(plan);
+    if (!P) return fail(PMOE_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 0) return fail(PMOE_ERR_INVALID_ARG, "T < 0");
+    if (!buf_slot || !host_experts || !missed || (T > 0 && !router_logits))
+        return fail(PMOE_ERR_INVALID_ARG, "NULL pointer");
+    if (buf != 0 && buf != 1) return fail(PMOE_ERR_INVALID_ARG, "buf must be 0 or 1");
+    if (!P->buf[buf] || P->desc.slots_per_buffer <= 0)
+        return fail(PMOE_ERR_INVALID_ARG, "plan has no such load buffer");
+    if (P->desc.slots_per_buffer > 65536) return fail(PMOE_ERR_UNSUPPORTED, "more than 65536 slots per buffer");
+    if ((int64_t)T * P->desc.top_k > (int64_t)1 << 30) return fail(PMOE_ERR_INVALID_ARG, "too many tokens");
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        PMOE_CUDA(cudaMemsetAsync(missed, 0, sizeof(int32_t), s), "copy-in count");
+        return PMOE_OK;
+    }
+    PMOE_CUDA(launch_copy_in(*P, router_logits, T, buf_slot, buf, host_experts, missed, s), "copy-in");
+    return PMOE_OK;
+}
+
+pmoe_status pmoe_device_pointers(int32_t n, const void* const* host, void** device) {
+    if (n < 0 || (n > 0 && (!host || !device))) return fail(PMOE_ERR_INVALID_ARG, "bad arguments");
+    for (int i = 0; i < n; ++i) {
+        if (!host[i]) {
+            device[i] = nullptr;
+            continue;
+        }
+        void* d = nullptr;
+        const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host[i]), 0);
+        if (e != cudaSuccess) {
+            cudaGetLastError();   // not a sticky error: clear it
+            return fail(PMOE_ERR_INVALID_ARG, "a pointer has no device address (not pinned host memory)");
+        }
+        if ((uintptr_t)d & 15) return fail(PMOE_ERR_INVALID_ARG, "a pointer is not 16-byte aligned");
+        device[i] = d;
+    }
     return PMOE_OK;
 }
 

@@ -31,7 +31,7 @@ struct ExpertLoc {
 
 // Byte offsets of the workspace regions for one call (all 256-byte aligned).
 struct WsLayout {
-    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, brows, x, h, y, total;
+    size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, ugroup, brows, x, h, y, total;
     size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
@@ -172,6 +172,9 @@ struct ResolveArgs {
     // count in meta[kMetaPairs], single-block units in meta[kMetaSingles]
     int4* units;
     int32_t* unit_w2;
+    // optional with units: for each unit, {first unit, number of units} of its expert (an
+    // expert's units are consecutive), so a GEMM can order its tiles by expert
+    int2* unit_group;
     // optional (NULL: not written): valid rows of each sorted block, 1..block_m (the last block of
     // an expert holds its remainder, the others are full)
     int32_t* block_rows;
@@ -262,8 +265,9 @@ cudaError_t launch_tc_gemm(int mode, bool contig, const CUtensorMap& act, const 
 // order).
 cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, const CUtensorMap& act64,
                               const CUtensorMap* wmaps, const CUtensorMap* wmaps64,
-                              const int4* units, const int32_t* unit_w2, const int32_t* meta,
-                              void* out, int64_t out_rows, int f, int d, int64_t units_max,
+                              const int4* units, const int32_t* unit_w2, const int2* unit_group,
+                              const int32_t* meta, void* out, int64_t out_rows, int f, int d,
+                              int64_t units_max,
                               int num_sms, int32_t* err, cudaStream_t s,
                               const CUtensorMap* hid = nullptr, const CUtensorMap* hid64 = nullptr,
                               SharedRows sh = SharedRows{}, int shared_units = 0);
@@ -299,6 +303,14 @@ struct FusedArgs {
 cudaError_t launch_fused_decode(const CUtensorMap& xmap, const CUtensorMap& hmap,
                                 const CUtensorMap* w64, const CUtensorMap* wf, const FusedArgs& a,
                                 int bn, int grid, cudaStream_t s);
+
+// Copy-in of absent routed experts (copy_in.cu): routes the T tokens, gives every routed expert
+// with buf_slot == -2 a free slot of load buffer `buf` (buf_slot updated on the device), lists
+// them in missed ([0] count, [1..] experts, [1+E..] slots) and copies each from
+// host_experts[e] (device-readable, 3*f*d bf16) into its slot.  Uses the plan's words at bytes
+// 256..388 (routed-expert bitmap and an arrival counter), which it leaves zeroed.
+cudaError_t launch_copy_in(const Plan& P, const float* logits, int T, int32_t* buf_slot, int buf,
+                           const void* const* host_experts, int32_t* missed, cudaStream_t s);
 
 // Small-batch tensor-core path (tc_decode.cu): mode 1 gate/up -> h, mode 2 down -> y partials,
 // mode 3 gate/up with 64+64-row stacked tiles (bn <= 32; weight maps with 64-row boxes).

@@ -105,11 +105,14 @@ __device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int 
         const int b0 = off[e] / block_m, nb = (off[e + 1] - off[e]) / block_m;
         if (nb == 0) continue;
         const int p0 = sloc[3 * e], p1 = sloc[3 * e + 1], p2 = sloc[3 * e + 2];
+        const int2 grp = make_int2(uu, (nb + 1) >> 1);
         for (int j = 0; j < (nb >> 1); ++j) {
+            if (rs.unit_group) rs.unit_group[uu] = grp;
             rs.units[uu] = make_int4((b0 + 2 * j) << 1, e, p0, p1);
             rs.unit_w2[uu++] = p2;
         }
         if (nb & 1) {
+            if (rs.unit_group) rs.unit_group[uu] = grp;
             rs.units[uu] = make_int4(((b0 + nb - 1) << 1) | 1, e, p0, p1);
             rs.unit_w2[uu++] = p2;
         }

@@ -109,6 +109,10 @@ class DecodeStack:
         self.copy_stream = torch.cuda.Stream(device=device)
         self.ready = [torch.cuda.Event() for _ in range(2)]
         self.free = [torch.cuda.Event() for _ in range(2)]
+        # copy-in of experts a prediction missed: device-readable addresses of the pinned host
+        # copies, and per layer the list of what the last step copied in
+        self.host_table = pm.device_pointers(self.host) if self.host is not None else None
+        self.missed = [torch.zeros(1 + 2 * E, dtype=torch.int32, device=device) for _ in range(n_layers)]
 
     # -- bookkeeping --------------------------------------------------------------------------
     def schedule(self, logits_np):
@@ -119,6 +123,23 @@ class DecodeStack:
         for l in range(self.L):
             need = np.intersect1d(routed_experts(logits_np[l], self.cfg.k), self.offloaded[l])
             bs = np.full(E, -1, np.int32)
+            slots = np.arange(len(need), dtype=np.int32)
+            bs[need] = (l % 2) * self.slots + slots
+            sched.append((need, slots, torch.from_numpy(bs).to(self.device)))
+        return sched
+
+    def schedule_predicted(self, predicted):
+        """For one step from a prediction (predicted[l] = experts expected at layer l, e.g. the
+        previous step's routing) instead of the actual routing: the predicted offloaded experts are
+        prefetched into buffer l % 2, every other offloaded expert is marked absent (-2), and the
+        copy-in step before the layer brings in whatever the actual routing adds (Rimuru, "The
+        pipeline...": predicted experts join the prefetch queue, actual routing decides)."""
+        E = self.cfg.E
+        sched = []
+        for l in range(self.L):
+            need = np.intersect1d(np.asarray(predicted[l], dtype=np.int64), self.offloaded[l])[:self.slots]
+            bs = np.full(E, -1, np.int32)
+            bs[self.offloaded[l]] = -2
             slots = np.arange(len(need), dtype=np.int32)
             bs[need] = (l % 2) * self.slots + slots
             sched.append((need, slots, torch.from_numpy(bs).to(self.device)))
@@ -145,10 +166,13 @@ class DecodeStack:
         self.ready[b].record(self.copy_stream)                 # RAW: compute waits for it
 
     # -- one step -----------------------------------------------------------------------------
-    def step(self, x0, logits_dev, sched, step_idx, acts, ws, first_prefetched=False):
+    def step(self, x0, logits_dev, sched, step_idx, acts, ws, first_prefetched=False,
+             copy_in=False, stall_events=None):
         """Run all layers on x0 ([T, d] bf16); layer l reads logits_dev[l].  The copy for layer 0
-        is issued here unless the previous step already issued it (first_prefetched).  Returns
-        the last layer's output tensor (one of `acts`)."""
+        is issued here unless the previous step already issued it (first_prefetched).  With
+        copy_in (a schedule from schedule_predicted), each layer first copies in the routed
+        experts the prediction missed, on the compute stream; stall_events[l] = (before, after)
+        bracket that step.  Returns the last layer's output tensor (one of `acts`)."""
         cur = torch.cuda.current_stream()
         j = step_idx % self.layouts
         if not first_prefetched:
@@ -158,6 +182,13 @@ class DecodeStack:
             if l + 1 < self.L:
                 self.prefetch(l + 1, sched[l + 1])          # overlaps layer l's compute
             cur.wait_event(self.ready[l % 2])                # RAW
+            if copy_in:
+                if stall_events is not None:
+                    stall_events[l][0].record(cur)
+                pm.copy_in_missing(self.plans[l][j], logits_dev[l], sched[l][2], l % 2,
+                                   self.host_table, self.missed[l], stream=cur)
+                if stall_events is not None:
+                    stall_events[l][1].record(cur)
             out = acts[l % 2]
             self.plans[l][j].forward(x, logits_dev[l], self.tables[l][j], sched[l][2], out=out,
                                      workspace=ws)

@@ -54,3 +54,16 @@ def test_measured_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
 
 def test_job_throughput_counts_all_ranks():
     assert bench.job_throughput(100.0, 4, 2.0) == pytest.approx(200.0)
+
+
+def test_dominant_kernel_takes_the_burst_peak_in_short_regions():
+    peaks = {"bf16_tflops_sustained": 1000.0, "bf16_tflops": 1200.0, "hbm_gbs": 5000.0,
+             "sm_max_mhz": 2000.0}
+    kw = {"flops": 1.2e12, "bytes": 1e9}          # tensor-bound; 1 ms at the burst peak
+    short = bench.dominant_roofline(kw, 2e-3, 4, peaks, region_s=0.1)
+    assert short["bound"] == "tensor" and short["peak"] == 1200.0 and short["peak_kind"] == "burst"
+    assert short["frac"] == pytest.approx(0.5)
+    long = bench.dominant_roofline(kw, 2e-3, 4, peaks, region_s=2.5)
+    assert long["peak"] == 1000.0 and long["peak_kind"] == "sustained"
+    mem = bench.dominant_roofline({"flops": 1e9, "bytes": 1e10}, 4e-3, 5, peaks, region_s=0.1)
+    assert mem["bound"] == "hbm" and mem["frac"] == pytest.approx(0.5)

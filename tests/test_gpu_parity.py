@@ -268,3 +268,27 @@ def test_pair_path_back_to_back_calls_are_identical():
     rows = np.arange(0, T, 37)
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np[rows], L.logits_np[rows])
     assert_close(first[rows], ref["out_bf16"])
+
+
+def test_pair_path_with_experts_larger_than_l2_share():
+    """Experts whose gate/up and down matrices each exceed a quarter of L2 switch the CTA-pair
+    GEMMs to the expert-major tile order (N tile by N tile, the expert's units innermost).  Its
+    output matches the oracle, is bit-identical to the contiguous twin, and the routing state is
+    unchanged by the order."""
+    cfg = syn.custom_config("bigexp", d=2048, f=8704, E=4, k=2, S=0, n_buffered=1, slots_per_buffer=1)
+    T = 1500
+    L = setup_layer(cfg, T)
+    L.plan.set_path(pm.PATH_TC2)
+    ws = pm.alloc_workspace(L.desc, T)
+    out = out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, workspace=ws))
+    assert L.plan.device_error() == 0
+    st = L.plan.routing_state(ws, T)
+    rids, _ = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
+    assert np.array_equal(st["ids"], rids)
+    cw = pl.contiguous_weights(cfg, L.w)
+    cplan = pm.Plan(L.desc, cw, 3 * (cfg.E + cfg.S))
+    cplan.set_path(pm.PATH_TC2)
+    assert np.array_equal(out, out_bits(cplan.contig_forward(L.hidden, L.logits)))
+    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(3).choice(T, 46, replace=False)]))
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np[rows], L.logits_np[rows])
+    assert_close(out[rows], ref["out_bf16"], "expert-major order")
