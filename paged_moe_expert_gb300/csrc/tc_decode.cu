@@ -363,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    // the roles above run on one lane of their warp; the warp converges before the block barrier
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

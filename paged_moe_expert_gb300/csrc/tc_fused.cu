@@ -63,7 +63,8 @@ constexpr int kTabIds = kTabSlotExpert + 2048;               // i32 [32][16] rou
 constexpr int kTabW = kTabIds + 2048;                        // f32 [32][16] routing weights
 constexpr int kTabStarts = kTabW + 2048;                     // i32 [3][257] CTA ranges
 constexpr int kTabMisc = kTabStarts + 3 * 4 * kStartsLen + 4;   // i32 [64]
-constexpr int kTabBytes = (kTabMisc + 256 + 127) / 128 * 128;
+constexpr int kTabXch = (kTabMisc + 256 + 15) / 16 * 16;        // f32 [32][64] up -> gate lanes
+constexpr int kTabBytes = (kTabXch + 32 * 64 * 4 + 127) / 128 * 128;
 
 template <int BN>
 struct FCfg {
@@ -198,6 +199,8 @@ __device__ bool grid_barrier(uint32_t* flags, int G, int cta, uint32_t target, i
 }
 
 __device__ __forceinline__ void group_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kGroupThreads) : "memory"); }
+// the four epilogue warps (2..5)
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -245,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* w_s = reinterpret_cast<float*>(tab + kTabW);
     int32_t* starts = reinterpret_cast<int32_t*>(tab + kTabStarts);   // [3][kStartsLen]
     int32_t* misc = reinterpret_cast<int32_t*>(tab + kTabMisc);
+    float* xch = reinterpret_cast<float*>(tab + kTabXch);
     // misc: [0..7] scan scratch, [8] routed experts Ar, [9] abort, [10] TMEM address,
     //       [11] barrier decision, [12] epoch word at entry, [13] down stages armed,
     //       [14] first down stage, [15] producer done, [20..23] gate/up pieces written per
@@ -604,10 +608,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (next_piece(it, hi, KB, u, kb0, kb1)) {
                     const int a = sp == 2 ? u / M2 : (sp == 1 ? S : 0) + u / F64;
                     const uint32_t mask = a < S ? all_tok : tok_mask[slot_expert[a]];
+                    // a gate/up piece that covers its whole tile is the tile's only piece: its h
+                    // comes straight from the accumulator (lanes 0..63 gate, 64..127 up of the
+                    // same 64 columns; the up lanes pass their values through shared memory)
+                    const bool whole = sp < 2 && kb0 == 0 && kb1 == KB;
                     if (ep_ok && !mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) ep_ok = false;
-                    if (ep_ok) {
-                        tc_fence_after();
-                        const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+                    if (ep_ok) tc_fence_after();
+                    const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+                    if (whole) {
+                        const int col = (quad & 1) * 32 + lane;
+                        const int ft = u % F64;
+                        uint16_t* hrow = args.h + (int64_t)a * BN * args.f + ft * 64 + col;
+#pragma unroll
+                        for (int c0 = 0; c0 < BN; c0 += 16) {
+                            float v[16];
+                            if (ep_ok) {
+                                tmem_ld16(taddr + c0, v);
+                                tmem_wait_ld();
+                                if (quad >= 2) {
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) xch[(c0 + j) * 64 + col] = v[j];
+                                }
+                            }
+                            epi_bar();
+                            if (ep_ok && quad < 2) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    if (mask >> (c0 + j) & 1u)
+                                        hrow[(int64_t)(c0 + j) * args.f] =
+                                            f32_to_bf16_bits(silu_mul(v[j], xch[(c0 + j) * 64 + col]));
+                            }
+                            epi_bar();
+                        }
+                        if (quad < 2) fence_proxy_async_global();   // h is read by TMA next
+                        epi_bar();
+                        if (ep_ok && quad == 0 && lane == 0)
+                            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(args.hflag + a * F64 + ft),
+                                         "r"(epoch)
+                                         : "memory");
+                        if (ep_ok) tc_fence_before();
+                    } else if (ep_ok) {
                         float* dst = P + ((int64_t)(u + cta) * BN) * 128 + row;
 #pragma unroll
                         for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -649,6 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (ok && next_piece(it, hi, KB1, u, kb0, kb1)) {
                     const int my = idx++;
                     if (my % nw != wsel) continue;
+                    if (kb0 == 0 && kb1 == KB1) continue;   // a whole tile: its epilogue wrote h
                     const uint64_t t0 = globaltimer();
                     for (uint32_t w = 1;; ++w) {
                         const bool done = epi_cnt[0] > my && epi_cnt[1] > my && epi_cnt[2] > my && epi_cnt[3] > my;
@@ -843,14 +884,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc_o = fmaf(wj[q], y, acc_o);
                     }
                 }
+                if (leader) TRACE(23);   // combine: first item's partials summed
                 if (m < args.d) args.out[(int64_t)t * args.d + m] = f32_to_bf16_bits(acc_o);
             }
             if (leader) TRACE(12);   // combine done
         }
     }
 
+    // the roles above run on one lane of their warp; the warp converges before the block barrier
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TRACE(24);   // every role done
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),

@@ -540,6 +540,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (kMode == kDown && lane == 0) bulk_wait_all();   // stores done before the CTA exits
     }
 
+    // the roles above run on one lane of their warp; the warp converges before the block barrier
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     cluster_sync();            // the leader's MMAs no longer read the peer's shared memory
