@@ -451,7 +451,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     P->last_T = T;
     P->last_block_m = bm;
     P->last_kernels = ev - 1;
-    P->last_launches = ev - 1 + (!prep && align_ctas(W.np - (int64_t)T * D.num_shared_chunks) > 1 ? 1 : 0);
+    P->last_launches = ev - 1 + (!prep && align_ctas(W.np - (int64_t)T * D.num_shared_chunks, D.num_experts + D.num_shared_chunks) > 1 ? 1 : 0);
     return PMOE_OK;
 }
 

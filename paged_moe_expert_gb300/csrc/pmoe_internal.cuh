@@ -195,7 +195,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int blo
 
 // Sort + pad over several CTAs when there are many pairs (two launches; `part` is scratch of
 // align_part_bytes()); falls back to the single-CTA kernel for few pairs.
-int align_ctas(int64_t NR);
+int align_ctas(int64_t NR, int ES);
 size_t align_part_bytes();
 cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, int block_m,
                                int32_t* part, int32_t* sorted_ids, int32_t* block_expert,

@@ -248,7 +248,12 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
 //            pads, the block map and the page resolution are split across the C CTAs.
 // ---------------------------------------------------------------------------------------------
 constexpr int kAlignMaxCtas = 64;
-constexpr int kAlignPairsPerCta = 2048;
+constexpr int kAlignOneCtaPairs = 2048;   // up to this many routed pairs: the one-CTA kernel
+// above: one CTA per max(512, 2 * (E + S)) pairs, at most 64 -- every scatter CTA also sums the
+// histograms of the CTAs before it over all experts, so CTAs get dearer with more experts
+// (measured at 4096 tokens: 60 experts 20 -> 16 us going from 8 to 32 CTAs; 513 experts 16 -> 18
+// us going from 20 to 64)
+constexpr int kAlignPairsPerCta = 512;
 
 __global__ void __launch_bounds__(kAlignWarps * 32) align_count_kernel(
     const int32_t* __restrict__ ids, int NR, int E, int ES, int seg, int32_t* __restrict__ part) {
@@ -490,8 +495,10 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int S, int blo
                       resolve ? 1 : 0);
 }
 
-int align_ctas(int64_t NR) {
-    int64_t c = (NR + kAlignPairsPerCta - 1) / kAlignPairsPerCta;
+int align_ctas(int64_t NR, int ES) {
+    if (NR <= kAlignOneCtaPairs) return 1;
+    const int64_t per = 2 * (int64_t)ES > kAlignPairsPerCta ? 2 * (int64_t)ES : kAlignPairsPerCta;
+    int64_t c = (NR + per - 1) / per;
     if (c < 1) c = 1;
     if (c > kAlignMaxCtas) c = kAlignMaxCtas;
     return (int)c;
@@ -504,7 +511,7 @@ cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, i
                                int32_t* inv, int32_t* meta, const ResolveArgs* resolve,
                                cudaStream_t s) {
     const int64_t NR = (int64_t)T * k;
-    const int C = align_ctas(NR);
+    const int C = align_ctas(NR, E + S);
     if (C == 1)
         return launch_align(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, resolve, s);
     const int ES = E + S;

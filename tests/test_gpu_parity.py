@@ -292,3 +292,44 @@ def test_pair_path_with_experts_larger_than_l2_share():
     rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(3).choice(T, 46, replace=False)]))
     ref = oracle_layer(cfg, L.w).forward(L.hidden_np[rows], L.logits_np[rows])
     assert_close(out[rows], ref["out_bf16"], "expert-major order")
+
+
+MAXCFG = syn.custom_config("maxsizes", d=64, f=128, E=976, k=16, S=48, n_buffered=40,
+                           slots_per_buffer=40)
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+@pytest.mark.parametrize("T", [1, 16, 300])
+def test_forward_at_maximum_sizes(T, path):
+    """E + S = 1024 experts (the most the library takes), k = 16, k + S = 64 pairs per token:
+    routing with 32 logits per lane, the widest sort and every kernel family against the oracle,
+    with the routing state of the call read back bit-exact."""
+    if path == pm.PATH_FUSED and T > FUSED_MAX_T:
+        pytest.skip("the fused decode kernel takes at most 32 tokens")
+    cfg = MAXCFG
+    L = setup_layer(cfg, T)
+    L.plan.set_path(path)
+    ws = pm.alloc_workspace(L.desc, T)
+    out = out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, workspace=ws))
+    assert L.plan.device_error() == 0
+    st = L.plan.routing_state(ws, T)
+    rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
+    assert np.array_equal(st["ids"], rids)
+    np.testing.assert_allclose(st["weights"], rw, rtol=3e-5, atol=1e-7)
+    if st["path"] != pm.PATH_FUSED:
+        ref_al = oracle.align(rids, cfg.E, cfg.S, st["block_m"])
+        assert np.array_equal(st["sorted_ids"], ref_al["sorted_ids"])
+        assert np.array_equal(st["inv"], ref_al["inv"])
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
+    assert_close(out, ref["out_bf16"], "max sizes T=%d" % T)
+
+
+def test_empty_batch_writes_nothing():
+    cfg = syn.CONFIGS["tiny"]
+    L = setup_layer(cfg, 4)
+    out = torch.full((0, cfg.d), 1.0, dtype=torch.bfloat16, device="cuda")
+    res = L.plan.forward(L.hidden[:0], L.logits[:0], L.page_table, L.buf_slot, out=out,
+                         workspace=pm.alloc_workspace(L.desc, 4))
+    torch.cuda.synchronize()
+    assert res.shape == (0, cfg.d)
+    assert L.plan.device_error() == 0
