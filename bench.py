@@ -34,7 +34,7 @@ if ROOT not in sys.path:
 from paged_moe_expert_gb300 import synthetic as syn  # noqa: E402
 
 METRIC = "paged fused-MoE TFLOP/s & weight GB/s vs roofline; overhead vs contiguous"
-PATH_NAMES = {0: "auto", 1: "stream", 2: "tc", 3: "tc_decode", 4: "tc2", 5: "fused"}
+PATH_NAMES = {0: "auto", 1: "stream", 2: "tc", 3: "tc_decode", 4: "tc2", 5: "fused", 6: "slice"}
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -253,7 +253,7 @@ class Layer:
 
 
 def tc_family_path(path):
-    return path in (2, 3, 4, 5)
+    return path in (2, 3, 4, 5, 6)
 
 
 def max_over_ranks(seconds: float, dist, device) -> float:
@@ -690,7 +690,7 @@ def elastic_sweep(args):
         print(json.dumps(line), flush=True)
 
 
-PATH_IDS = {"auto": 0, "stream": 1, "tc": 2, "tc_decode": 3, "tc2": 4, "fused": 5}
+PATH_IDS = {"auto": 0, "stream": 1, "tc": 2, "tc_decode": 3, "tc2": 4, "fused": 5, "slice": 6}
 # a timed region at least this long runs at the power-capped (sustained) clocks; shorter ones are
 # compared with the burst peak
 SUSTAINED_REGION_S = 2.0

@@ -93,9 +93,15 @@ typedef enum {
                                (tcgen05 cta_group::2, 256x256 tiles); an expert's odd last
                                block runs in the same pair kernel with the weights on the MMA's
                                M side and its 128 tokens on N */
-    PMOE_PATH_FUSED = 5     /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
+    PMOE_PATH_FUSED = 5,    /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
                                (one CTA per SM) whose weight streams are split evenly over the
                                SMs; see moe_paged_forward for what it requires of the caller */
+    PMOE_PATH_SLICE = 6     /* T <= 16 only: the whole layer in one persistent tcgen05 kernel
+                               whose CTAs each own whole 64-column tiles of the intermediate
+                               dimension (gate/up, SiLU-and-mul and their slice of the down
+                               projection, no cross-CTA hand-off before the final sum); refused
+                               (PMOE_ERR_UNSUPPORTED) when a routing could leave more than 16
+                               tiles per SM; same caller requirements as PMOE_PATH_FUSED */
 } pmoe_path;
 
 /* Text of a status; never NULL. */
@@ -124,7 +130,8 @@ pmoe_status pmoe_plan_last_run(pmoe_plan_t plan, int32_t* path, int32_t* n_steps
  * launching its i-th kernel and events[n_kernels] after the last one (at most n events are
  * recorded), so elapsed times between consecutive events are per-kernel durations.  The kernel
  * order is: routing, sort-and-pad, [row gather,] gate/up GEMM, down GEMM, combine, where for
- * T <= 128 routing and sort-and-pad are one kernel; the fused decode path is one kernel.  NULL entries
+ * T <= 128 routing and sort-and-pad are one kernel; the fused and column-slice decode paths are one
+ * kernel each.  NULL entries
  * are skipped (to bracket one kernel only).  The caller owns the events; n = 0 (or events = NULL)
  * turns the hook off.  At most 16 events. */
 pmoe_status pmoe_plan_set_profile_events(pmoe_plan_t plan, const pmoe_event_t* events, int32_t n);
@@ -152,9 +159,9 @@ size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens);
  * workspace).  So those four must not be written by a kernel of the same stream that triggers
  * its dependents early (no kernel of this library writes them; ordinary kernels and copies are
  * complete before the next launch starts).
- * The fused decode path (T <= 32) synchronises its CTAs through two words that the plan owns, so
- * forward calls of one plan must not overlap on the GPU (the plan's error word is shared the same
- * way).  Its waits give up after about 2 s with PMOE_ERR_TIMEOUT in the error word (only if the
+ * The fused and column-slice decode paths (T <= 32, T <= 16) synchronise their CTAs through words
+ * that the plan owns, so forward calls of one plan must not overlap on the GPU (the plan's error
+ * word is shared the same way).  Their waits give up after about 2 s with PMOE_ERR_TIMEOUT in the error word (only if the
  * GPU cannot hold one CTA per SM for this call, e.g. when other work occupies SMs indefinitely);
  * reading the error word with clear != 0 resets the plan's words for the next call. */
 pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
@@ -171,22 +178,26 @@ pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,
 typedef struct {
     int32_t path;          /* pmoe_path the call ran */
     int32_t tokens;        /* its T */
-    int32_t block_m;       /* rows per sorted block; 0 on the fused path, which sorts nothing */
+    int32_t block_m;       /* rows per sorted block; 0 on the fused and column-slice paths, which
+                              sort nothing */
     int32_t top_k;         /* k */
     int64_t ids;           /* int32 [T][k]: the k experts of each token, largest logit first
-                              (the fused path: CTA 0's routing, every CTA routes the same way) */
+                              (fused and column-slice paths: CTA 0's routing, every CTA routes
+                              the same way) */
     int64_t weights;       /* fp32 [T][k]: their routing weights */
     int64_t sorted_ids;    /* int32 [n_padded]: the pair in each sorted row (pads hold T*(k+S)) */
     int64_t block_expert;  /* int32 [n_padded / block_m]: the expert of each block */
     int64_t inv;           /* int32 [T*(k+S)]: the sorted row of each pair */
     int64_t meta;          /* int32 [16]: [0] n_padded (sorting paths), [1] work units and [2] of
-                              them single blocks (CTA-pair path), [3] active slots (fused path) */
+                              them single blocks (CTA-pair path), [3] active slots (fused and
+                              column-slice paths) */
     int64_t block_rows;    /* int32 [n_padded / block_m]: valid rows of each block (PMOE_PATH_TC) */
     int64_t units;         /* int32 [meta[1]][4]: CTA-pair work units {first block << 1 | single
                               block, expert, W1 location, W3 location}, location = map << 29 | page
                               with map 0 pool, 1 + b load buffer b (PMOE_PATH_TC2) */
     int64_t active;        /* int32 [meta[3]]: the expert of each active slot, shared chunks
-                              E..E+S-1 first, then the routed experts in ascending id (fused path) */
+                              E..E+S-1 first, then the routed experts in ascending id (fused and
+                              column-slice paths) */
 } pmoe_routing_view;
 pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_view* out);
 

@@ -16,11 +16,11 @@ import torch
 
 from . import _lib
 from .adjuster import Adjuster
-from ._lib import (PATH_AUTO, PATH_FUSED, PATH_STREAM, PATH_TC, PATH_TC2, PATH_TC_DECODE, LayerDesc,
+from ._lib import (PATH_AUTO, PATH_FUSED, PATH_SLICE, PATH_STREAM, PATH_TC, PATH_TC2, PATH_TC_DECODE, LayerDesc,
                    PmoeError)
 
 __all__ = ["Adjuster", "LayerDesc", "Plan", "PmoeError", "workspace_size", "route", "align",
-           "prefetch_async", "fill_pages_async", "wait_event", "copy_in_missing", "device_pointers", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED",
+           "prefetch_async", "fill_pages_async", "wait_event", "copy_in_missing", "device_pointers", "PATH_AUTO", "PATH_STREAM", "PATH_TC", "PATH_TC_DECODE", "PATH_TC2", "PATH_FUSED", "PATH_SLICE",
            "make_desc"]
 
 

@@ -21,7 +21,7 @@ STATUS = {0: "PMOE_OK", 1: "PMOE_ERR_INVALID_ARG", 2: "PMOE_ERR_PAGE_OOB", 3: "P
           7: "PMOE_ERR_WORKSPACE"}
 OK, ERR_INVALID_ARG, ERR_PAGE_OOB, ERR_SLOT_OOB, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, \
     ERR_WORKSPACE = range(8)
-PATH_AUTO, PATH_STREAM, PATH_TC, PATH_TC_DECODE, PATH_TC2, PATH_FUSED = 0, 1, 2, 3, 4, 5
+PATH_AUTO, PATH_STREAM, PATH_TC, PATH_TC_DECODE, PATH_TC2, PATH_FUSED, PATH_SLICE = 0, 1, 2, 3, 4, 5, 6
 
 
 class LayerDesc(ctypes.Structure):

@@ -182,7 +182,36 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
         W.fp2 = q; q = align256(q + sizeof(float) * (size_t)F.p2_pieces * F.bn * 128);
         if (q > W.total) W.total = q;
     }
+    // column-slice decode kernel (T <= kSliceMaxTokens): one fp32 partial of the output per CTA
+    W.sp = 0;
+    if (T <= kSliceMaxTokens) {
+        W.sp = W.x;
+        const size_t q = align256(W.sp + sizeof(float) * (size_t)kFusedMaxGrid * T * D.d);
+        if (q > W.total) W.total = q;
+    }
     return W;
+}
+
+// The column-slice decode kernel over `grid` CTAs: whether every routing of T tokens leaves at
+// most kSliceMaxTiles 64-column tiles per CTA, and g0, the CTAs whose first tile is a shared-chunk
+// tile under every routing (tile c of CTA c < G' for G' = ceil(NT / ceil(NT / grid)), NT the
+// tiles of the active experts), which may stream it before routing.
+static bool slice_fit(const pmoe_layer_desc& D, int64_t T, int grid, int* g0) {
+    if (T < 1 || T > kSliceMaxTokens || grid < 1) return false;
+    const int64_t f64 = D.f / 64, E = D.num_experts, S = D.num_shared_chunks;
+    const int64_t ar_lo = D.top_k < E ? D.top_k : E;
+    const int64_t ar_hi = T * D.top_k < E ? T * D.top_k : E;
+    int64_t gmin = grid;
+    for (int64_t ar = ar_lo; ar <= ar_hi; ++ar) {
+        const int64_t nt = (S + ar) * f64;
+        const int64_t tpc = (nt + grid - 1) / grid;
+        if (tpc > kSliceMaxTiles) return false;
+        const int64_t gw = (nt + tpc - 1) / tpc;
+        if (gw < gmin) gmin = gw;
+    }
+    const int64_t shared_tiles = S * f64;
+    *g0 = (int)(shared_tiles < gmin ? shared_tiles : gmin);
+    return true;
 }
 
 // Records the plan's i-th profiling event, if the measurement hook is set.
@@ -215,6 +244,12 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     int path = P->path;
     if (path == PMOE_PATH_FUSED && T > kFusedMaxTokens)
         return fail(PMOE_ERR_UNSUPPORTED, "the fused decode kernel takes at most 32 tokens");
+    const int dgrid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;   // decode kernels
+    int slice_g0 = 0;
+    const bool slice_ok = slice_fit(D, T, dgrid, &slice_g0);
+    if (path == PMOE_PATH_SLICE && !slice_ok)
+        return fail(PMOE_ERR_UNSUPPORTED,
+                    "the column-slice decode kernel takes at most 16 tokens and 16 column tiles per SM");
     if (path == PMOE_PATH_AUTO) {
         const int64_t routed = (int64_t)T * D.top_k;   // routed tokens; per expert: routed / E
         // the fused decode kernel up to 32 tokens for layers of at most 128 experts and up to 16
@@ -228,7 +263,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
              : PMOE_PATH_TC;
     }
     const bool tc_family = path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE || path == PMOE_PATH_TC2 ||
-                           path == PMOE_PATH_FUSED;
+                           path == PMOE_PATH_FUSED || path == PMOE_PATH_SLICE;
     if (tc_family && !P->have_tmaps)
         return fail(PMOE_ERR_UNSUPPORTED, "tensor maps unavailable for this plan");
 
@@ -256,10 +291,53 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
             return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
     }
 
+    if (path == PMOE_PATH_SLICE) {
+        // routing, gate/up + SiLU-and-mul, down and the combine in one persistent launch, each CTA
+        // on whole columns of the intermediate dimension
+        CUtensorMap sx;
+        if (!encode_rows_map(&sx, hidden, T, D.d, 16)) return fail(PMOE_ERR_CUDA, "tensor map encoding failed");
+        FusedArgs fa{};
+        fa.logits = logits;
+        fa.page_table = page_table;
+        fa.buf_slot = buf_slot;
+        fa.p2 = at<float>(ws, W.sp);
+        fa.out = static_cast<uint16_t*>(out);
+        fa.flags = P->d_flags;
+        fa.err = P->d_error;
+        fa.ids_out = ids;
+        fa.w_out = w;
+        fa.active_out = sorted;
+        fa.meta_out = meta;
+        fa.num_pages = P->num_pages;
+        fa.g0 = slice_g0;
+        fa.T = T;
+        fa.E = D.num_experts;
+        fa.k = D.top_k;
+        fa.S = D.num_shared_chunks;
+        fa.renorm = D.renormalize;
+        fa.d = D.d;
+        fa.f = D.f;
+        fa.slots_per_buffer = D.slots_per_buffer;
+        fa.have_buf0 = P->buf[0] != nullptr;
+        fa.have_buf1 = P->buf[1] != nullptr;
+        fa.contig = contig ? 1 : 0;
+        fa.epl = 1;
+        while (32 * fa.epl < D.num_experts) fa.epl <<= 1;
+        PMOE_CUDA(mark(P, 0, stream), "profile event");
+        PMOE_CUDA(launch_slice_decode(sx, P->tm_rows_d64, P->tm_rows_f, fa, dgrid, stream), "slice decode");
+        PMOE_CUDA(mark(P, 1, stream), "profile event");
+        P->last_path = path;
+        P->last_kernels = 1;
+        P->last_launches = 1;
+        P->last_T = T;
+        P->last_block_m = 0;
+        return PMOE_OK;
+    }
+
     if (path == PMOE_PATH_FUSED) {
         // routing, gate/up + SiLU-and-mul, down and the combine in one persistent launch
         const FusedShape F = fused_shape(D, T);
-        const int grid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;
+        const int grid = dgrid;
         CUtensorMap fx, fh;
         if (!encode_rows_map(&fx, hidden, T, D.d, F.bn) ||
             !encode_rows_map(&fh, at<uint16_t>(ws, W.fh), F.a_max * F.bn, D.f, F.bn))
@@ -544,7 +622,7 @@ pmoe_status pmoe_plan_destroy(pmoe_plan_t plan) {
 }
 
 pmoe_status pmoe_plan_set_path(pmoe_plan_t plan, int32_t path) {
-    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_FUSED)
+    if (!plan || path < PMOE_PATH_AUTO || path > PMOE_PATH_SLICE)
         return fail(PMOE_ERR_INVALID_ARG, "bad plan or path");
     reinterpret_cast<Plan*>(plan)->path = path;
     return PMOE_OK;
@@ -583,7 +661,7 @@ pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_vie
     v.weights = (int64_t)W.w;
     v.meta = (int64_t)W.meta;
     v.sorted_ids = v.block_expert = v.inv = v.block_rows = v.units = v.active = -1;
-    if (v.path == PMOE_PATH_FUSED) {
+    if (v.path == PMOE_PATH_FUSED || v.path == PMOE_PATH_SLICE) {
         v.active = (int64_t)W.sorted;
     } else {
         v.sorted_ids = (int64_t)W.sorted;

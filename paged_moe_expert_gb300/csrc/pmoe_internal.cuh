@@ -21,6 +21,8 @@ constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorte
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
 constexpr int kFusedMaxTokens = 32;     // fused decode kernel: tokens per call (MMA N <= 32)
 constexpr int kFusedMaxGrid = 256;      // fused decode kernel: CTAs (one per SM)
+constexpr int kSliceMaxTokens = 16;     // column-slice decode kernel: tokens per call (MMA N = 16)
+constexpr int kSliceMaxTiles = 16;      // column-slice decode kernel: 64-column tiles per CTA
 
 // Where one expert matrix lives: map 0 = pool, 1 = load buffer 0, 2 = load buffer 1; `page` is
 // the page index within that map (for a buffer, 3 * slot + matrix).  map < 0: invalid.
@@ -33,6 +35,7 @@ struct ExpertLoc {
 struct WsLayout {
     size_t ids, w, sorted, bexp, inv, meta, loc, part, units, unit_w2, ugroup, brows, x, h, y, total;
     size_t fp1, fh, fp2;   // fused decode kernel: gate/up partials, h, down partials
+    size_t sp;             // column-slice decode kernel: per-CTA partials [kFusedMaxGrid][T][d] fp32
     int64_t np;          // T * (k + S) pairs
     int64_t cap;         // rows of sorted_ids / h / y / x
     int64_t nblk_max;    // upper bound on sorted blocks
@@ -273,7 +276,10 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, con
                               SharedRows sh = SharedRows{}, int shared_units = 0);
 
 // Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
-// tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.
+// tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.  The
+// column-slice decode kernel (tc_slice.cu, T <= 16) takes the same arguments: p2 holds its
+// per-CTA partials [grid][T][d] fp32, g0 the CTAs whose first tile (a shared-chunk tile) is
+// streamed before routing, and p1, h, ucnt, hflag, p1_base1 are unused.
 struct FusedArgs {
     const float* logits;        // [T][E]
     const int32_t* page_table;  // [E+S][3]
@@ -303,6 +309,8 @@ struct FusedArgs {
 cudaError_t launch_fused_decode(const CUtensorMap& xmap, const CUtensorMap& hmap,
                                 const CUtensorMap* w64, const CUtensorMap* wf, const FusedArgs& a,
                                 int bn, int grid, cudaStream_t s);
+cudaError_t launch_slice_decode(const CUtensorMap& xmap, const CUtensorMap* w64, const CUtensorMap* wf,
+                                const FusedArgs& a, int grid, cudaStream_t s);
 
 // Copy-in of absent routed experts (copy_in.cu): routes the T tokens, gives every routed expert
 // with buf_slot == -2 a free slot of load buffer `buf` (buf_slot updated on the device), lists

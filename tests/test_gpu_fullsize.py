@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 _W = {}
 PATH_NAMES = {pm.PATH_STREAM: "stream", pm.PATH_TC: "tc", pm.PATH_TC_DECODE: "tc_decode",
-              pm.PATH_TC2: "tc2", pm.PATH_FUSED: "fused"}
+              pm.PATH_TC2: "tc2", pm.PATH_FUSED: "fused", pm.PATH_SLICE: "slice"}
 
 
 def weights(name):
@@ -35,11 +35,12 @@ CASES = [("qwen15", 1), ("qwen15", 16), ("qwen15", 32), ("qwen15", 128), ("qwen1
 
 
 @pytest.mark.parametrize("name,T", CASES)
-@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM, pm.PATH_TC_DECODE, pm.PATH_TC, pm.PATH_TC2],
-                         ids=["auto", "stream", "tc_decode", "tc", "tc2"])
+@pytest.mark.parametrize("path", [pm.PATH_AUTO, pm.PATH_STREAM, pm.PATH_TC_DECODE, pm.PATH_TC, pm.PATH_TC2,
+                                  pm.PATH_SLICE],
+                         ids=["auto", "stream", "tc_decode", "tc", "tc2", "slice"])
 def test_full_size_sampled(name, T, path):
-    if path == pm.PATH_STREAM and T > 16:
-        pytest.skip("the weight-streaming kernels serve decode sizes")
+    if path in (pm.PATH_STREAM, pm.PATH_SLICE) and T > 16:
+        pytest.skip("the weight-streaming and column-slice kernels serve decode sizes")
     if path == pm.PATH_TC_DECODE and T > 32:
         pytest.skip("covered by the automatic path above 32 tokens")
     if path in (pm.PATH_TC, pm.PATH_TC2) and T < 512:
@@ -55,7 +56,7 @@ def test_full_size_sampled(name, T, path):
     rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
     assert np.array_equal(st["ids"], rids)
     np.testing.assert_allclose(st["weights"], rw, rtol=3e-5, atol=1e-7)
-    if st["path"] == pm.PATH_FUSED:
+    if st["path"] in (pm.PATH_FUSED, pm.PATH_SLICE):
         assert np.array_equal(st["active"], np.concatenate([cfg.E + np.arange(cfg.S), np.unique(rids)]))
     else:
         ref_al = oracle.align(rids, cfg.E, cfg.S, st["block_m"])

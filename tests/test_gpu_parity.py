@@ -74,17 +74,23 @@ SMALL = [
 ]
 
 
-PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED]
-PATH_IDS = ["stream", "tc", "tc_decode", "tc2", "fused"]
+PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED, pm.PATH_SLICE]
+PATH_IDS = ["stream", "tc", "tc_decode", "tc2", "fused", "slice"]
 FUSED_MAX_T = 32
+SLICE_MAX_T = 16
+DECODE_PATHS = (pm.PATH_FUSED, pm.PATH_SLICE)   # no sort: active slots instead
+
+
+def serves(path, T):
+    return not ((path == pm.PATH_FUSED and T > FUSED_MAX_T) or (path == pm.PATH_SLICE and T > SLICE_MAX_T))
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
 @pytest.mark.parametrize("T", [1, 3, 16, 17, 32, 37, 128, 300])
 def test_forward_matches_oracle(cfg, T, path):
-    if path == pm.PATH_FUSED and T > FUSED_MAX_T:
-        pytest.skip("the fused decode kernel takes at most 32 tokens")
+    if not serves(path, T):
+        pytest.skip("the decode kernels take at most 32 (fused) or 16 (column-slice) tokens")
     if path != pm.PATH_FUSED and T in (17, 32):
         pytest.skip("token counts that only change the fused kernel's tile width")
     L = setup_layer(cfg, T)
@@ -102,7 +108,7 @@ def test_output_independent_of_placement(path):
     cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
                             num_pages=60)
     w = syn.make_weights(cfg)
-    T = 29   # <= 32: every path serves it
+    T = 13 if path == pm.PATH_SLICE else 29   # every path serves it
     outs = []
     for pseed, bidx, nb in [(1, 0, 4), (2, 0, 4), (3, 1, 4), (4, 1, 6), (5, 0, 0)]:
         L = setup_layer(cfg, T, placement_seed=pseed, buffer_index=bidx, n_buffered=nb, weights=w)
@@ -165,7 +171,7 @@ def test_paths_agree(T):
     L = setup_layer(cfg, T)
     outs = []
     for path in PATHS:
-        if path == pm.PATH_FUSED and T > FUSED_MAX_T:
+        if not serves(path, T):
             continue
         L.plan.set_path(path)
         outs.append(out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)))
@@ -177,7 +183,7 @@ def test_paths_agree(T):
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_forward_replays_from_a_cuda_graph(path):
     cfg = syn.custom_config("graph", d=256, f=256, E=6, k=2, S=1, n_buffered=2)
-    T = 24 if path == pm.PATH_FUSED else 40
+    T = {pm.PATH_FUSED: 24, pm.PATH_SLICE: 12}.get(path, 40)
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
     ws = pm.alloc_workspace(L.desc, T)
@@ -304,8 +310,8 @@ def test_forward_at_maximum_sizes(T, path):
     """E + S = 1024 experts (the most the library takes), k = 16, k + S = 64 pairs per token:
     routing with 32 logits per lane, the widest sort and every kernel family against the oracle,
     with the routing state of the call read back bit-exact."""
-    if path == pm.PATH_FUSED and T > FUSED_MAX_T:
-        pytest.skip("the fused decode kernel takes at most 32 tokens")
+    if not serves(path, T):
+        pytest.skip("the decode kernels take at most 32 (fused) or 16 (column-slice) tokens")
     cfg = MAXCFG
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
@@ -316,7 +322,7 @@ def test_forward_at_maximum_sizes(T, path):
     rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
     assert np.array_equal(st["ids"], rids)
     np.testing.assert_allclose(st["weights"], rw, rtol=3e-5, atol=1e-7)
-    if st["path"] != pm.PATH_FUSED:
+    if st["path"] not in DECODE_PATHS:
         ref_al = oracle.align(rids, cfg.E, cfg.S, st["block_m"])
         assert np.array_equal(st["sorted_ids"], ref_al["sorted_ids"])
         assert np.array_equal(st["inv"], ref_al["inv"])
@@ -333,3 +339,67 @@ def test_empty_batch_writes_nothing():
     torch.cuda.synchronize()
     assert res.shape == (0, cfg.d)
     assert L.plan.device_error() == 0
+
+
+def test_slice_rejects_more_than_16_tokens():
+    cfg = syn.CONFIGS["tiny"]
+    L = setup_layer(cfg, 17)
+    L.plan.set_path(pm.PATH_SLICE)
+    with pytest.raises(pm.PmoeError) as ei:
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
+    assert ei.value.status == pm._lib.ERR_UNSUPPORTED
+
+
+def test_slice_and_fused_calls_share_one_plan():
+    """Column-slice and fused calls of different token counts in turn on one plan and one
+    workspace: both kernels step the plan's grid-barrier words the same way, so no call waits
+    out its barrier, every output matches the oracle, and repeated calls are bit-identical."""
+    cfg = syn.custom_config("mixS", d=256, f=384, E=16, k=4, S=2, n_buffered=3)
+    L = setup_layer(cfg, 32)
+    orc = oracle_layer(cfg, L.w)
+    ws = pm.alloc_workspace(L.desc, 32)
+    seen = {}
+    for T, path in [(1, pm.PATH_SLICE), (16, pm.PATH_FUSED), (5, pm.PATH_SLICE), (16, pm.PATH_SLICE),
+                    (32, pm.PATH_FUSED), (1, pm.PATH_SLICE), (5, pm.PATH_SLICE), (1, pm.PATH_FUSED)]:
+        h, lg = syn.make_tokens(cfg, T)
+        L.plan.set_path(path)
+        out = out_bits(L.plan.forward(pl._bf16(h).cuda(), torch.from_numpy(lg).cuda(), L.page_table,
+                                      L.buf_slot, workspace=ws))
+        assert L.plan.device_error() == 0, "T=%d path=%d" % (T, path)
+        assert L.plan.last_run()[0] == path
+        assert_close(out, orc.forward(h, lg)["out_bf16"], "T=%d path=%d" % (T, path))
+        if (T, path) in seen:
+            assert np.array_equal(out, seen[(T, path)])
+        seen[(T, path)] = out
+
+
+@pytest.mark.parametrize("name,T", [("qwen15", 1), ("qwen15", 4), ("qwen15", 16), ("qwen3next", 1),
+                                    ("qwen3next", 16), ("mixtral", 1), ("mixtral", 16)])
+def test_slice_tile_counts_per_cta(name, T):
+    """The column-slice kernel on the measured layer shapes, from one tile per working CTA
+    (Qwen3-Next-shaped, one token: 88 tiles on 88 CTAs) to twelve (Mixtral-shaped, 16 tokens),
+    with shared-chunk tiles streamed before routing on the Qwen shapes, against the oracle on
+    every token."""
+    cfg = syn.CONFIGS[name]
+    L = setup_layer(cfg, T, weights=_weights(name))
+    L.plan.set_path(pm.PATH_SLICE)
+    ws = pm.alloc_workspace(L.desc, T)
+    out = out_bits(L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot, workspace=ws))
+    assert L.plan.device_error() == 0
+    assert L.plan.last_run()[0] == pm.PATH_SLICE
+    st = L.plan.routing_state(ws, T)
+    rids, rw = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
+    assert np.array_equal(st["ids"], rids)
+    assert np.array_equal(st["active"], np.concatenate([cfg.E + np.arange(cfg.S), np.unique(rids)]))
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, L.logits_np)
+    assert_close(out, ref["out_bf16"], "%s T=%d" % (name, T))
+
+
+_WCACHE = {}
+
+
+def _weights(name):
+    if name not in _WCACHE:
+        _WCACHE.clear()
+        _WCACHE[name] = syn.make_weights(syn.CONFIGS[name])
+    return _WCACHE[name]

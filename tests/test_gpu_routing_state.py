@@ -98,7 +98,7 @@ def run_and_check(name, T, path=pm.PATH_AUTO, logits=None, want_path=None):
     assert np.array_equal(st["ids"], rids), "routing ids differ"
     np.testing.assert_allclose(st["weights"].astype(np.float64), rw, rtol=3e-5, atol=1e-7)
     E, S = cfg.E, cfg.S
-    if st["path"] == pm.PATH_FUSED:
+    if st["path"] in (pm.PATH_FUSED, pm.PATH_SLICE):
         want = np.concatenate([E + np.arange(S), np.unique(rids)]).astype(np.int32)
         assert np.array_equal(st["active"], want), "active slots differ"
         return st
@@ -149,6 +149,10 @@ def test_forward_routing_state_mixtral_8192():
     ("qwen3next", 64, pm.PATH_TC_DECODE),  # heavy routing: routing kernel + one-CTA sort
     ("qwen3next", 16, pm.PATH_FUSED),
     ("mixtral", 32, pm.PATH_FUSED),
+    ("tiny", 3, pm.PATH_SLICE),
+    ("qwen15", 16, pm.PATH_SLICE),
+    ("qwen3next", 1, pm.PATH_SLICE),
+    ("qwen3next", 16, pm.PATH_SLICE),
     ("mixtral", 2048, pm.PATH_TC2),
 ])
 def test_forced_path_routing_state_matches_oracle(name, T, path):
