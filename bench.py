@@ -861,14 +861,36 @@ def measure(lay, cfg_key, T, path_name, steps, warmup, device, dist, world, peak
     return res
 
 
+CHAIN_LAYERS = 8
+CHAIN_MAX_TOKENS = 32
+
+
+def chain_plans(lay, n):
+    """n more layers with the same weights and placement in page pools and load buffers of their
+    own, so that a chain of distinct layers can be timed as a decode step runs it (each layer's
+    pages streamed from HBM, the next layer's launch overlapping the previous one's tail)."""
+    from paged_moe_expert_gb300 import pool as pl
+    cfg, out = lay.cfg, []
+    for _ in range(n):
+        pool = pl.new_pool(cfg.num_pages, cfg.f, cfg.d, lay.device)
+        bufs = pl.new_load_buffers(cfg.slots_per_buffer, cfg.f, cfg.d, lay.device)
+        pt, bs = pl.place(cfg, lay.w, lay.placement, pool, bufs, 0)
+        plan = lay.pm.Plan(lay.desc, pool, cfg.num_pages, bufs)
+        out.append((plan, pool, bufs, pt.to(lay.device), bs.to(lay.device)))
+    return out
+
+
 def token_sweep(lay, iters, peaks, device):
     """Every token count of the workload: paged and contiguous forward replayed from CUDA graphs,
-    interleaved, L2 flushed before every timed call (short bursts: the burst bf16 peak)."""
+    interleaved, L2 flushed before every timed call (short bursts: the burst bf16 peak).  Decode
+    sizes (up to 32 tokens) are also timed per layer in a chain of CHAIN_LAYERS distinct layers
+    (one graph, L2 flushed before the chain), the way consecutive layers of a decode step run."""
     pm, cfg = lay.pm, lay.cfg
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     sweep = []
     lay.plan.set_path(pm.PATH_AUTO)
     lay.cplan.set_path(pm.PATH_AUTO)
+    chain = chain_plans(lay, CHAIN_LAYERS) if min(cfg.tokens) <= CHAIN_MAX_TOKENS else []
     for Ts in cfg.tokens:
         _, _, hs, ls = lay.tokens(Ts)
         wss = pm.alloc_workspace(lay.desc, Ts, device)
@@ -888,13 +910,32 @@ def token_sweep(lay, iters, peaks, device):
         ea = lay.e_act(ls)
         wk_s = work(cfg, Ts, ea)
         frac, bound = binding_fraction(wk_s["flops"], wk_s["bytes"], tp, peaks, sustained=False)
-        sweep.append({"tokens": Ts, "path": PATH_NAMES[ps], "launch": "cuda_graph", "ms": tp * 1e3,
-                      "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
-                      "tflops": wk_s["flops"] / tp / 1e12,
-                      "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
-                      "tokens_per_s": Ts / tp, "experts_active": ea,
-                      "binding_roof": bound, "roof_frac": frac})
+        point = {"tokens": Ts, "path": PATH_NAMES[ps], "launch": "cuda_graph", "ms": tp * 1e3,
+                 "contig_ms": tc * 1e3, "overhead_vs_contig": tp / tc - 1.0,
+                 "tflops": wk_s["flops"] / tp / 1e12,
+                 "weight_gbs": wk_s["weight_bytes"] / tp / 1e9,
+                 "tokens_per_s": Ts / tp, "experts_active": ea,
+                 "binding_roof": bound, "roof_frac": frac}
+        if chain and Ts <= CHAIN_MAX_TOKENS:
+            outs = [torch.empty_like(hs) for _ in chain]
+
+            def run_chain():
+                for (pln, _, _, pt_, bs_), o_ in zip(chain, outs):
+                    pln.forward(hs, ls, pt_, bs_, out=o_, workspace=wss)
+            run_chain()
+            gch = capture(run_chain)
+            tch, = time_iters([gch.replay], max(iters // 4, 5), flush)
+            for pln, _, _, _, _ in chain:
+                if pln.device_error() != 0:
+                    raise RuntimeError("device error word set during the %d-token chain" % Ts)
+            per = tch / len(chain)
+            cfrac, _ = binding_fraction(wk_s["flops"], wk_s["bytes"], per, peaks, sustained=False)
+            point.update({"chain_layers": len(chain), "chain_ms_per_layer": per * 1e3, "chain_roof_frac": cfrac})
+            del gch, outs
+        sweep.append(point)
         del wss, gp, gc
+    del chain
+    torch.cuda.empty_cache()
     return sweep
 
 

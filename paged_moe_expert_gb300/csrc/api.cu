@@ -35,9 +35,10 @@ static pmoe_status cuda_fail(cudaError_t e, const char* where) {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Device words a plan owns: the error word, (at 1 KB) one barrier word per CTA, (at 2 KB)
-// the fused decode kernel's gate/up tile counters (8 B) and ready words (4 B), one per tile of
-// f/64 columns of every expert and shared chunk.
+// Device words a plan owns: the error word, (at 256 B) the copy-in's routed-expert bitmap and
+// arrival counter, (at 512 B) the column-slice decode kernel's arrival counter (8 B), (at 1 KB)
+// one barrier word per CTA, (at 2 KB) the fused decode kernel's gate/up tile counters (8 B) and
+// ready words (4 B), one per tile of f/64 columns of every expert and shared chunk.
 static size_t plan_words_bytes(const pmoe_layer_desc& D) {
     const size_t tiles = (size_t)(D.num_experts + D.num_shared_chunks) * (D.f / 64);
     return 2048 + 12 * tiles;
@@ -73,6 +74,12 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
 // hundreds of small experts most experts end in an odd block, which costs a CTA pair as much as
 // a pair of blocks).  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
 constexpr int kSwapMaxTokensPerExpert = 24;
+// The column-slice decode kernel up to 8 tokens while a routing leaves at most 8 column tiles per
+// SM (measured on GB300 against the fused kernel: ahead from 1 to 8 tokens on the Qwen1.5- and
+// Qwen3-Next-shaped layers and at 1 and 2 on the Mixtral-shaped one; behind once a CTA streams
+// twelve tiles, where the fused kernel's even k-block split keeps more bytes in flight per SM).
+constexpr int kSliceAutoTokens = 8;
+constexpr int kSliceAutoTiles = 8;
 constexpr int kPairMinTokensPerExpert = 64;
 constexpr int kPairMaxExperts = 128;
 constexpr int kPrepSmallMaxTokens = 128;
@@ -196,7 +203,7 @@ static WsLayout layout(const pmoe_layer_desc& D, int64_t T) {
 // most kSliceMaxTiles 64-column tiles per CTA, and g0, the CTAs whose first tile is a shared-chunk
 // tile under every routing (tile c of CTA c < G' for G' = ceil(NT / ceil(NT / grid)), NT the
 // tiles of the active experts), which may stream it before routing.
-static bool slice_fit(const pmoe_layer_desc& D, int64_t T, int grid, int* g0) {
+static bool slice_fit(const pmoe_layer_desc& D, int64_t T, int grid, int* g0, int* tiles_max) {
     if (T < 1 || T > kSliceMaxTokens || grid < 1) return false;
     const int64_t f64 = D.f / 64, E = D.num_experts, S = D.num_shared_chunks;
     const int64_t ar_lo = D.top_k < E ? D.top_k : E;
@@ -211,6 +218,7 @@ static bool slice_fit(const pmoe_layer_desc& D, int64_t T, int grid, int* g0) {
     }
     const int64_t shared_tiles = S * f64;
     *g0 = (int)(shared_tiles < gmin ? shared_tiles : gmin);
+    *tiles_max = (int)(((S + ar_hi) * f64 + grid - 1) / grid);
     return true;
 }
 
@@ -245,18 +253,19 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     if (path == PMOE_PATH_FUSED && T > kFusedMaxTokens)
         return fail(PMOE_ERR_UNSUPPORTED, "the fused decode kernel takes at most 32 tokens");
     const int dgrid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;   // decode kernels
-    int slice_g0 = 0;
-    const bool slice_ok = slice_fit(D, T, dgrid, &slice_g0);
+    int slice_g0 = 0, slice_tiles = 0;
+    const bool slice_ok = slice_fit(D, T, dgrid, &slice_g0, &slice_tiles);
     if (path == PMOE_PATH_SLICE && !slice_ok)
         return fail(PMOE_ERR_UNSUPPORTED,
-                    "the column-slice decode kernel takes at most 16 tokens and 16 column tiles per SM");
+                    "the column-slice decode kernel takes at most 8 tokens and 12 column tiles per SM");
     if (path == PMOE_PATH_AUTO) {
         const int64_t routed = (int64_t)T * D.top_k;   // routed tokens; per expert: routed / E
         // the fused decode kernel up to 32 tokens for layers of at most 128 experts and up to 16
         // tokens otherwise (measured on GB300: with hundreds of small experts at 17..32 tokens
         // the small-batch kernels stream a little faster)
         const int fused_max = D.num_experts <= 128 ? kFusedMaxTokens : 16;
-        path = T <= fused_max ? PMOE_PATH_FUSED
+        path = (slice_ok && T <= kSliceAutoTokens && slice_tiles <= kSliceAutoTiles) ? PMOE_PATH_SLICE
+             : T <= fused_max ? PMOE_PATH_FUSED
              : routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
              : (routed >= (int64_t)kPairMinTokensPerExpert * D.num_experts &&
                 D.num_experts <= kPairMaxExperts) ? PMOE_PATH_TC2
@@ -302,7 +311,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         fa.buf_slot = buf_slot;
         fa.p2 = at<float>(ws, W.sp);
         fa.out = static_cast<uint16_t*>(out);
-        fa.flags = P->d_flags;
+        fa.arrive = P->d_arrive;
         fa.err = P->d_error;
         fa.ids_out = ids;
         fa.w_out = w;
@@ -581,6 +590,7 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
     if (e == cudaSuccess) {
         char* base = reinterpret_cast<char*>(P->d_error);
         const size_t tiles = (size_t)(desc->num_experts + desc->num_shared_chunks) * (desc->f / 64);
+        P->d_arrive = reinterpret_cast<unsigned long long*>(base + 512);
         P->d_flags = reinterpret_cast<uint32_t*>(base + 1024);
         P->d_ucnt = reinterpret_cast<unsigned long long*>(base + 2048);
         P->d_hflag = reinterpret_cast<uint32_t*>(base + 2048 + 8 * tiles);
@@ -818,8 +828,8 @@ pmoe_status pmoe_get_device_error(pmoe_plan_t plan, int32_t clear, int32_t* code
     PMOE_CUDA(cudaMemcpyAsync(&v, P->d_error, sizeof v, cudaMemcpyDeviceToHost, s), "read error word");
     PMOE_CUDA(cudaStreamSynchronize(s), "sync");
     if (clear) {
-        // also resets the fused kernel's barrier and tile words, which a kernel that timed out
-        // may leave behind
+        // also resets the decode kernels' barrier words, arrival counter and tile words, which a
+        // kernel that timed out may leave behind
         PMOE_CUDA(cudaMemsetAsync(P->d_error, 0, P->words_bytes, s), "clear error word");
         PMOE_CUDA(cudaStreamSynchronize(s), "sync");
     }

@@ -21,8 +21,8 @@ constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorte
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
 constexpr int kFusedMaxTokens = 32;     // fused decode kernel: tokens per call (MMA N <= 32)
 constexpr int kFusedMaxGrid = 256;      // fused decode kernel: CTAs (one per SM)
-constexpr int kSliceMaxTokens = 16;     // column-slice decode kernel: tokens per call (MMA N = 16)
-constexpr int kSliceMaxTiles = 16;      // column-slice decode kernel: 64-column tiles per CTA
+constexpr int kSliceMaxTokens = 8;      // column-slice decode kernel: tokens per call (MMA N = 16)
+constexpr int kSliceMaxTiles = 12;      // column-slice decode kernel: 64-column tiles per CTA
 
 // Where one expert matrix lives: map 0 = pool, 1 = load buffer 0, 2 = load buffer 1; `page` is
 // the page index within that map (for a buffer, 3 * slot + matrix).  map < 0: invalid.
@@ -52,6 +52,7 @@ struct Plan {
     int64_t num_pages;
     const void* buf[2];
     int32_t* d_error;    // device error word
+    unsigned long long* d_arrive;   // arrival counter of the column-slice decode kernel
     uint32_t* d_flags;   // grid-barrier words of the fused decode kernel (one per CTA)
     unsigned long long* d_ucnt;   // its gate/up tile counters, (E+S)*f/64 of them
     uint32_t* d_hflag;            // its gate/up tile ready words, (E+S)*f/64 of them
@@ -277,9 +278,10 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, con
 
 // Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
 // tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.  The
-// column-slice decode kernel (tc_slice.cu, T <= 16) takes the same arguments: p2 holds its
+// column-slice decode kernel (tc_slice.cu, T <= 8) takes the same arguments: p2 holds its
 // per-CTA partials [grid][T][d] fp32, g0 the CTAs whose first tile (a shared-chunk tile) is
-// streamed before routing, and p1, h, ucnt, hflag, p1_base1 are unused.
+// streamed before routing, arrive its barrier counter, and p1, h, flags, ucnt, hflag, p1_base1
+// are unused (the fused kernel does not use arrive).
 struct FusedArgs {
     const float* logits;        // [T][E]
     const int32_t* page_table;  // [E+S][3]
@@ -289,6 +291,7 @@ struct FusedArgs {
     float* p2;                  // down partials: [pieces][bn][128] fp32
     uint16_t* out;              // [T][d] bf16
     uint32_t* flags;            // grid-barrier words, one per CTA (plan-owned)
+    unsigned long long* arrive; // column-slice kernel: CTAs arrived, +grid per call (plan-owned)
     unsigned long long* ucnt;   // per gate/up tile: (epoch << 32 | pieces done) (plan-owned)
     uint32_t* hflag;            // per gate/up tile: epoch once its h is written (plan-owned)
     int32_t* err;

@@ -1,4 +1,4 @@
-// The paged MoE layer for a few tokens (T <= 16) in one persistent kernel whose CTAs own whole
+// The paged MoE layer for a few tokens (T <= 8) in one persistent kernel whose CTAs own whole
 // columns of the intermediate dimension.
 //
 // The layer is Rimuru's paged fused MoE (paper-daily.com/en, "Expert weights are scattered across
@@ -16,20 +16,25 @@
 //     the CTAs that work (HBM, not the SM count, bounds the stream: 76 or more of the 152 SMs
 //     stream a fixed volume as fast as all of them);
 //   * a CTA computes the gate/up projection of its tiles over the whole K = d (no partial sums),
-//     applies SiLU-and-mul and the token's routing weight in the epilogue, and keeps the result
-//     h' = w_{t,e} * silu(g) * u as bf16 tiles in its own shared memory;
+//     applies SiLU-and-mul (h = bf16(silu(g) * u), the activation every path feeds the down
+//     projection) and the token's routing weight in the epilogue, and keeps h' = w_{t,e} * h in
+//     its own shared memory as two bf16 parts, h'_hi + h'_lo, whose sum carries h' to 17 bits;
 //   * it then computes the down projection restricted to its own columns, y_c = W2[:, its
 //     columns] h'[its columns], for all d output rows, and stores that fp32 partial; after the one
 //     grid barrier of the call each CTA sums a slice of the output over the partials in CTA order
 //     and rounds it to bf16.
 //
 // The routing weight goes into h' because the down projection is linear, so one partial per CTA
-// covers every expert it touched: out_t = sum_c y_c[t].  The first tile of each CTA c < g0 is a
+// covers every expert it touched: out_t = sum_c y_c[t].  Rounding w * h itself to bf16 instead
+// would move the rounding point off the definition's bf16(h) by up to 2^-9 per element, an error
+// that grows from layer to layer of a model; the low part keeps it below 2^-17.  It takes the
+// MMA's spare token rows 8..15 (N is 16, the tokens at most 8), so the down projection still
+// needs one MMA per k-step.  The first tile of each CTA c < g0 is a
 // shared-chunk tile fixed before routing (tile c), so those CTAs stream it while the tokens are
 // routed.  Roles: warp 0 the TMA producer, warp 1 the MMA issuer, warps 2..9 route every token (in
 // every CTA), warps 2..5 then run the epilogues, and all eight the combine.  The MMA's M side holds
 // 128 weight rows (64 W1 over the 64 W3 rows of the same columns for gate/up; 128 W2 rows for the
-// down projection), its N side the 16 token slots.  All waits are bounded; a time-out sets the
+// down projection), its N side 16 rows: the tokens, then (down projection) their h'_lo.  All waits are bounded; a time-out sets the
 // error word and the kernel unwinds.  The grid barrier needs every CTA resident: one CTA per SM.
 #include <math.h>
 
@@ -45,12 +50,12 @@ using namespace tc;
 using namespace dec;
 
 constexpr int SBK = 64;                        // k-block (elements)
-constexpr int BN = 16;                         // MMA N: token slots
+constexpr int BN = 16;                         // MMA N: 8 token slots (+ 8 rows of h'_lo)
 constexpr int kThreads = 320;                  // 10 warps
 constexpr int kW = 128 * SBK * 2;              // 16 KB weight operand per stage
 constexpr int kAct = BN * SBK * 2;             // 2 KB token tile of a gate/up stage
 constexpr int kStage = kW + kAct;
-constexpr int kHTile = BN * SBK * 2;           // 2 KB: one h' tile (16 tokens x 64 columns)
+constexpr int kHTile = BN * SBK * 2;           // 2 KB: one h' tile, rows t = h'_hi, 8 + t = h'_lo
 constexpr int kSmemMax = 232448;               // 227 KB opt-in dynamic shared memory
 
 // shared-memory tables after the ring and the h' tiles (byte offsets)
@@ -65,7 +70,9 @@ constexpr int kTabRed = kTabXch + BN * 64 * 4;               // f32 [8][32] comb
 constexpr int kTabBytes = (kTabRed + 8 * 32 * 4 + 127) / 128 * 128;
 constexpr int kStagesRaw = (kSmemMax - 1024 - kSliceMaxTiles * kHTile - kTabBytes - 512) / kStage;
 constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-constexpr uint32_t kTmemCols = 64;             // gate/up accumulators 2 x 16, down 2 x 16
+constexpr int kPassTiles = 28;                 // output blocks of 128 rows per down pass
+constexpr int kPassGroups = kPassTiles / 4;    // the epilogue takes a pass's blocks four at a time
+constexpr uint32_t kTmemCols = 512;            // gate/up accumulators 2 x 16, down <= 28 x 16
 constexpr uint32_t kIdesc = idesc_bf16(128, BN);
 constexpr int kSmem = 1024 + kStages * kStage + kSliceMaxTiles * kHTile + kTabBytes + 512;
 static_assert(kStage % 1024 == 0 && kHTile % 1024 == 0, "operands keep 1024-byte alignment");
@@ -77,11 +84,44 @@ struct SMaps {
     CUtensorMap wf[3];    // pool / load buffer 0 / 1 as [pages*d][f], boxes of 128 rows
 };
 
+// Barrier of the G CTAs of a call on one 64-bit counter that every call raises by exactly G
+// (each CTA adds 1 once its partial is written, release): the call's target is the next multiple
+// of G above the value its CTAs read at entry, which some of them may already have raised, never
+// all.  Run by one thread per CTA; bounded: gives up after ~2 s (or when the CTA already
+// aborted, after arriving), raising PMOE_ERR_TIMEOUT.
+__device__ bool count_barrier(unsigned long long* ctr, unsigned long long target, volatile int* abort_flag,
+                              int32_t* err) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+    if (*abort_flag) return false;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((it & 15u) == 0 && (*abort_flag || globaltimer() - t0 > 2000000000ull)) {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                raise_error(err, PMOE_ERR_TIMEOUT);
+            }
+            return false;
+        }
+        __nanosleep(32);
+    }
+}
+
 #ifdef PMOE_SLICE_TRACE
 __device__ unsigned long long g_slice_trace[kFusedMaxGrid * 32];
-#define TRACE(i) (g_slice_trace[blockIdx.x * 32 + (i)] = globaltimer())
+// the time stamp is taken where the macro stands (the clobber keeps it after a preceding barrier)
+__device__ __forceinline__ unsigned long long trace_time() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    return t;
+}
+#define TRACE(i) (g_slice_trace[blockIdx.x * 32 + (i)] = trace_time())
+#define TRACEV(i, v) (g_slice_trace[blockIdx.x * 32 + (i)] = (unsigned long long)(v))
 #else
 #define TRACE(i) ((void)0)
+#define TRACEV(i, v) ((void)0)
 #endif
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -101,18 +141,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(tab + kTabXch);
     float* red = reinterpret_cast<float*>(tab + kTabRed);
     // misc: [0..7] scan scratch, [8] routed experts Ar, [9] abort, [10] TMEM address,
-    //       [11] barrier decision, [12] barrier word at entry, [13] CTAs that work (G'),
-    //       [14] this CTA's tiles
+    //       [11] barrier decision, [12..13] arrival counter at entry (low, high), [14] CTAs
+    //       that work (G'), [15] this CTA's tiles
     const uint32_t bar0 = sbase + kStages * kStage + kSliceMaxTiles * kHTile + kTabBytes;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
     auto gfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
     auto gempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-    auto dfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 4 + a); };
-    auto dempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 6 + a); };
-    const uint32_t route_bar = bar0 + 8u * (2 * kStages + 8);
-    const uint32_t hready_bar = bar0 + 8u * (2 * kStages + 9);
-    const uint32_t mmadone_bar = bar0 + 8u * (2 * kStages + 10);
+    const uint32_t dempty_bar = bar0 + 8u * (2 * kStages + 4);
+    const uint32_t route_bar = bar0 + 8u * (2 * kStages + 5);
+    const uint32_t mmadone_bar = bar0 + 8u * (2 * kStages + 6);
+    // down accumulators of output blocks 4q .. 4q+3 of a pass complete
+    auto dfull_bar = [&](int q) { return bar0 + 8u * (2 * kStages + 7 + q); };
+    auto hready_bar = [&](int j) { return bar0 + 8u * (2 * kStages + 7 + kPassGroups + j); };   // h' tile j written
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 9);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc + 10);
     volatile int* decision = reinterpret_cast<volatile int*>(misc + 11);
@@ -122,7 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int T = args.T, E = args.E, S = args.S;
     const int F64 = args.f / SBK, KB1 = args.d / SBK;
     const int M2 = (args.d + 127) / 128;
-    const uint32_t all_tok = (1u << T) - 1u;   // T <= 16
+    // the down projection's output blocks in passes of at most kPassTiles accumulators
+    const int n_pass = (M2 + kPassTiles - 1) / kPassTiles;
+    const int MP = (M2 + n_pass - 1) / n_pass;
+    const uint32_t all_tok = (1u << T) - 1u;   // T <= 8
     const bool primed_tile = cta < args.g0;     // first tile = shared tile `cta`, known now
 
     if (threadIdx.x == 0) {
@@ -133,12 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(gfull_bar(a), 1);
             mbar_init(gempty_bar(a), 4);
-            mbar_init(dfull_bar(a), 1);
-            mbar_init(dempty_bar(a), 4);
         }
+        for (int q = 0; q < kPassGroups; ++q) mbar_init(dfull_bar(q), 1);
+        mbar_init(dempty_bar, 4);
         mbar_init(route_bar, 1);
-        mbar_init(hready_bar, 1);
         mbar_init(mmadone_bar, 1);
+        for (int j = 0; j < kSliceMaxTiles; ++j) mbar_init(hready_bar(j), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -217,10 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok && !mbar_wait(route_bar, 0, abort_flag, args.err)) ok = false;
             TRACE(2);   // producer: routing known
-            const int Gw = ok ? misc[13] : 1, nt = ok ? misc[14] : 0;
-            for (int j = j0; ok && j < nt; ++j) ok = stream_gu(cta + j * Gw, 0);
-            TRACE(3);   // producer: gate/up loads issued
-            // down projection, output block by output block: 128 W2 rows x this CTA's columns
+            const int Gw = ok ? misc[14] : 1, nt = ok ? misc[15] : 0;
+            // down projection of tile j, pass p: 128 W2 rows of its 64 columns per output block
             int2 l2[kSliceMaxTiles];
             int ftj[kSliceMaxTiles];
             for (int j = 0; ok && j < nt; ++j) {
@@ -228,12 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ftj[j] = u - a * F64;
                 l2[j] = resolve(args, slot_expert_of(a), 2);
             }
-            for (int m = 0; ok && m < M2; ++m) {
-                for (int j = 0; j < nt; ++j) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) {
-                        ok = false;
-                        break;
-                    }
+            auto stream_dn = [&](int p, int j) -> bool {
+                const int m1 = min(M2, (p + 1) * MP);
+                for (int m = p * MP; m < m1; ++m) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.err)) return false;
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, kW);
                     tma_load_2d_hint(sbase + stage * kStage, &maps.wf[l2[j].x], fb, ftj[j] * SBK,
@@ -241,7 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pend[stage] = (int)phase;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
+                return true;
+            };
+            // the gate/up of tile j + 1 goes before the down projection of tile j, which then finds
+            // tile j's h' written
+            for (int j = j0; ok && j < nt; ++j) {
+                ok = stream_gu(cta + j * Gw, 0);
+                if (ok && j >= 1) ok = stream_dn(0, j - 1);
             }
+            TRACE(3);   // producer: gate/up loads issued
+            if (ok && nt > 0) ok = stream_dn(0, nt - 1);
+            for (int p = 1; ok && p < n_pass; ++p)
+                for (int j = 0; ok && j < nt; ++j) ok = stream_dn(p, j);
             TRACE(4);   // producer: all loads issued
             if (!ok) {
                 // wait for this CTA's copies in flight before it may exit
@@ -285,39 +336,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 j0 = 1;
             }
             if (ok && !mbar_wait(route_bar, 0, abort_flag, args.err)) ok = false;
-            const int nt = ok ? misc[14] : 0;
-            for (int j = j0; ok && j < nt; ++j) ok = mma_gu(j);
-            // the down projection needs every h' tile of this CTA
-            if (ok && nt > 0) {
-                ok = mbar_wait(hready_bar, 0, abort_flag, args.err);
-                tc_fence_after();
-            }
-            for (int m = 0; ok && nt > 0 && m < M2; ++m) {
-                const int db = m & 1;
-                if (!mbar_wait(dempty_bar(db), (((uint32_t)m >> 1) & 1u) ^ 1u, abort_flag, args.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d0 = tmem_base + (uint32_t)(2 * BN + db * BN);
-                for (int j = 0; j < nt; ++j) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) {
-                        ok = false;
-                        break;
-                    }
+            const int nt = ok ? misc[15] : 0;
+            // down projection of tile j over the output blocks of pass p, accumulated over the
+            // tiles in TMEM (columns 2 BN + BN * block of the pass)
+            auto mma_dn = [&](int p, int j) -> bool {
+                if (p == 0) {
+                    if (!mbar_wait(hready_bar(j), 0, abort_flag, args.err)) return false;
                     tc_fence_after();
+                } else if (j == 0) {
+                    // the previous pass's accumulators have been read out
+                    if (!mbar_wait(dempty_bar, (uint32_t)(p - 1) & 1u, abort_flag, args.err)) return false;
+                    tc_fence_after();
+                }
+                const uint64_t bd = smem_desc(hbase + (uint32_t)(j * kHTile));
+                const int m1 = min(M2, (p + 1) * MP);
+                for (int m = p * MP; m < m1; ++m) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) return false;
+                    tc_fence_after();
+                    const uint32_t d0 = tmem_base + (uint32_t)(2 * BN + (m - p * MP) * BN);
                     const uint64_t ad = smem_desc(sbase + stage * kStage);
-                    const uint64_t bd = smem_desc(hbase + (uint32_t)(j * kHTile));
+                    // columns t and 8 + t: W2 h'_hi and W2 h'_lo of token t
 #pragma unroll
                     for (int k = 0; k < SBK / 16; ++k)
                         mma_bf16(d0, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc,
                                  (j > 0 || k > 0) ? 1u : 0u);
                     mma_commit(empty_bar(stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    // the last tile completes output blocks four at a time for the epilogue
+                    if (j == nt - 1 && ((m - p * MP) % 4 == 3 || m == m1 - 1)) mma_commit(dfull_bar((m - p * MP) / 4));
                 }
-                if (!ok) break;
-                mma_commit(dfull_bar(db));
+                return true;
+            };
+            for (int j = j0; ok && j < nt; ++j) {
+                ok = mma_gu(j);
+                if (ok && j >= 1) ok = mma_dn(0, j - 1);
             }
+            if (ok && nt > 0) ok = mma_dn(0, nt - 1);
+            for (int p = 1; ok && p < n_pass; ++p)
+                for (int j = 0; ok && j < nt; ++j) ok = mma_dn(p, j);
             TRACE(13);   // MMA: all issued
             // every MMA this thread issued has completed before the TMEM is released
             mma_commit(mmadone_bar);
@@ -338,8 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         pdl_wait_prev();
         pdl_allow_next();
-        // this CTA's barrier word as the previous call left it (read after that call finished)
-        if (leader) misc[12] = (int32_t)ld_relaxed(args.flags + cta);
+        // the arrival counter as the previous call left it (read after that call finished)
+        if (leader) {
+            unsigned long long v;
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(args.arrive) : "memory");
+            misc[12] = (int32_t)(uint32_t)v;
+            misc[13] = (int32_t)(uint32_t)(v >> 32);
+        }
         // routing of all T tokens (each CTA on its own)
         for (int e = gi; e < E; e += kGroupThreads) tok_mask[e] = 0u;
         group_bar();
@@ -359,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane < args.k) atomicOr(&tok_mask[io[lane]], 1u << t);
         }
+        if (leader) TRACE(18);   // this warp's tokens routed
         group_bar();
         // active routed experts in ascending id -> slots S, S+1, ...; shared chunk s -> slot s
         {
@@ -384,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             group_bar();
         }
+        if (leader) TRACE(19);   // slots assigned
         const int A = S + misc[8];
         if (cta == 0) {
             // CTA 0's routing and slot table go to the workspace, where the other paths keep their
@@ -407,14 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nt = 0;
                 *abort_flag = 1;
             }
-            misc[13] = Gw;
-            misc[14] = nt;
+            misc[14] = Gw;
+            misc[15] = nt;
             mbar_arrive(route_bar);
             TRACE(5);   // routing done
+            TRACEV(30, nt);
+            TRACEV(31, primed_tile ? 1 : 0);
         }
         group_bar();
-        const int Gw = misc[13], nt = misc[14];
-        const uint32_t epoch = (uint32_t)misc[12] + 1u;   // this call's barrier target
+        const int Gw = misc[14], nt = misc[15];
+        const unsigned long long entry = (unsigned long long)(uint32_t)misc[12] |
+                                         ((unsigned long long)(uint32_t)misc[13] << 32);
+        const unsigned long long target = (entry / (unsigned)G + 1ull) * (unsigned)G;
 
         if (gw < 4) {
             // ---- epilogues: gate/up accumulators -> h' tiles in shared memory; down
@@ -433,71 +500,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ep_ok) {
                     tmem_ld16(tmem_base + (uint32_t)(g * BN) + ((uint32_t)(quad * 32) << 16), v);
                     tmem_wait_ld();
-                    if (quad >= 2) {
+                    tc_fence_before();
+                }
+                // the accumulator is free for tile j + 2 as soon as it is read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gempty_bar(g));
+                if (ep_ok && quad >= 2) {
 #pragma unroll
-                        for (int t = 0; t < BN; ++t) xch[t * 64 + col] = v[t];
-                    }
+                    for (int t = 0; t < BN; ++t) xch[t * 64 + col] = v[t];
                 }
                 epi_bar();
                 if (quad < 2) {
-                    // h'[t][col] = w_{t,e} * silu(gate) * up, 0 for tokens not routed to e; stored
-                    // as the down MMA's K-major operand (row t, 16-byte chunk col/8 ^ t mod 8)
+                    // h = bf16(silu(gate) * up), the activation the down projection consumes, and
+                    // h' = w_{t,e} * h (0 for tokens not routed to e) carried exactly enough as two
+                    // bf16 parts, h'_hi = bf16(h') and h'_lo = bf16(h' - h'_hi) (17 bits together), so
+                    // the down projection sees the routing weight applied to the rounded h; stored
+                    // as the down MMA's K-major operand (row t and row 8 + t, 16-byte chunk
+                    // col/8 ^ t mod 8)
                     const uint32_t hb = hbase + (uint32_t)(j * kHTile) + (uint32_t)((col & 7) * 2);
 #pragma unroll
-                    for (int t = 0; t < BN; ++t) {
+                    for (int t = 0; t < 8; ++t) {
                         float hv = 0.f;
                         if (ep_ok && (mask >> t & 1u)) {
                             float wt = 1.f;
                             if (a >= S)
                                 for (int q = 0; q < args.k; ++q)
                                     if (ids_s[t * kMaxTopK + q] == e) wt = w_s[t * kMaxTopK + q];
-                            hv = wt * silu_mul(v[t], xch[t * 64 + col]);
+                            hv = wt * bf16_lo(f32_to_bf16_bits(silu_mul(v[t], xch[t * 64 + col])));
                         }
+                        const uint16_t hi = f32_to_bf16_bits(hv);
+                        const uint16_t lo = f32_to_bf16_bits(hv - bf16_lo(hi));
                         const uint32_t addr = hb + (uint32_t)(t * 128) + ((uint32_t)((col >> 3) ^ (t & 7)) << 4);
-                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(f32_to_bf16_bits(hv)) : "memory");
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hi) : "memory");
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + 8u * 128u), "h"(lo) : "memory");
                     }
+                    // h' is read by the tensor cores next: order the stores before the async proxy
+                    fence_proxy_async_shared();
                 }
-                epi_bar();   // xch is reused by the next tile
-                if (ep_ok) tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(gempty_bar(g));
+                epi_bar();   // h' tile j complete; xch free for the next tile
+                if (quad == 0 && lane == 0) mbar_arrive(hready_bar(j));
             }
-            // h' is read by the tensor cores next: order the stores before the async proxy
-            if (quad < 2) fence_proxy_async_shared();
-            epi_bar();
-            if (quad == 0 && lane == 0 && nt > 0) mbar_arrive(hready_bar);
             if (gw == 0 && lane == 0) TRACE(6);   // h' complete
             float* P = args.p2 + (int64_t)cta * T * args.d;
-            for (int m = 0; nt > 0 && m < M2; ++m) {
-                const int db = m & 1;
-                if (ep_ok && !mbar_wait(dfull_bar(db), ((uint32_t)m >> 1) & 1u, abort_flag, args.err)) ep_ok = false;
-                if (ep_ok) {
-                    tc_fence_after();
+            for (int p = 0; nt > 0 && p < n_pass; ++p) {
+                const int m1 = min(M2, (p + 1) * MP);
+                for (int m = p * MP; m < m1; ++m) {
+                    if ((m - p * MP) % 4 == 0) {
+                        if (ep_ok && !mbar_wait(dfull_bar((m - p * MP) / 4), (uint32_t)p & 1u, abort_flag, args.err))
+                            ep_ok = false;
+                        if (ep_ok) tc_fence_after();
+                    }
+                    if (!ep_ok) break;
                     float v[16];
-                    tmem_ld16(tmem_base + (uint32_t)(2 * BN + db * BN) + ((uint32_t)(quad * 32) << 16), v);
+                    tmem_ld16(tmem_base + (uint32_t)(2 * BN + (m - p * MP) * BN) + ((uint32_t)(quad * 32) << 16), v);
                     tmem_wait_ld();
                     const int r = m * 128 + quad * 32 + lane;
                     if (r < args.d) {
 #pragma unroll
-                        for (int t = 0; t < BN; ++t)
-                            if (t < T) __stcg(P + (int64_t)t * args.d + r, v[t]);
+                        for (int t = 0; t < 8; ++t)
+                            if (t < T) __stcg(P + (int64_t)t * args.d + r, v[t] + v[t + 8]);
                     }
-                    tc_fence_before();
                 }
+                if (ep_ok) tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(dempty_bar(db));
+                if (lane == 0) mbar_arrive(dempty_bar);
             }
             if (gw == 0 && lane == 0) TRACE(10);   // partial written
         }
 
-        // the one grid barrier of the call (it also leaves this call's epoch in every CTA's word):
-        // every partial is written
+        // the one grid barrier of the call: every partial is written
         __syncwarp();
         group_bar();
-        if (gw == 0) {
-            const bool ok = !*abort_flag && grid_barrier(args.flags, G, cta, epoch, lane, abort_flag, args.err);
-            if (leader) *decision = ok ? 1 : 0;
-        }
+        if (leader) TRACE(26);   // arriving
+        if (leader) *decision = count_barrier(args.arrive, target, abort_flag, args.err) ? 1 : 0;
         group_bar();
         if (*decision) {
             if (leader) TRACE(11);   // barrier
@@ -510,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rr = r < args.d ? r : args.d - 1;
                 const float* src = args.p2 + (int64_t)t * args.d + rr;
                 const int64_t cstride = (int64_t)T * args.d;
+                // loads clamped to a written partial so that all of them issue at once; only the
+                // partials c < G' are added, in order
                 float s = 0.f;
                 int c = gw;
                 for (; c + 56 < Gw; c += 64) {
@@ -550,7 +627,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_slice_decode(const CUtensorMap& xmap, const CUtensorMap* w64, const CUtensorMap* wf,
                                 const FusedArgs& a, int grid, cudaStream_t s) {
-    if (grid < 1 || grid > kFusedMaxGrid || a.T < 1 || a.T > kSliceMaxTokens || a.g0 < 0 || a.g0 > grid)
+    if (grid < 1 || grid > kFusedMaxGrid || a.T < 1 || a.T > kSliceMaxTokens || kSliceMaxTokens > 8 || a.g0 < 0 ||
+        a.g0 > grid)
         return cudaErrorInvalidValue;
     SMaps m;
     m.x = xmap;
