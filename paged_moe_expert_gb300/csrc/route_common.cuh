@@ -14,8 +14,9 @@ namespace pmoe {
 // order-preserving 32-bit keys (-0 counted as +0, so equal values tie).  Each of the k rounds
 // takes the warp maximum of the lanes' best keys with one redux, then the lowest expert id among
 // the lanes holding it with a second, so the order is (value desc, id asc) exactly; only the
-// winning lane rescans its EPL keys.  Softmax over all E with the top-1 value as the max;
-// optional renormalisation of the k weights (their sum taken across the lanes that hold them).
+// winning lane rescans its EPL keys.  Softmax over all E with the top-1 value as the max, or, with
+// renormalisation, e^(v - max) of the k chosen over their own sum (the same weights: the sum over
+// all E cancels, so it is not formed).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(float v) {
     const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
@@ -74,19 +75,22 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
         }
     }
     const float mx = key_value(top);
-    float s = 0.f;
+    const float ej = lane < k ? expf(key_value(my_key) - mx) : 0.f;
+    float den = 0.f;
+    if (renorm) {
+        // renormalised over the k chosen experts, the softmax's sum over all E cancels:
+        // w_j = e^(v_j - max) / sum over the chosen of e^(v_i - max)
+        den = ej;
+    } else {
 #pragma unroll
-    for (int i = 0; i < EPL; ++i)
-        if (key[i] != 0u) s += expf(key_value(key[i]) - mx);
+        for (int i = 0; i < EPL; ++i)
+            if (key[i] != 0u) den += expf(key_value(key[i]) - mx);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float wj = lane < k ? expf(key_value(my_key) - mx) / s : 0.f;
-    float wsum = wj;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     if (lane < k) {
         ids_out[lane] = my_id;
-        w_out[lane] = renorm ? wj / wsum : wj;
+        w_out[lane] = ej / den;
     }
 }
 
