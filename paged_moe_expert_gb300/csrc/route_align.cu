@@ -292,10 +292,16 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
     for (int e = tid; e < ES; e += NT) {
         int tot = 0, mine = 0;
         if (e < E) {
-            for (int cc = 0; cc < C; ++cc) {
-                const int v = part[(int64_t)cc * ES + e];
-                if (cc < c) mine += v;
-                tot += v;
+            // the C histograms' entries of expert e, eight loads in flight (each an L2 round trip)
+            for (int c0 = 0; c0 < C; c0 += 8) {
+                int v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = c0 + q < C ? part[(int64_t)(c0 + q) * ES + e] : 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (c0 + q < c) mine += v[q];
+                    tot += v[q];
+                }
             }
         } else {
             tot = T;
