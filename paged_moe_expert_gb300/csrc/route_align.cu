@@ -123,6 +123,20 @@ __device__ __forceinline__ void write_unit_list(const int32_t* off, int ES, int 
     }
 }
 
+// Phase time stamps of the one-CTA sort for performance work (compiled in only with
+// -DPMOE_ALIGN_TRACE): globaltimer readings by thread 0 at the milestones named where ATRACE is used.
+#ifdef PMOE_ALIGN_TRACE
+__device__ unsigned long long g_align_trace[16];
+__device__ __forceinline__ unsigned long long atrace_time() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    return t;
+}
+#define ATRACE(i) do { if (threadIdx.x == 0) g_align_trace[(i)] = atrace_time(); } while (0)
+#else
+#define ATRACE(i) ((void)0)
+#endif
+
 __device__ __forceinline__ void align_block(
     const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
@@ -137,8 +151,10 @@ __device__ __forceinline__ void align_block(
     const int64_t NR = (int64_t)T * k;
     const int64_t NP = (int64_t)T * (k + S);
 
+    ATRACE(0);   // start
     for (int i = tid; i < kAlignWarps * ES; i += NT) cw[i] = 0;
     __syncthreads();
+    ATRACE(1);   // counters zeroed
 
     const int64_t seg = (NR + kAlignWarps - 1) / kAlignWarps;
     const int64_t s0 = (int64_t)w * seg;
@@ -149,6 +165,7 @@ __device__ __forceinline__ void align_block(
         atomicAdd(&cw[w * ES + e], 1);
     }
     __syncthreads();
+    ATRACE(2);   // counted
 
     for (int e = tid; e < ES; e += NT) {
         int c = 0;
@@ -160,6 +177,7 @@ __device__ __forceinline__ void align_block(
         cnt[e] = e < E ? c : T;
     }
     __syncthreads();
+    ATRACE(3);   // per-warp prefix
 
     if (w == 0) {  // padded exclusive scan over experts
         const int per = (ES + 31) / 32;
@@ -181,6 +199,7 @@ __device__ __forceinline__ void align_block(
         if (lane == 31) off[ES] = incl;
     }
     __syncthreads();
+    ATRACE(4);   // offsets
 
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int64_t base = s0; base < s1; base += 32) {
@@ -198,12 +217,14 @@ __device__ __forceinline__ void align_block(
         if (valid && (__ffs(peers) - 1) == lane) cw[w * ES + e] += __popc(peers);
         __syncwarp();
     }
+    ATRACE(5);   // routed pairs placed
     for (int64_t idx = tid; idx < (int64_t)S * T; idx += NT) {
         const int s = (int)(idx / T), t = (int)(idx % T);
         const int pos = off[E + s] + t;
         sorted_ids[pos] = (int32_t)(NR + idx);
         inv[NR + idx] = pos;
     }
+    ATRACE(6);   // shared pairs placed
     for (int e = tid; e < ES; e += NT) {
         const int o = off[e], c = cnt[e], end = off[e + 1];
         for (int r = o + c; r < end; ++r) sorted_ids[r] = (int32_t)NP;
@@ -213,6 +234,7 @@ __device__ __forceinline__ void align_block(
                 rs.block_rows[b] = min(block_m, o + c - b * block_m);
     }
     if (tid == 0) meta[kMetaNPadded] = off[ES];
+    ATRACE(7);   // pads and block map
     if (rs.units) {
         __syncthreads();   // the per-warp counters are free: they hold the locations now
         resolve_all(rs, E, ES, cnt, cw, tid, NT);
@@ -226,6 +248,7 @@ __device__ __forceinline__ void align_block(
             rs.loc[idx] = cnt[e] > 0 ? resolve_loc(rs, E, e, j) : ExpertLoc{-1, -1};
         }
     }
+    ATRACE(8);   // resolved
 }
 
 __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
@@ -451,9 +474,11 @@ __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
         const int idx = tid + i * NT;
         tv[i] = idx < ntab ? (idx < E ? rs.buf_slot[idx] : rs.page_table[idx - E]) : 0;
     }
+    ATRACE(9);   // prep: tables loading, routing starts
     for (int t = warp; t < T; t += kAlignWarps)
         route_token<EPL>(logits + (int64_t)t * E, E, k, renorm, lane, s_ids + t * k,
                          wout + (int64_t)t * k);
+    ATRACE(10);   // prep: thread 0's warp routed
 #pragma unroll
     for (int i = 0; i < kPrepTabPerThread; ++i) {
         const int idx = tid + i * NT;
@@ -475,7 +500,14 @@ __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
         const int NP = T * (k + S);
         for (int i = warp; i < NP; i += kAlignWarps) gather_pair(hidden, inv, i, T, k, d, lane, x);
     }
+    ATRACE(11);   // prep: rows gathered
 }
+
+#ifdef PMOE_ALIGN_TRACE
+extern "C" int pmoe_align_trace_read(unsigned long long* host) {
+    return (int)cudaMemcpyFromSymbol(host, g_align_trace, sizeof(unsigned long long) * 16);
+}
+#endif
 
 static size_t align_smem_bytes(int ES) { return sizeof(int32_t) * (size_t)align_words(ES); }
 

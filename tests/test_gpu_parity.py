@@ -126,9 +126,10 @@ def test_output_independent_of_placement(path):
     assert_close(outs[0], ref["out_bf16"])
 
 
-def test_bad_page_sets_device_error():
+@pytest.mark.parametrize("T", [16, 4])   # the fused and the column-slice decode kernels
+def test_bad_page_sets_device_error(T):
     cfg = syn.CONFIGS["tiny"]
-    L = setup_layer(cfg, 16)
+    L = setup_layer(cfg, T)
     pt = L.page_table.clone()
     ids, _ = oracle.route(L.logits_np, cfg.k, cfg.renormalize)
     e = int(next(x for x in ids.reshape(-1) if not L.placement.buffered[x]))
