@@ -254,7 +254,12 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         return fail(PMOE_ERR_UNSUPPORTED, "the fused decode kernel takes at most 32 tokens");
     const int dgrid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;   // decode kernels
     int slice_g0 = 0, slice_tiles = 0;
-    const bool slice_ok = slice_fit(D, T, dgrid, &slice_g0, &slice_tiles);
+    bool slice_ok = false;
+    if (T >= 1 && T <= kSliceMaxTokens) {   // worked out at plan creation
+        slice_ok = P->slice_fits[T] != 0;
+        slice_g0 = P->slice_g0[T];
+        slice_tiles = P->slice_tiles[T];
+    }
     if (path == PMOE_PATH_SLICE && !slice_ok)
         return fail(PMOE_ERR_UNSUPPORTED,
                     "the column-slice decode kernel takes at most 8 tokens and 12 column tiles per SM");
@@ -583,6 +588,12 @@ pmoe_status pmoe_plan_create(const pmoe_layer_desc* desc, const void* page_pool,
     P->path = PMOE_PATH_AUTO;
     cudaError_t e = cudaGetDevice(&P->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+    if (e == cudaSuccess) {
+        // the column-slice kernel's fit depends only on the layer, T and the grid
+        const int dgrid = P->num_sms < kFusedMaxGrid ? P->num_sms : kFusedMaxGrid;
+        for (int t = 1; t <= kSliceMaxTokens; ++t)
+            P->slice_fits[t] = slice_fit(*desc, t, dgrid, &P->slice_g0[t], &P->slice_tiles[t]) ? 1 : 0;
+    }
     // one allocation of device words: the error word, the fused kernel's barrier words and tiles
     P->words_bytes = plan_words_bytes(*desc);
     if (e == cudaSuccess) e = cudaMalloc(&P->d_error, P->words_bytes);

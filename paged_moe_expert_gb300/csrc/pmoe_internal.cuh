@@ -65,6 +65,10 @@ struct Plan {
     int last_path, last_kernels, last_launches;  // what the last forward ran
     int last_T, last_block_m;                    // its token count and sorted block size
     int num_sms;
+    // column-slice decode kernel, per token count 1..kSliceMaxTokens (set at plan creation):
+    // whether every routing fits it, its g0 and the most 64-column tiles a CTA can get
+    int8_t slice_fits[kSliceMaxTokens + 1];
+    int slice_g0[kSliceMaxTokens + 1], slice_tiles[kSliceMaxTokens + 1];
     CUtensorMap tm_rows_d[3];  // pool / buf0 / buf1 viewed as [pages * f, d]   (W1, W3 pages)
     CUtensorMap tm_rows_d64[3];  // the same views with 64-row boxes (stacked gate/up tiles)
     CUtensorMap tm_rows_f[3];  // pool / buf0 / buf1 viewed as [pages * d, f]   (W2 pages)

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t all_tok = (1u << T) - 1u;   // T <= 8
     const bool primed_tile = cta < args.g0;     // first tile = shared tile `cta`, known now
 
+    if (threadIdx.x == 0) TRACE(25);   // entry
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
@@ -620,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
                      : "memory");
+        if (lane == 0) TRACE(27);   // TMEM released
     }
 }
 
