@@ -82,8 +82,8 @@ typedef struct pmoe_plan* pmoe_plan_t;
 
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
-    PMOE_PATH_AUTO = 0,   /* SLICE up to 8 tokens while a routing leaves at most 8 column tiles
-                             per SM; else FUSED up to 32 tokens (E <= 128) or 16 tokens
+    PMOE_PATH_AUTO = 0,   /* SLICE up to 16 tokens while a routing leaves at most 8 column
+                             tiles per SM; else FUSED up to 32 tokens (E <= 128) or 16 tokens
                              (E > 128); above, by routed tokens per expert T*k/E: <= 24
                              TC_DECODE, >= 64 TC2 when E <= 128, else TC */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
@@ -97,7 +97,7 @@ typedef enum {
     PMOE_PATH_FUSED = 5,    /* T <= 32 only: the whole layer in one persistent tcgen05 kernel
                                (one CTA per SM) whose weight streams are split evenly over the
                                SMs; see moe_paged_forward for what it requires of the caller */
-    PMOE_PATH_SLICE = 6     /* T <= 8 only: the whole layer in one persistent tcgen05 kernel
+    PMOE_PATH_SLICE = 6     /* T <= 16 only: the whole layer in one persistent tcgen05 kernel
                                whose CTAs each own whole 64-column tiles of the intermediate
                                dimension (gate/up, SiLU-and-mul and their slice of the down
                                projection, no cross-CTA hand-off before the final sum); refused
@@ -160,7 +160,7 @@ size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens);
  * workspace).  So those four must not be written by a kernel of the same stream that triggers
  * its dependents early (no kernel of this library writes them; ordinary kernels and copies are
  * complete before the next launch starts).
- * The fused and column-slice decode paths (T <= 32, T <= 8) synchronise their CTAs through words
+ * The fused and column-slice decode paths (T <= 32, T <= 16) synchronise their CTAs through words
  * that the plan owns, so forward calls of one plan must not overlap on the GPU (the plan's error
  * word is shared the same way).  Their waits give up after about 2 s with PMOE_ERR_TIMEOUT in the error word (only if the
  * GPU cannot hold one CTA per SM for this call, e.g. when other work occupies SMs indefinitely);

@@ -74,11 +74,12 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
 // hundreds of small experts most experts end in an odd block, which costs a CTA pair as much as
 // a pair of blocks).  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
 constexpr int kSwapMaxTokensPerExpert = 24;
-// The column-slice decode kernel up to 8 tokens while a routing leaves at most 8 column tiles per
-// SM (measured on GB300 against the fused kernel: ahead from 1 to 8 tokens on the Qwen1.5- and
-// Qwen3-Next-shaped layers and at 1 and 2 on the Mixtral-shaped one; behind once a CTA streams
-// twelve tiles, where the fused kernel's even k-block split keeps more bytes in flight per SM).
-constexpr int kSliceAutoTokens = 8;
+// The column-slice decode kernel up to 16 tokens while a routing leaves at most 8 column tiles
+// per SM (measured on GB300 against the fused kernel: ahead from 1 to 12 tokens on the Qwen1.5-
+// and Qwen3-Next-shaped layers and at 1 and 2 on the Mixtral-shaped one, level at 16; behind
+// once a CTA streams more tiles, where the fused kernel's even k-block split keeps more bytes in
+// flight per SM).
+constexpr int kSliceAutoTokens = 16;
 constexpr int kSliceAutoTiles = 8;
 constexpr int kPairMinTokensPerExpert = 64;
 constexpr int kPairMaxExperts = 128;
@@ -262,7 +263,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
     }
     if (path == PMOE_PATH_SLICE && !slice_ok)
         return fail(PMOE_ERR_UNSUPPORTED,
-                    "the column-slice decode kernel takes at most 8 tokens and 12 column tiles per SM");
+                    "the column-slice decode kernel takes at most 16 tokens and 12 column tiles per SM");
     if (path == PMOE_PATH_AUTO) {
         const int64_t routed = (int64_t)T * D.top_k;   // routed tokens; per expert: routed / E
         // the fused decode kernel up to 32 tokens for layers of at most 128 experts and up to 16

@@ -21,7 +21,7 @@ constexpr int kStreamMaxBlockM = 16;    // weight-streaming path: rows per sorte
 constexpr int kStreamKChunk = 2048;     // weight-streaming down GEMM: K (= f) chunk per CTA
 constexpr int kFusedMaxTokens = 32;     // fused decode kernel: tokens per call (MMA N <= 32)
 constexpr int kFusedMaxGrid = 256;      // fused decode kernel: CTAs (one per SM)
-constexpr int kSliceMaxTokens = 8;      // column-slice decode kernel: tokens per call (MMA N = 16)
+constexpr int kSliceMaxTokens = 16;     // column-slice decode kernel: tokens per call
 constexpr int kSliceMaxTiles = 12;      // column-slice decode kernel: 64-column tiles per CTA
 
 // Where one expert matrix lives: map 0 = pool, 1 = load buffer 0, 2 = load buffer 1; `page` is
@@ -282,7 +282,7 @@ cudaError_t launch_tc_gemm2sm(int mode, bool contig, const CUtensorMap& act, con
 
 // Fused decode kernel (tc_fused.cu): routing, both projections and the combine of T <= 32
 // tokens in one persistent launch of `grid` CTAs (one per SM); bn = 16 or 32 >= T.  The
-// column-slice decode kernel (tc_slice.cu, T <= 8) takes the same arguments: p2 holds its
+// column-slice decode kernel (tc_slice.cu, T <= 16) takes the same arguments: p2 holds its
 // per-CTA partials [grid][T][d] fp32, g0 the CTAs whose first tile (a shared-chunk tile) is
 // streamed before routing, arrive its barrier counter, and p1, h, flags, ucnt, hflag, p1_base1
 // are unused (the fused kernel does not use arrive).

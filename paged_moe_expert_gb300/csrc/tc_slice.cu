@@ -1,4 +1,4 @@
-// The paged MoE layer for a few tokens (T <= 8) in one persistent kernel whose CTAs own whole
+// The paged MoE layer for a few tokens (T <= 16) in one persistent kernel whose CTAs own whole
 // columns of the intermediate dimension.
 //
 // The layer is Rimuru's paged fused MoE (paper-daily.com/en, "Expert weights are scattered across
@@ -28,13 +28,14 @@
 // covers every expert it touched: out_t = sum_c y_c[t].  Rounding w * h itself to bf16 instead
 // would move the rounding point off the definition's bf16(h) by up to 2^-9 per element, an error
 // that grows from layer to layer of a model; the low part keeps it below 2^-17.  It takes the
-// MMA's spare token rows 8..15 (N is 16, the tokens at most 8), so the down projection still
-// needs one MMA per k-step.  The first tile of each CTA c < g0 is a
+// down MMA's rows after the tokens' own (N = 2 MT for at most MT = 8 or 16 tokens, one kernel
+// instance each), so the down projection still needs one MMA per k-step.  The first tile of each CTA c < g0 is a
 // shared-chunk tile fixed before routing (tile c), so those CTAs stream it while the tokens are
 // routed.  Roles: warp 0 the TMA producer, warp 1 the MMA issuer, warps 2..9 route every token (in
 // every CTA), warps 2..5 then run the epilogues, and all eight the combine.  The MMA's M side holds
 // 128 weight rows (64 W1 over the 64 W3 rows of the same columns for gate/up; 128 W2 rows for the
-// down projection), its N side 16 rows: the tokens, then (down projection) their h'_lo.  All waits are bounded; a time-out sets the
+// down projection), its N side the 16 token slots (gate/up) or the MT tokens' h'_hi rows followed
+// by their h'_lo rows (down projection).  All waits are bounded; a time-out sets the
 // error word and the kernel unwinds.  The grid barrier needs every CTA resident: one CTA per SM.
 #include <math.h>
 
@@ -50,12 +51,11 @@ using namespace tc;
 using namespace dec;
 
 constexpr int SBK = 64;                        // k-block (elements)
-constexpr int BN = 16;                         // MMA N: 8 token slots (+ 8 rows of h'_lo)
+constexpr int BN = 16;                         // gate/up MMA N: token slots
 constexpr int kThreads = 320;                  // 10 warps
 constexpr int kW = 128 * SBK * 2;              // 16 KB weight operand per stage
 constexpr int kAct = BN * SBK * 2;             // 2 KB token tile of a gate/up stage
 constexpr int kStage = kW + kAct;
-constexpr int kHTile = BN * SBK * 2;           // 2 KB: one h' tile, rows t = h'_hi, 8 + t = h'_lo
 constexpr int kSmemMax = 232448;               // 227 KB opt-in dynamic shared memory
 
 // shared-memory tables after the ring and the h' tiles (byte offsets)
@@ -68,15 +68,24 @@ constexpr int kTabMisc = kTabW + 1024;                       // i32 [64]
 constexpr int kTabXch = kTabMisc + 256;                      // f32 [16][64] up -> gate lanes
 constexpr int kTabRed = kTabXch + BN * 64 * 4;               // f32 [8][32] combine sums
 constexpr int kTabBytes = (kTabRed + 8 * 32 * 4 + 127) / 128 * 128;
-constexpr int kStagesRaw = (kSmemMax - 1024 - kSliceMaxTiles * kHTile - kTabBytes - 512) / kStage;
-constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-constexpr int kPassTiles = 28;                 // output blocks of 128 rows per down pass
-constexpr int kPassGroups = kPassTiles / 4;    // the epilogue takes a pass's blocks four at a time
-constexpr uint32_t kTmemCols = 512;            // gate/up accumulators 2 x 16, down <= 28 x 16
+constexpr uint32_t kTmemCols = 512;            // gate/up accumulators 2 x 16, down <= 480 columns
 constexpr uint32_t kIdesc = idesc_bf16(128, BN);
-constexpr int kSmem = 1024 + kStages * kStage + kSliceMaxTiles * kHTile + kTabBytes + 512;
-static_assert(kStage % 1024 == 0 && kHTile % 1024 == 0, "operands keep 1024-byte alignment");
-static_assert(kSmem <= kSmemMax, "shared memory budget");
+
+// The sizes that follow from MT, the most tokens a kernel instance takes (8 or 16).
+template <int MT>
+struct SCfg {
+    static constexpr int DN = 2 * MT;                   // down MMA N: MT rows of h'_hi, MT of h'_lo
+    static constexpr int HTILE = DN * SBK * 2;          // one h' tile (2 or 4 KB)
+    static constexpr int PASS = MT == 8 ? 28 : 14;      // output blocks per down pass: 32 + PASS*DN <= 480
+    static constexpr int GROUPS = (PASS + 3) / 4;       // the epilogue takes a pass's blocks four at a time
+    static constexpr int STAGES_RAW = (kSmemMax - 1024 - kSliceMaxTiles * HTILE - kTabBytes - 512) / kStage;
+    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+    static constexpr uint32_t IDESC_DN = idesc_bf16(128, DN);
+    static constexpr int SMEM = 1024 + STAGES * kStage + kSliceMaxTiles * HTILE + kTabBytes + 512;
+    static_assert(kStage % 1024 == 0 && HTILE % 1024 == 0, "operands keep 1024-byte alignment");
+    static_assert(SMEM <= kSmemMax, "shared memory budget");
+    static_assert(32 + PASS * DN <= (int)kTmemCols, "tensor memory budget");
+};
 
 struct SMaps {
     CUtensorMap x;        // hidden [T][d], boxes of 16 rows x 64
@@ -124,8 +133,15 @@ __device__ __forceinline__ unsigned long long trace_time() {
 #define TRACEV(i, v) ((void)0)
 #endif
 
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     slice_decode_kernel(const __grid_constant__ SMaps maps, const FusedArgs args) {
+    using C = SCfg<MT>;
+    constexpr int kStages = C::STAGES;
+    constexpr int kHTile = C::HTILE;
+    constexpr int kPassTiles = C::PASS;
+    constexpr int kPassGroups = C::GROUPS;
+    constexpr int DN = C::DN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -166,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the down projection's output blocks in passes of at most kPassTiles accumulators
     const int n_pass = (M2 + kPassTiles - 1) / kPassTiles;
     const int MP = (M2 + n_pass - 1) / n_pass;
-    const uint32_t all_tok = (1u << T) - 1u;   // T <= 8
+    const uint32_t all_tok = (1u << T) - 1u;   // T <= MT <= 16
     const bool primed_tile = cta < args.g0;     // first tile = shared tile `cta`, known now
 
     if (threadIdx.x == 0) TRACE(25);   // entry
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && !mbar_wait(route_bar, 0, abort_flag, args.err)) ok = false;
             const int nt = ok ? misc[15] : 0;
             // down projection of tile j over the output blocks of pass p, accumulated over the
-            // tiles in TMEM (columns 2 BN + BN * block of the pass)
+            // tiles in TMEM (columns 2 BN + DN * block of the pass)
             auto mma_dn = [&](int p, int j) -> bool {
                 if (p == 0) {
                     if (!mbar_wait(hready_bar(j), 0, abort_flag, args.err)) return false;
@@ -354,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = p * MP; m < m1; ++m) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, args.err)) return false;
                     tc_fence_after();
-                    const uint32_t d0 = tmem_base + (uint32_t)(2 * BN + (m - p * MP) * BN);
+                    const uint32_t d0 = tmem_base + (uint32_t)(2 * BN + (m - p * MP) * DN);
                     const uint64_t ad = smem_desc(sbase + stage * kStage);
-                    // columns t and 8 + t: W2 h'_hi and W2 h'_lo of token t
+                    // columns t and MT + t: W2 h'_hi and W2 h'_lo of token t
 #pragma unroll
                     for (int k = 0; k < SBK / 16; ++k)
-                        mma_bf16(d0, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc,
+                        mma_bf16(d0, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), C::IDESC_DN,
                                  (j > 0 || k > 0) ? 1u : 0u);
                     mma_commit(empty_bar(stage));
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -516,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // h' = w_{t,e} * h (0 for tokens not routed to e) carried exactly enough as two
                     // bf16 parts, h'_hi = bf16(h') and h'_lo = bf16(h' - h'_hi) (17 bits together), so
                     // the down projection sees the routing weight applied to the rounded h; stored
-                    // as the down MMA's K-major operand (row t and row 8 + t, 16-byte chunk
+                    // as the down MMA's K-major operand (row t and row MT + t, 16-byte chunk
                     // col/8 ^ t mod 8)
                     const uint32_t hb = hbase + (uint32_t)(j * kHTile) + (uint32_t)((col & 7) * 2);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
+                    for (int t = 0; t < MT; ++t) {
                         float hv = 0.f;
                         if (ep_ok && (mask >> t & 1u)) {
                             float wt = 1.f;
@@ -533,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint16_t lo = f32_to_bf16_bits(hv - bf16_lo(hi));
                         const uint32_t addr = hb + (uint32_t)(t * 128) + ((uint32_t)((col >> 3) ^ (t & 7)) << 4);
                         asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hi) : "memory");
-                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + 8u * 128u), "h"(lo) : "memory");
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr + (uint32_t)(MT * 128)), "h"(lo) : "memory");
                     }
                     // h' is read by the tensor cores next: order the stores before the async proxy
                     fence_proxy_async_shared();
@@ -552,14 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ep_ok) tc_fence_after();
                     }
                     if (!ep_ok) break;
-                    float v[16];
-                    tmem_ld16(tmem_base + (uint32_t)(2 * BN + (m - p * MP) * BN) + ((uint32_t)(quad * 32) << 16), v);
+                    float v[DN];
+                    const uint32_t ta = tmem_base + (uint32_t)(2 * BN + (m - p * MP) * DN) + ((uint32_t)(quad * 32) << 16);
+#pragma unroll
+                    for (int c0 = 0; c0 < DN; c0 += 16) tmem_ld16(ta + (uint32_t)c0, *reinterpret_cast<float(*)[16]>(v + c0));
                     tmem_wait_ld();
                     const int r = m * 128 + quad * 32 + lane;
                     if (r < args.d) {
 #pragma unroll
-                        for (int t = 0; t < 8; ++t)
-                            if (t < T) __stcg(P + (int64_t)t * args.d + r, v[t] + v[t + 8]);
+                        for (int t = 0; t < MT; ++t)
+                            if (t < T) __stcg(P + (int64_t)t * args.d + r, v[t] + v[t + MT]);
                     }
                 }
                 if (ep_ok) tc_fence_before();
@@ -629,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_slice_decode(const CUtensorMap& xmap, const CUtensorMap* w64, const CUtensorMap* wf,
                                 const FusedArgs& a, int grid, cudaStream_t s) {
-    if (grid < 1 || grid > kFusedMaxGrid || a.T < 1 || a.T > kSliceMaxTokens || kSliceMaxTokens > 8 || a.g0 < 0 ||
+    if (grid < 1 || grid > kFusedMaxGrid || a.T < 1 || a.T > kSliceMaxTokens || kSliceMaxTokens > 16 || a.g0 < 0 ||
         a.g0 > grid)
         return cudaErrorInvalidValue;
     SMaps m;
@@ -638,10 +656,16 @@ cudaError_t launch_slice_decode(const CUtensorMap& xmap, const CUtensorMap* w64,
         m.w64[i] = w64[i];
         m.wf[i] = wf[i];
     }
-    static std::atomic<unsigned long long> attr{0};
-    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(slice_decode_kernel), kSmem, &attr);
+    if (a.T <= 8) {
+        static std::atomic<unsigned long long> attr8{0};
+        cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(slice_decode_kernel<8>), SCfg<8>::SMEM, &attr8);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(slice_decode_kernel<8>, dim3(grid), dim3(kThreads), SCfg<8>::SMEM, s, m, a);
+    }
+    static std::atomic<unsigned long long> attr16{0};
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(slice_decode_kernel<16>), SCfg<16>::SMEM, &attr16);
     if (e != cudaSuccess) return e;
-    return launch_pdl(slice_decode_kernel, dim3(grid), dim3(kThreads), kSmem, s, m, a);
+    return launch_pdl(slice_decode_kernel<16>, dim3(grid), dim3(kThreads), SCfg<16>::SMEM, s, m, a);
 }
 
 #ifdef PMOE_SLICE_TRACE

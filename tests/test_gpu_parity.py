@@ -77,7 +77,7 @@ SMALL = [
 PATHS = [pm.PATH_STREAM, pm.PATH_TC, pm.PATH_TC_DECODE, pm.PATH_TC2, pm.PATH_FUSED, pm.PATH_SLICE]
 PATH_IDS = ["stream", "tc", "tc_decode", "tc2", "fused", "slice"]
 FUSED_MAX_T = 32
-SLICE_MAX_T = 8
+SLICE_MAX_T = 16
 DECODE_PATHS = (pm.PATH_FUSED, pm.PATH_SLICE)   # no sort: active slots instead
 
 
@@ -90,7 +90,7 @@ def serves(path, T):
 @pytest.mark.parametrize("T", [1, 3, 16, 17, 32, 37, 128, 300])
 def test_forward_matches_oracle(cfg, T, path):
     if not serves(path, T):
-        pytest.skip("the decode kernels take at most 32 (fused) or 8 (column-slice) tokens")
+        pytest.skip("the decode kernels take at most 32 (fused) or 16 (column-slice) tokens")
     if path != pm.PATH_FUSED and T in (17, 32):
         pytest.skip("token counts that only change the fused kernel's tile width")
     L = setup_layer(cfg, T)
@@ -108,7 +108,7 @@ def test_output_independent_of_placement(path):
     cfg = syn.custom_config("inv", d=256, f=256, E=12, k=3, S=1, n_buffered=4, slots_per_buffer=6,
                             num_pages=60)
     w = syn.make_weights(cfg)
-    T = 7 if path == pm.PATH_SLICE else 29   # every path serves it
+    T = 13 if path == pm.PATH_SLICE else 29   # every path serves it
     outs = []
     for pseed, bidx, nb in [(1, 0, 4), (2, 0, 4), (3, 1, 4), (4, 1, 6), (5, 0, 0)]:
         L = setup_layer(cfg, T, placement_seed=pseed, buffer_index=bidx, n_buffered=nb, weights=w)
@@ -156,10 +156,10 @@ def test_invalid_arguments_rejected():
 
 def test_auto_path_by_token_count():
     cfg = syn.CONFIGS["tiny"]
-    # up to 8 tokens the column-slice kernel, up to 32 the fused decode kernel; then by T*k/E (tiny:
-    # E=8, k=2 -> T/4): small-batch kernels up to T=96, single-CTA blocks below T=256, pairs from
-    # T=256
-    for T, want in [(1, pm.PATH_SLICE), (8, pm.PATH_SLICE), (9, pm.PATH_FUSED), (16, pm.PATH_FUSED),
+    # up to 16 tokens the column-slice kernel (tiny: one column tile per CTA at most), up to 32 the
+    # fused decode kernel; then by T*k/E (tiny: E=8, k=2 -> T/4): small-batch kernels up to T=96,
+    # single-CTA blocks below T=256, pairs from T=256
+    for T, want in [(1, pm.PATH_SLICE), (8, pm.PATH_SLICE), (16, pm.PATH_SLICE), (17, pm.PATH_FUSED),
                     (32, pm.PATH_FUSED),
                     (33, pm.PATH_TC_DECODE), (96, pm.PATH_TC_DECODE), (97, pm.PATH_TC),
                     (255, pm.PATH_TC), (256, pm.PATH_TC2), (4096, pm.PATH_TC2)]:
@@ -314,7 +314,7 @@ def test_forward_at_maximum_sizes(T, path):
     routing with 32 logits per lane, the widest sort and every kernel family against the oracle,
     with the routing state of the call read back bit-exact."""
     if not serves(path, T):
-        pytest.skip("the decode kernels take at most 32 (fused) or 8 (column-slice) tokens")
+        pytest.skip("the decode kernels take at most 32 (fused) or 16 (column-slice) tokens")
     cfg = MAXCFG
     L = setup_layer(cfg, T)
     L.plan.set_path(path)
@@ -344,9 +344,9 @@ def test_empty_batch_writes_nothing():
     assert L.plan.device_error() == 0
 
 
-def test_slice_rejects_more_than_8_tokens():
+def test_slice_rejects_more_than_16_tokens():
     cfg = syn.CONFIGS["tiny"]
-    L = setup_layer(cfg, 9)
+    L = setup_layer(cfg, 17)
     L.plan.set_path(pm.PATH_SLICE)
     with pytest.raises(pm.PmoeError) as ei:
         L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
@@ -363,7 +363,8 @@ def test_slice_and_fused_calls_share_one_plan():
     ws = pm.alloc_workspace(L.desc, 32)
     seen = {}
     for T, path in [(1, pm.PATH_SLICE), (16, pm.PATH_FUSED), (5, pm.PATH_SLICE), (8, pm.PATH_SLICE),
-                    (32, pm.PATH_FUSED), (1, pm.PATH_SLICE), (5, pm.PATH_SLICE), (1, pm.PATH_FUSED)]:
+                    (32, pm.PATH_FUSED), (16, pm.PATH_SLICE), (1, pm.PATH_SLICE), (11, pm.PATH_SLICE),
+                    (5, pm.PATH_SLICE), (1, pm.PATH_FUSED)]:
         h, lg = syn.make_tokens(cfg, T)
         L.plan.set_path(path)
         out = out_bits(L.plan.forward(pl._bf16(h).cuda(), torch.from_numpy(lg).cuda(), L.page_table,
@@ -376,8 +377,9 @@ def test_slice_and_fused_calls_share_one_plan():
         seen[(T, path)] = out
 
 
-@pytest.mark.parametrize("name,T", [("qwen15", 1), ("qwen15", 4), ("qwen15", 8), ("qwen3next", 1),
-                                    ("qwen3next", 8), ("mixtral", 1), ("mixtral", 4)])
+@pytest.mark.parametrize("name,T", [("qwen15", 1), ("qwen15", 4), ("qwen15", 8), ("qwen15", 16),
+                                    ("qwen3next", 1), ("qwen3next", 8), ("qwen3next", 12), ("qwen3next", 16),
+                                    ("mixtral", 1), ("mixtral", 4)])
 def test_slice_tile_counts_per_cta(name, T):
     """The column-slice kernel on the measured layer shapes, from one tile per working CTA
     (Qwen3-Next-shaped, one token: 88 tiles on 88 CTAs) to twelve (Mixtral-shaped, 4 tokens),

@@ -151,6 +151,7 @@ def test_forward_routing_state_mixtral_8192():
     ("mixtral", 32, pm.PATH_FUSED),
     ("tiny", 3, pm.PATH_SLICE),
     ("qwen15", 8, pm.PATH_SLICE),
+    ("qwen15", 16, pm.PATH_SLICE),
     ("qwen3next", 1, pm.PATH_SLICE),
     ("qwen3next", 8, pm.PATH_SLICE),
     ("mixtral", 2048, pm.PATH_TC2),
@@ -182,7 +183,7 @@ def test_routing_view_refuses_another_token_count():
     assert ei.value.status == pm._lib.ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("T", [1, 2, 5, 8])
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 16])
 @pytest.mark.parametrize("name", ["qwen15", "qwen3next"])
 def test_tied_logits_on_the_column_slice_path(name, T):
     """The column-slice kernel's own routing (every CTA routes all tokens) on integer logits,
