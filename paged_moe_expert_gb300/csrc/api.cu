@@ -85,9 +85,11 @@ constexpr int kPairMinTokensPerExpert = 64;
 constexpr int kPairMaxExperts = 128;
 constexpr int kPrepSmallMaxTokens = 128;
 // The one-CTA prep routes every token on one SM; its routing work grows with tokens x logits per
-// lane x k.  Past this (the Qwen1.5-MoE-shaped layer at 128 tokens) the routing kernel's many CTAs
-// and a separate sort win: 512 experts top-10 at 64 tokens took 36 us in the prep.
-constexpr int64_t kPrepSmallRouteWork = 128 * 2 * 4;
+// lane x k.  Past this the routing kernel's many CTAs and a separate sort win (measured on GB300:
+// the Qwen1.5-MoE-shaped layer at 128 tokens 22.4 us in the prep against 6.1 + 12.3 us, at 40
+// and 64 tokens 1-2 us; 512 experts top-10 at 64 tokens took 36 us in the prep); the
+// Mixtral-shaped layer stays in the prep up to 128 tokens.
+constexpr int64_t kPrepSmallRouteWork = 256;
 
 static bool use_prep_small(int T, int E, int k) {
     return T <= kPrepSmallMaxTokens && (int64_t)T * ((E + 31) / 32) * k <= kPrepSmallRouteWork;

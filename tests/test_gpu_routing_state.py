@@ -145,7 +145,8 @@ def test_forward_routing_state_mixtral_8192():
     ("tiny", 4096, pm.PATH_TC2),        # routing kernel + multi-CTA sort writing units
     ("qwen15", 16, pm.PATH_STREAM),     # prep with shared chunks
     ("qwen15", 4096, pm.PATH_TC),       # multi-CTA sort with valid-row counts
-    ("qwen3next", 3, pm.PATH_TC_DECODE),   # prep with 512 experts (16 logits per lane)
+    ("qwen3next", 1, pm.PATH_TC_DECODE),   # prep with 512 experts (16 logits per lane)
+    ("qwen3next", 3, pm.PATH_TC_DECODE),   # routing kernel + one-CTA sort, 512 experts
     ("qwen3next", 64, pm.PATH_TC_DECODE),  # heavy routing: routing kernel + one-CTA sort
     ("qwen3next", 16, pm.PATH_FUSED),
     ("mixtral", 32, pm.PATH_FUSED),
