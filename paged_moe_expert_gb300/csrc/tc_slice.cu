@@ -29,14 +29,16 @@
 // would move the rounding point off the definition's bf16(h) by up to 2^-9 per element, an error
 // that grows from layer to layer of a model; the low part keeps it below 2^-17.  It takes the
 // down MMA's rows after the tokens' own (N = 2 MT for at most MT = 8 or 16 tokens, one kernel
-// instance each), so the down projection still needs one MMA per k-step.  The first tile of each CTA c < g0 is a
-// shared-chunk tile fixed before routing (tile c), so those CTAs stream it while the tokens are
-// routed.  Roles: warp 0 the TMA producer, warp 1 the MMA issuer, warps 2..9 route every token (in
-// every CTA), warps 2..5 then run the epilogues, and all eight the combine.  The MMA's M side holds
-// 128 weight rows (64 W1 over the 64 W3 rows of the same columns for gate/up; 128 W2 rows for the
-// down projection), its N side the 16 token slots (gate/up) or the MT tokens' h'_hi rows followed
-// by their h'_lo rows (down projection).  All waits are bounded; a time-out sets the
-// error word and the kernel unwinds.  The grid barrier needs every CTA resident: one CTA per SM.
+// instance each), so the down projection still needs one MMA per k-step.
+//
+// The first tile of each CTA c < g0 is a shared-chunk tile fixed before routing (tile c), so those
+// CTAs stream it while the tokens are routed.  Roles: warp 0 the TMA producer, warp 1 the MMA
+// issuer, warps 2..9 route every token (in every CTA), warps 2..5 then run the epilogues, and all
+// eight the combine.  The MMA's M side holds 128 weight rows (64 W1 over the 64 W3 rows of the
+// same columns for gate/up; 128 W2 rows for the down projection), its N side the 16 token slots
+// (gate/up) or the MT tokens' h'_hi rows followed by their h'_lo rows (down projection).  All
+// waits are bounded; a time-out sets the error word and the kernel unwinds.  The grid barrier
+// needs every CTA resident: one CTA per SM.
 #include <math.h>
 
 #include "decode_common.cuh"
