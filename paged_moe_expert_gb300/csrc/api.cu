@@ -700,7 +700,16 @@ pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_vie
 
 size_t pmoe_workspace_size(const pmoe_layer_desc* desc, int32_t max_tokens) {
     if (!desc_ok(desc) || max_tokens < 0) return 0;
-    return layout(*desc, max_tokens).total;
+    // every region grows with T inside the ranges the decode kernels serve, but those kernels'
+    // scratch exists only up to their own token limits, so a call of up to 16 or 32 tokens can
+    // need more than a larger one: take the largest of the three
+    size_t m = layout(*desc, max_tokens).total;
+    const int32_t lim[2] = {kSliceMaxTokens, kFusedMaxTokens};
+    for (int i = 0; i < 2; ++i) {
+        const size_t b = layout(*desc, max_tokens < lim[i] ? max_tokens : lim[i]).total;
+        if (b > m) m = b;
+    }
+    return m;
 }
 
 pmoe_status moe_paged_forward(pmoe_plan_t plan, const void* hidden, int32_t T,

@@ -57,6 +57,20 @@ def test_workspace_size_is_host_only_and_monotone(lib):
     assert pm.workspace_size(d, -1) == 0
 
 
+@pytest.mark.parametrize("shape", [(256, 128, 8, 2, 0), (2048, 1408, 60, 4, 4), (2048, 512, 512, 10, 1),
+                                   (4096, 14336, 8, 2, 0)])
+def test_workspace_size_covers_every_smaller_call(lib, shape):
+    """pmoe_workspace_size(desc, n) is enough for any call of up to n tokens: the decode kernels'
+    scratch exists only up to 16 and 32 tokens, so a call of that size can need more than a larger
+    one, and the size for n must cover it."""
+    d, f, E, k, S = shape
+    desc = pm.make_desc(d, f, E, k, True, S, 4)
+    own = {T: pm.workspace_size(desc, T) for T in range(0, 70)}
+    for n in range(0, 70):
+        need = max(own[T] for T in range(0, n + 1))
+        assert pm.workspace_size(desc, n) >= need, (n, pm.workspace_size(desc, n), need)
+
+
 def test_host_validation_statuses(lib):
     h = ctypes.c_void_p()
     bad = pm.make_desc(2048, 1408, 60, 61, False)          # k > E
