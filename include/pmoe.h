@@ -192,7 +192,8 @@ typedef struct {
     int64_t meta;          /* int32 [16]: [0] n_padded (sorting paths), [1] work units and [2] of
                               them single blocks (CTA-pair path), [3] active slots (fused and
                               column-slice paths) */
-    int64_t block_rows;    /* int32 [n_padded / block_m]: valid rows of each block (PMOE_PATH_TC) */
+    int64_t block_rows;    /* int32 [n_padded / block_m]: valid rows of each block (PMOE_PATH_TC,
+                              PMOE_PATH_TC_DECODE) */
     int64_t units;         /* int32 [meta[1]][4]: CTA-pair work units {first block << 1 | single
                               block, expert, W1 location, W3 location}, location = map << 29 | page
                               with map 0 pool, 1 + b load buffer b (PMOE_PATH_TC2) */

@@ -109,8 +109,12 @@ struct SwapParams {
 };
 static SwapParams swap_params(const pmoe_layer_desc& D, int64_t T) {
     SwapParams p{};
+    // tokens per block: T rounded up to a power of two, at most 64 up to 128 tokens (a block of
+    // 128 token rows leaves room for only four 48 KB ring stages, and with few tokens per expert
+    // the deeper ring of 40 KB stages streams faster: Qwen3-Next-shaped T=128 150 -> 143 us)
+    // and 128 above
     int bn = 16;
-    while (bn < T && bn < 128) bn <<= 1;
+    while (bn < T && bn < (T > 128 ? 128 : 64)) bn <<= 1;
     p.bn = bn;
     const int64_t ES = D.num_experts + D.num_shared_chunks;
     const int64_t np = T * (D.top_k + D.num_shared_chunks);
@@ -430,7 +434,7 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         rs.unit_group = at<int2>(ws, W.ugroup);
     }
     int32_t* brows = at<int32_t>(ws, W.brows);
-    if (path == PMOE_PATH_TC) rs.block_rows = brows;
+    if (path == PMOE_PATH_TC || path == PMOE_PATH_TC_DECODE) rs.block_rows = brows;
     const uint16_t* hid = static_cast<const uint16_t*>(hidden);
     int ev = 0;
     // the single-CTA prep also copies the rows when they are few (at most 64 KB)
@@ -514,12 +518,13 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         PMOE_CUDA(launch_tc_swap(stacked ? 3 : 1, contig, sw.bn, xmap,
                                  stacked ? P->tm_rows_d64 : P->tm_rows_d, sorted, T, D.top_k,
                                  D.num_shared_chunks, bexp, meta, loc, h, D.f, D.d, 1, 0, nblk,
-                                 P->num_sms, P->d_error, gather_in_prep ? 0 : 1, stream, hidp, sh),
+                                 P->num_sms, P->d_error, gather_in_prep ? 0 : 1, stream, hidp, sh, brows),
                   "gate/up gemm");
         PMOE_CUDA(mark(P, ev++, stream), "profile event");
         PMOE_CUDA(launch_tc_swap(2, contig, sw.bn, hmap, P->tm_rows_f, sorted, T, D.top_k,
                                  D.num_shared_chunks, bexp, meta, loc, y, D.f, D.d, sw.splits,
-                                 sw.ystride, nblk, P->num_sms, P->d_error, 1, stream), "down gemm");
+                                 sw.ystride, nblk, P->num_sms, P->d_error, 1, stream, nullptr,
+                                 SharedRows{}, brows), "down gemm");
         ystride = sw.ystride;
         splits = sw.splits;
     } else {
@@ -691,7 +696,7 @@ pmoe_status pmoe_plan_routing_view(pmoe_plan_t plan, int32_t T, pmoe_routing_vie
         v.sorted_ids = (int64_t)W.sorted;
         v.block_expert = (int64_t)W.bexp;
         v.inv = (int64_t)W.inv;
-        if (v.path == PMOE_PATH_TC) v.block_rows = (int64_t)W.brows;
+        if (v.path == PMOE_PATH_TC || v.path == PMOE_PATH_TC_DECODE) v.block_rows = (int64_t)W.brows;
         if (v.path == PMOE_PATH_TC2) v.units = (int64_t)W.units;
     }
     *out = v;

@@ -335,6 +335,6 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
                            int early, cudaStream_t s, const CUtensorMap* hid = nullptr,
-                           SharedRows sh = SharedRows{});
+                           SharedRows sh = SharedRows{}, const int32_t* block_rows = nullptr);
 
 }  // namespace pmoe

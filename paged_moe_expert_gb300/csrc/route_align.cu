@@ -137,22 +137,99 @@ __device__ __forceinline__ unsigned long long atrace_time() {
 #define ATRACE(i) ((void)0)
 #endif
 
+// Exclusive scan over experts of their padded row counts (cnt[e] rounded up to block_m) into
+// off[0..ES], by the whole CTA: each thread sums a contiguous run of experts, warps scan their
+// threads' sums with shuffles and warp 0 scans the warps' totals (wsum: kAlignWarps words).
+// Every thread must call it; off is complete after the caller's next __syncthreads.
+__device__ __forceinline__ void padded_offsets(const int32_t* cnt, int32_t* off, int ES, int block_m,
+                                               int32_t* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, NT = kAlignWarps * 32;
+    const int per = (ES + NT - 1) / NT;
+    const int e0 = tid * per, e1 = min(ES, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) local += (cnt[e] + block_m - 1) / block_m * block_m;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int v = lane < kAlignWarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += y;
+        }
+        if (lane < kAlignWarps) wsum[lane] = v;
+    }
+    __syncthreads();
+    int run = incl - local + (w > 0 ? wsum[w - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        off[e] = run;
+        run += (cnt[e] + block_m - 1) / block_m * block_m;
+    }
+    if (tid == 0) off[ES] = wsum[kAlignWarps - 1];
+}
+
+// Pad rows, block map and valid rows per block of experts e = first, first + step, ... (one
+// calling warp): lane i reads the offsets of the i-th expert of each group of 32, then the warp
+// takes the group's experts that have rows one at a time, its lanes over the expert's pad rows
+// and blocks (coalesced stores).
+__device__ __forceinline__ void fill_blocks(const int32_t* off, const int32_t* cnt, int first, int step,
+                                            int ES, int block_m, int32_t pad, int32_t* sorted_ids,
+                                            int32_t* block_expert, int32_t* block_rows, int lane) {
+    for (int g = first; g < ES; g += 32 * step) {
+        const int e = g + lane * step;
+        int o = 0, n = 0, end = 0;
+        if (e < ES) {
+            o = off[e];
+            n = cnt[e];
+            end = off[e + 1];
+        }
+        const int b0 = o / block_m, b1 = end / block_m;
+        for (unsigned act = __ballot_sync(0xffffffffu, end > o); act; act &= act - 1) {
+            const int src = __ffs(act) - 1;
+            const int ee = g + src * step;
+            const int oo = __shfl_sync(0xffffffffu, o, src), nn = __shfl_sync(0xffffffffu, n, src);
+            const int en = __shfl_sync(0xffffffffu, end, src);
+            const int bb0 = __shfl_sync(0xffffffffu, b0, src), bb1 = __shfl_sync(0xffffffffu, b1, src);
+            for (int r = oo + nn + lane; r < en; r += 32) sorted_ids[r] = pad;
+            for (int b = bb0 + lane; b < bb1; b += 32) {
+                block_expert[b] = ee;
+                if (block_rows) block_rows[b] = min(block_m, oo + nn - b * block_m);
+            }
+        }
+    }
+}
+
+// `after_count` runs in every thread once the pairs are counted, before the CTA synchronises
+// (the one-CTA sort stores its page tables to shared memory there, so their loads overlap the
+// count).
+template <typename AfterCount>
 __device__ __forceinline__ void align_block(
     const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ inv, int32_t* __restrict__ meta, const ResolveArgs& rs, int do_resolve,
-    int32_t* smem) {
+    int32_t* smem, AfterCount&& after_count) {
     const int ES = E + S;
     int32_t* cw = smem;                         // [kAlignWarps][ES]
     int32_t* cnt = cw + kAlignWarps * ES;       // [ES]
     int32_t* off = cnt + ES;                    // [ES + 1]
+    int32_t* wsum = off + ES + 1;               // [kAlignWarps]
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int NT = kAlignWarps * 32;
     const int64_t NR = (int64_t)T * k;
     const int64_t NP = (int64_t)T * (k + S);
 
     ATRACE(0);   // start
-    for (int i = tid; i < kAlignWarps * ES; i += NT) cw[i] = 0;
+    {
+        // shared memory is 16-byte aligned and kAlignWarps * ES is a multiple of 4
+        int4* cw4 = reinterpret_cast<int4*>(cw);
+        for (int i = tid; i < kAlignWarps * ES / 4; i += NT) cw4[i] = make_int4(0, 0, 0, 0);
+    }
     __syncthreads();
     ATRACE(1);   // counters zeroed
 
@@ -164,6 +241,7 @@ __device__ __forceinline__ void align_block(
         if (e < 0 || e >= E) e = 0;  // routing output is in range; guard the test entry point
         atomicAdd(&cw[w * ES + e], 1);
     }
+    after_count();
     __syncthreads();
     ATRACE(2);   // counted
 
@@ -179,25 +257,7 @@ __device__ __forceinline__ void align_block(
     __syncthreads();
     ATRACE(3);   // per-warp prefix
 
-    if (w == 0) {  // padded exclusive scan over experts
-        const int per = (ES + 31) / 32;
-        const int b0 = lane * per;
-        int local = 0;
-        for (int e = b0; e < b0 + per && e < ES; ++e)
-            local += (cnt[e] + block_m - 1) / block_m * block_m;
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        int run = incl - local;
-        for (int e = b0; e < b0 + per && e < ES; ++e) {
-            off[e] = run;
-            run += (cnt[e] + block_m - 1) / block_m * block_m;
-        }
-        if (lane == 31) off[ES] = incl;
-    }
+    padded_offsets(cnt, off, ES, block_m, wsum);
     __syncthreads();
     ATRACE(4);   // offsets
 
@@ -225,14 +285,8 @@ __device__ __forceinline__ void align_block(
         inv[NR + idx] = pos;
     }
     ATRACE(6);   // shared pairs placed
-    for (int e = tid; e < ES; e += NT) {
-        const int o = off[e], c = cnt[e], end = off[e + 1];
-        for (int r = o + c; r < end; ++r) sorted_ids[r] = (int32_t)NP;
-        for (int b = o / block_m; b < end / block_m; ++b) block_expert[b] = e;
-        if (rs.block_rows)
-            for (int b = o / block_m; b < end / block_m; ++b)
-                rs.block_rows[b] = min(block_m, o + c - b * block_m);
-    }
+    fill_blocks(off, cnt, w, kAlignWarps, ES, block_m, (int32_t)NP, sorted_ids, block_expert,
+                rs.block_rows, lane);
     if (tid == 0) meta[kMetaNPadded] = off[ES];
     ATRACE(7);   // pads and block map
     if (rs.units) {
@@ -251,14 +305,51 @@ __device__ __forceinline__ void align_block(
     ATRACE(8);   // resolved
 }
 
+constexpr int kPrepTabPerThread = 8;   // (E + 3*(E+S)) / threads for E + S <= 1024
+static_assert(kPrepTabPerThread * kAlignWarps * 32 >= 4 * kMaxExpertsTotal,
+              "every buffer-slot and page-table entry needs a thread's table register");
+
+__host__ __device__ constexpr int align_words(int ES) { return kAlignWarps * ES + 2 * ES + 1 + kAlignWarps; }
+
+// The one-CTA sort.  With page resolution, the buffer-slot and page tables are loaded at the
+// start (a few loads per thread, in flight while the pairs are counted) and kept in shared
+// memory after the sort's own words, so the resolution at the end reads shared memory only.
 __global__ void __launch_bounds__(kAlignWarps * 32) align_kernel(
     const int32_t* __restrict__ ids, int T, int k, int E, int S, int block_m,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_expert,
     int32_t* __restrict__ inv, int32_t* __restrict__ meta, ResolveArgs rs, int do_resolve) {
     extern __shared__ int32_t smem[];
+    const int ES = E + S;
+    int32_t* s_bs = smem + align_words(ES);   // [E]
+    int32_t* s_pt = s_bs + E;                 // [ES*3]
     pdl_wait_prev();
     pdl_allow_next();
-    align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, rs, do_resolve, smem);
+    const int tid = threadIdx.x;
+    constexpr int NT = kAlignWarps * 32;
+    const int ntab = do_resolve && !rs.contiguous ? E + 3 * ES : 0;
+    int32_t tv[kPrepTabPerThread];
+#pragma unroll
+    for (int i = 0; i < kPrepTabPerThread; ++i) {
+        const int idx = tid + i * NT;
+        tv[i] = idx < ntab ? (idx < E ? rs.buf_slot[idx] : rs.page_table[idx - E]) : 0;
+    }
+    auto stash = [&]() {
+#pragma unroll
+        for (int i = 0; i < kPrepTabPerThread; ++i) {
+            const int idx = tid + i * NT;
+            if (idx < ntab) {
+                if (idx < E) s_bs[idx] = tv[i];
+                else s_pt[idx - E] = tv[i];
+            }
+        }
+    };
+    ResolveArgs local = rs;
+    if (ntab > 0) {
+        local.buf_slot = s_bs;
+        local.page_table = s_pt;
+    }
+    align_block(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, local, do_resolve, smem,
+                stash);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -307,6 +398,7 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
     int32_t* cnt = off + ES + 1;       // [ES]
     int32_t* base = cnt + ES;          // [ES]
     int32_t* cw = base + ES;           // [kAlignWarps][ES]
+    int32_t* wsum = cw + kAlignWarps * ES;   // [kAlignWarps]
     pdl_wait_prev();
     pdl_allow_next();
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, NT = kAlignWarps * 32;
@@ -334,25 +426,7 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
     }
     for (int i = tid; i < kAlignWarps * ES; i += NT) cw[i] = 0;
     __syncthreads();
-
-    if (w == 0) {  // padded exclusive scan over experts
-        const int per = (ES + 31) / 32;
-        const int b0 = lane * per;
-        int local = 0;
-        for (int e = b0; e < b0 + per && e < ES; ++e) local += (cnt[e] + block_m - 1) / block_m * block_m;
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        int run = incl - local;
-        for (int e = b0; e < b0 + per && e < ES; ++e) {
-            off[e] = run;
-            run += (cnt[e] + block_m - 1) / block_m * block_m;
-        }
-        if (lane == 31) off[ES] = incl;
-    }
+    padded_offsets(cnt, off, ES, block_m, wsum);
     // this CTA's segment, split into per-warp sub-segments
     const int64_t c0 = (int64_t)c * seg, c1 = c0 + seg < NR ? c0 + seg : NR;
     const int64_t sub = (c1 - c0 + kAlignWarps - 1) / kAlignWarps;
@@ -396,14 +470,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) align_scatter_kernel(
         sorted_ids[pos] = (int32_t)(NR + idx);
         inv[NR + idx] = pos;
     }
-    for (int e = c + C * tid; e < ES; e += C * NT) {
-        const int o = off[e], n = cnt[e], end = off[e + 1];
-        for (int r = o + n; r < end; ++r) sorted_ids[r] = (int32_t)NP;
-        for (int bb = o / block_m; bb < end / block_m; ++bb) block_expert[bb] = e;
-        if (rs.block_rows)
-            for (int bb = o / block_m; bb < end / block_m; ++bb)
-                rs.block_rows[bb] = min(block_m, o + n - bb * block_m);
-    }
+    fill_blocks(off, cnt, c * kAlignWarps + w, C * kAlignWarps, ES, block_m, (int32_t)NP, sorted_ids,
+                block_expert, rs.block_rows, lane);
     if (c == 0 && tid == 0) meta[kMetaNPadded] = off[ES];
     if (c == 0 && rs.units) {
         __syncthreads();   // the per-warp counters are free: they hold the locations now
@@ -447,9 +515,6 @@ __global__ void __launch_bounds__(256) gather_pairs_kernel(const uint16_t* __res
 // one launch on them instead of two.  The page-table loads are issued before the routing so the
 // two latencies overlap; the routing ids and the tables then stay in shared memory for the sort.
 // When the gathered rows are small, the row gather runs here too (x != NULL).
-constexpr int kPrepTabPerThread = 8;   // (E + 3*(E+S)) / threads for E + S <= 1024
-
-__host__ __device__ constexpr int align_words(int ES) { return kAlignWarps * ES + 2 * ES + 1; }
 
 template <int EPL>
 __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
@@ -494,7 +559,8 @@ __global__ void __launch_bounds__(kAlignWarps * 32) prep_small_kernel(
         local.buf_slot = s_bs;
         local.page_table = s_pt;
     }
-    align_block(s_ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, local, 1, s_align);
+    align_block(s_ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, local, 1, s_align,
+                [] {});
     if (x) {
         __syncthreads();
         const int NP = T * (k + S);
@@ -509,7 +575,8 @@ extern "C" int pmoe_align_trace_read(unsigned long long* host) {
 }
 #endif
 
-static size_t align_smem_bytes(int ES) { return sizeof(int32_t) * (size_t)align_words(ES); }
+// the one-CTA sort's words and its copy of the buffer-slot and page tables (E <= ES)
+static size_t align_smem_bytes(int ES) { return sizeof(int32_t) * ((size_t)align_words(ES) + 4 * (size_t)ES); }
 
 static size_t prep_smem_bytes(int T, int E, int k, int S) {
     return sizeof(int32_t) * ((size_t)align_words(E + S) + (size_t)T * k + E + 3 * (size_t)(E + S));
@@ -554,10 +621,10 @@ cudaError_t launch_align_multi(const int32_t* ids, int T, int k, int E, int S, i
         return launch_align(ids, T, k, E, S, block_m, sorted_ids, block_expert, inv, meta, resolve, s);
     const int ES = E + S;
     const int seg = (int)((NR + C - 1) / C);
-    const size_t sm2 = sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * ES + 1);
+    const size_t sm2 = sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * ES + 1 + kAlignWarps);
     static std::atomic<unsigned long long> attr{0};
     cudaError_t e0 = raise_smem_limit(reinterpret_cast<const void*>(align_scatter_kernel),
-                                      (int)(sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * kMaxExpertsTotal + 1)),
+                                      (int)(sizeof(int32_t) * ((size_t)(kAlignWarps + 3) * kMaxExpertsTotal + 1 + kAlignWarps)),
                                       &attr);
     if (e0 != cudaSuccess) return e0;
     ResolveArgs rs{};

@@ -75,6 +75,7 @@ struct SwapArgs {
     int early;            // 1: the sort's outputs are complete at launch (see the priming below)
     int32_t* err;
     SharedRows sh;        // gate/up: shared-chunk blocks straight from hidden
+    const int32_t* block_rows;   // tokens of each block (the rest of its BN rows are pads), or NULL
 };
 
 struct SwapMaps {
@@ -298,6 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_tile(t, b, wt, sp, kb0, kb1);
             ExpertLoc l0, l1;
             if (!tile_valid(b, l0, l1) || kb0 >= kb1) continue;
+            // only the block's token columns are read out and stored: its pad columns feed rows
+            // of h and y that nothing reads
+            const int rows = args.block_rows ? args.block_rows[b] : BN;
             if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.err)) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * C::ACC_COLS) + ((uint32_t)(quad * 32) << 16);
@@ -305,15 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kMode == kGateUp) {
                 uint16_t* h = static_cast<uint16_t*>(args.out) + wt * WROWS + wrow;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                for (int c0 = 0; c0 < rows; c0 += 16) {
                     float g[16], u[16];
                     tmem_ld16(taddr + c0, g);
                     tmem_ld16(taddr + BN + c0, u);
                     tmem_wait_ld();
+                    uint16_t* hc = h + (row_base + c0) * args.f;
+                    // (warp-uniform branch: whole chunks store without per-element tests)
+                    if (rows - c0 >= 16) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float a = silu_mul(g[j], u[j]);
-                        h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(a);
+                        for (int j = 0; j < 16; ++j) hc[(int64_t)j * args.f] = f32_to_bf16_bits(silu_mul(g[j], u[j]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (j < rows - c0) hc[(int64_t)j * args.f] = f32_to_bf16_bits(silu_mul(g[j], u[j]));
                     }
                 }
             } else if (kMode == kGateUpStacked) {
@@ -323,8 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool up_half = quad >= 2;
                 const int r = wrow & 63;
                 uint16_t* h = static_cast<uint16_t*>(args.out) + wt * 64 + r;
+                // (rows is the same in all four epilogue warps, so each meets every named barrier)
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                for (int c0 = 0; c0 < rows; c0 += 16) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_wait_ld();
@@ -334,10 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     asm volatile("bar.sync 1, 128;" ::: "memory");
                     if (!up_half) {
+                        uint16_t* hc = h + (row_base + c0) * args.f;
+                        if (rows - c0 >= 16) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float g = v[j], u = xch[(c0 + j) * 64 + r];
-                            h[(row_base + c0 + j) * args.f] = f32_to_bf16_bits(silu_mul(g, u));
+                            for (int j = 0; j < 16; ++j)
+                                hc[(int64_t)j * args.f] = f32_to_bf16_bits(silu_mul(v[j], xch[(c0 + j) * 64 + r]));
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < rows - c0)
+                                    hc[(int64_t)j * args.f] = f32_to_bf16_bits(silu_mul(v[j], xch[(c0 + j) * 64 + r]));
                         }
                     }
                     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -346,13 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r = wt * WROWS + wrow;
                 float* y = static_cast<float*>(args.out) + (int64_t)sp * args.ystride * args.d + r;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                for (int c0 = 0; c0 < rows; c0 += 16) {
                     float v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_wait_ld();
                     if (r < args.d) {
+                        float* yc = y + (row_base + c0) * args.d;
+                        if (rows - c0 >= 16) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) y[(row_base + c0 + j) * args.d] = v[j];
+                            for (int j = 0; j < 16; ++j) yc[(int64_t)j * args.d] = v[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (j < rows - c0) yc[(int64_t)j * args.d] = v[j];
+                        }
                     }
                 }
             }
@@ -407,7 +430,8 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
                            int S, const int32_t* block_expert, const int32_t* meta,
                            const ExpertLoc* loc, void* out, int f, int d, int splits,
                            int64_t ystride, int64_t nblk_max, int num_sms, int32_t* err,
-                           int early, cudaStream_t s, const CUtensorMap* hid, SharedRows sh) {
+                           int early, cudaStream_t s, const CUtensorMap* hid, SharedRows sh,
+                           const int32_t* block_rows) {
     SwapMaps maps;
     maps.act = act;
     for (int i = 0; i < 3; ++i) maps.w[i] = wmaps[i];
@@ -427,6 +451,7 @@ cudaError_t launch_tc_swap(int mode, bool contig, int bn, const CUtensorMap& act
     a.ystride = ystride;
     a.early = early;
     a.sh = hid ? sh : SharedRows{};
+    a.block_rows = block_rows;
     if (mode == kGateUp || mode == kGateUpStacked) {
         a.k_blocks = d / BK;
         a.w_tiles = f / (mode == kGateUp ? WROWS : 64);
