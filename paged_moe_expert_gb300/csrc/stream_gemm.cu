@@ -343,14 +343,20 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
 }
 
 // The same sum over bf16 y rows (the 128-token-block and CTA-pair paths, no K split): a thread owns
-// eight columns (one 16-byte load per pair row).
+// CPT groups of eight columns, c, c + G, ... (G: the token's threads), one 16-byte load per pair
+// row and group, eight loads in flight per thread: with few pairs per token (top-2) a thread takes
+// four groups, so each round trip to memory carries as many bytes as with eight pairs.  Each
+// column is summed over the pairs in order, whatever CPT is.
+template <int CPT>
 __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(
     const uint16_t* __restrict__ y, const float* __restrict__ w, const int32_t* __restrict__ inv,
     int T, int d, int k, int S, uint16_t* __restrict__ out) {
+    constexpr int PB = 8 / CPT;   // pairs per batch of loads
     pdl_wait_prev();
     pdl_allow_next();
     const int t = blockIdx.y;
-    const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // group of 8 columns
+    const int c = blockIdx.x * kCombineThreads + threadIdx.x;   // first group of 8 columns
+    const int G = gridDim.x * kCombineThreads;
     const int P = k + S;
     const int64_t NR = (int64_t)T * k;
     __shared__ int64_t s_row[64];
@@ -360,40 +366,51 @@ __global__ void __launch_bounds__(kCombineThreads) combine_bf16_kernel(
         s_w[p] = p < k ? w[(int64_t)t * k + p] : 1.f;
     }
     __syncthreads();
-    if (c >= (d >> 3)) return;
+    const int d8 = d >> 3;
+    if (c >= d8) return;
     const uint4* y8 = reinterpret_cast<const uint4*>(y);
-    const int64_t d8 = d >> 3;
-    float acc[8];
+    float acc[CPT][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int p0 = 0; p0 < P; p0 += 8) {
-        uint4 v[8];
+    for (int j = 0; j < CPT; ++j)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (p0 + i < P) v[i] = __ldg(y8 + s_row[p0 + i] * d8 + c);
-        }
+        for (int q = 0; q < 8; ++q) acc[j][q] = 0.f;
+    for (int p0 = 0; p0 < P; p0 += PB) {
+        uint4 v[PB][CPT];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < PB; ++i)
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                v[i][j] = make_uint4(0u, 0u, 0u, 0u);
+                if (p0 + i < P && c + j * G < d8) v[i][j] = __ldg(y8 + s_row[p0 + i] * d8 + c + j * G);
+            }
+#pragma unroll
+        for (int i = 0; i < PB; ++i) {
             if (p0 + i < P) {
                 const float wp = s_w[p0 + i];
-                acc[0] = fmaf(wp, bf16_lo(v[i].x), acc[0]);
-                acc[1] = fmaf(wp, bf16_hi(v[i].x), acc[1]);
-                acc[2] = fmaf(wp, bf16_lo(v[i].y), acc[2]);
-                acc[3] = fmaf(wp, bf16_hi(v[i].y), acc[3]);
-                acc[4] = fmaf(wp, bf16_lo(v[i].z), acc[4]);
-                acc[5] = fmaf(wp, bf16_hi(v[i].z), acc[5]);
-                acc[6] = fmaf(wp, bf16_lo(v[i].w), acc[6]);
-                acc[7] = fmaf(wp, bf16_hi(v[i].w), acc[7]);
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    acc[j][0] = fmaf(wp, bf16_lo(v[i][j].x), acc[j][0]);
+                    acc[j][1] = fmaf(wp, bf16_hi(v[i][j].x), acc[j][1]);
+                    acc[j][2] = fmaf(wp, bf16_lo(v[i][j].y), acc[j][2]);
+                    acc[j][3] = fmaf(wp, bf16_hi(v[i][j].y), acc[j][3]);
+                    acc[j][4] = fmaf(wp, bf16_lo(v[i][j].z), acc[j][4]);
+                    acc[j][5] = fmaf(wp, bf16_hi(v[i][j].z), acc[j][5]);
+                    acc[j][6] = fmaf(wp, bf16_lo(v[i][j].w), acc[j][6]);
+                    acc[j][7] = fmaf(wp, bf16_hi(v[i][j].w), acc[j][7]);
+                }
             }
         }
     }
-    uint4 o;
-    o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
-    o.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
-    o.z = (uint32_t)f32_to_bf16_bits(acc[4]) | ((uint32_t)f32_to_bf16_bits(acc[5]) << 16);
-    o.w = (uint32_t)f32_to_bf16_bits(acc[6]) | ((uint32_t)f32_to_bf16_bits(acc[7]) << 16);
-    reinterpret_cast<uint4*>(out + (int64_t)t * d)[c] = o;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        if (c + j * G >= d8) break;
+        uint4 o;
+        o.x = (uint32_t)f32_to_bf16_bits(acc[j][0]) | ((uint32_t)f32_to_bf16_bits(acc[j][1]) << 16);
+        o.y = (uint32_t)f32_to_bf16_bits(acc[j][2]) | ((uint32_t)f32_to_bf16_bits(acc[j][3]) << 16);
+        o.z = (uint32_t)f32_to_bf16_bits(acc[j][4]) | ((uint32_t)f32_to_bf16_bits(acc[j][5]) << 16);
+        o.w = (uint32_t)f32_to_bf16_bits(acc[j][6]) | ((uint32_t)f32_to_bf16_bits(acc[j][7]) << 16);
+        reinterpret_cast<uint4*>(out + (int64_t)t * d)[c + j * G] = o;
+    }
 }
 
 cudaError_t launch_combine(const void* y, bool y_bf16, int splits, int64_t ystride, const float* w,
@@ -401,9 +418,16 @@ cudaError_t launch_combine(const void* y, bool y_bf16, int splits, int64_t ystri
                            cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     if (y_bf16) {
-        const dim3 grid((unsigned)((d / 8 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
-        return launch_pdl(combine_bf16_kernel, grid, dim3(kCombineThreads), 0, s,
-                          static_cast<const uint16_t*>(y), w, inv, T, d, k, S, out);
+        const int P = k + S;
+        const int cpt = P <= 2 ? 4 : P <= 4 ? 2 : 1;   // groups of 8 columns per thread
+        const int threads = (d / 8 + cpt - 1) / cpt;
+        const dim3 grid((unsigned)((threads + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
+        const uint16_t* yb = static_cast<const uint16_t*>(y);
+        if (cpt == 4)
+            return launch_pdl(combine_bf16_kernel<4>, grid, dim3(kCombineThreads), 0, s, yb, w, inv, T, d, k, S, out);
+        if (cpt == 2)
+            return launch_pdl(combine_bf16_kernel<2>, grid, dim3(kCombineThreads), 0, s, yb, w, inv, T, d, k, S, out);
+        return launch_pdl(combine_bf16_kernel<1>, grid, dim3(kCombineThreads), 0, s, yb, w, inv, T, d, k, S, out);
     }
     const dim3 grid((unsigned)((d / 4 + kCombineThreads - 1) / kCombineThreads), (unsigned)T);
     return launch_pdl(combine_kernel, grid, dim3(kCombineThreads), 0, s, static_cast<const float*>(y),
