@@ -85,7 +85,7 @@ typedef enum {
     PMOE_PATH_AUTO = 0,   /* SLICE up to 16 tokens while a routing leaves at most 8 column
                              tiles per SM; else FUSED up to 32 tokens (E <= 128) or 16 tokens
                              (E > 128); above, by routed tokens per expert T*k/E: <= 24
-                             TC_DECODE, >= 64 TC2 when E <= 128, else TC */
+                             (and T <= 320) TC_DECODE, >= 64 TC2 when E <= 128, else TC */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */
     PMOE_PATH_TC = 2,     /* tcgen05 tensor-core grouped GEMMs, 128 tokens per tile (large T) */
     PMOE_PATH_TC_DECODE = 3, /* tcgen05 with weight rows on the MMA's M side and 16..128 tokens

@@ -69,11 +69,14 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
 }
 
 // The automatic path, by the routed tokens per expert T*k/E (measured crossovers on GB300): up to
-// 24 the small-batch tensor-core kernels (tokens on the MMA's N side); above, the CTA-pair kernels
+// 24, and up to 320 tokens, the small-batch tensor-core kernels (tokens on the MMA's N side; the
+// 512-expert Zipf-routed layer crosses to 128-token blocks between 256 and 384 tokens, 512 of them
+// 194.8 -> 187.9 us, 1024 244.0 -> 229.6 us); above, the CTA-pair kernels
 // from 64 on for layers of at most 128 experts, else the single-CTA 128-token-block kernels (with
 // hundreds of small experts most experts end in an odd block, which costs a CTA pair as much as
 // a pair of blocks).  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
 constexpr int kSwapMaxTokensPerExpert = 24;
+constexpr int kSwapMaxTokens = 320;
 // The column-slice decode kernel up to 16 tokens while a routing leaves at most 8 column tiles
 // per SM (measured on GB300 against the fused kernel: ahead from 1 to 12 tokens on the Qwen1.5-
 // and Qwen3-Next-shaped layers and at 1 and 2 on the Mixtral-shaped one, level at 16; behind
@@ -278,7 +281,8 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         const int fused_max = D.num_experts <= 128 ? kFusedMaxTokens : 16;
         path = (slice_ok && T <= kSliceAutoTokens && slice_tiles <= kSliceAutoTiles) ? PMOE_PATH_SLICE
              : T <= fused_max ? PMOE_PATH_FUSED
-             : routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts ? PMOE_PATH_TC_DECODE
+             : (routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts && T <= kSwapMaxTokens)
+                 ? PMOE_PATH_TC_DECODE
              : (routed >= (int64_t)kPairMinTokensPerExpert * D.num_experts &&
                 D.num_experts <= kPairMaxExperts) ? PMOE_PATH_TC2
              : PMOE_PATH_TC;

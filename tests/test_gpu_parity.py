@@ -168,6 +168,16 @@ def test_auto_path_by_token_count():
         assert L.plan.last_run()[0] == want
 
 
+def test_auto_path_small_batch_token_cap():
+    """Many experts: T*k/E stays small far past 320 tokens, but from 321 tokens the automatic path
+    takes 128-token blocks (layers of more than 128 experts never take CTA pairs)."""
+    cfg = syn.custom_config("e256", d=256, f=128, E=256, k=2)
+    for T, want in [(320, pm.PATH_TC_DECODE), (321, pm.PATH_TC)]:
+        L = setup_layer(cfg, T)
+        L.plan.forward(L.hidden, L.logits, L.page_table, L.buf_slot)
+        assert L.plan.last_run()[0] == want
+
+
 @pytest.mark.parametrize("T", [16, 300])
 def test_paths_agree(T):
     cfg = syn.custom_config("agree", d=256, f=256, E=6, k=2, S=1, n_buffered=2)
