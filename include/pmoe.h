@@ -82,8 +82,8 @@ typedef struct pmoe_plan* pmoe_plan_t;
 
 /* Kernel families a forward call may use (pmoe_plan_set_path). */
 typedef enum {
-    PMOE_PATH_AUTO = 0,   /* SLICE up to 16 tokens while a routing leaves at most 8 column
-                             tiles per SM; else FUSED up to 32 tokens (E <= 128) or 16 tokens
+    PMOE_PATH_AUTO = 0,   /* SLICE up to 16 tokens while no routing leaves an SM more than
+                             10 MiB of weights; else FUSED up to 32 tokens (E <= 128) or 16 tokens
                              (E > 128); above, by routed tokens per expert T*k/E: <= 24
                              (and T <= 320) TC_DECODE, >= 64 TC2 when E <= 128, else TC */
     PMOE_PATH_STREAM = 1, /* weight-streaming kernels (decode sizes; CUDA cores) */

@@ -77,13 +77,17 @@ static int stream_block_m(const pmoe_layer_desc& D, int64_t T) {
 // a pair of blocks).  Routing and sort + pad run as one single-CTA kernel up to 128 tokens.
 constexpr int kSwapMaxTokensPerExpert = 24;
 constexpr int kSwapMaxTokens = 320;
-// The column-slice decode kernel up to 16 tokens while a routing leaves at most 8 column tiles
-// per SM (measured on GB300 against the fused kernel: ahead from 1 to 12 tokens on the Qwen1.5-
-// and Qwen3-Next-shaped layers and at 1 and 2 on the Mixtral-shaped one, level at 16; behind
-// once a CTA streams more tiles, where the fused kernel's even k-block split keeps more bytes in
-// flight per SM).
+// The column-slice decode kernel up to 16 tokens while no routing leaves a CTA more than 10 MiB
+// of weights to stream (its column tiles x 64 columns x d x 3 matrices x 2 bytes).  Measured on
+// GB300 against the fused kernel, with the layers' own routings and with routings that spread
+// the tokens over the most experts: ahead or level up to 16 tokens on the Qwen1.5- and
+// Qwen3-Next-shaped layers (d = 2048: at most 10 and 9 tiles, 7.9 and 7.1 MiB per CTA; 16
+// tokens 140 against 144 us and 72 against 78 us), and at 1 and 2 tokens on the Mixtral-shaped
+// one (d = 4096, 9.4 MiB at 2 tokens); behind beyond that (3 and more Mixtral-shaped tokens, up
+// to 12 tiles = 18.9 MiB, 8-9% behind), where the fused kernel's even k-block split keeps more
+// bytes in flight per SM.
 constexpr int kSliceAutoTokens = 16;
-constexpr int kSliceAutoTiles = 8;
+constexpr int64_t kSliceAutoBytes = (int64_t)10 << 20;
 constexpr int kPairMinTokensPerExpert = 64;
 constexpr int kPairMaxExperts = 128;
 constexpr int kPrepSmallMaxTokens = 128;
@@ -279,7 +283,9 @@ static pmoe_status forward_impl(Plan* P, const void* hidden, int32_t T, const fl
         // tokens otherwise (measured on GB300: with hundreds of small experts at 17..32 tokens
         // the small-batch kernels stream a little faster)
         const int fused_max = D.num_experts <= 128 ? kFusedMaxTokens : 16;
-        path = (slice_ok && T <= kSliceAutoTokens && slice_tiles <= kSliceAutoTiles) ? PMOE_PATH_SLICE
+        const bool slice_auto = slice_ok && T <= kSliceAutoTokens &&
+                                (int64_t)slice_tiles * 64 * D.d * 3 * 2 <= kSliceAutoBytes;
+        path = slice_auto ? PMOE_PATH_SLICE
              : T <= fused_max ? PMOE_PATH_FUSED
              : (routed <= (int64_t)kSwapMaxTokensPerExpert * D.num_experts && T <= kSwapMaxTokens)
                  ? PMOE_PATH_TC_DECODE

@@ -94,4 +94,70 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
     }
 }
 
+// Two tokens by one warp, their k rounds interleaved so that the two tokens' reductions are in
+// flight together (the rounds are latency-bound): the same selection and weights as route_token
+// for each of them.
+template <int EPL>
+__device__ __forceinline__ void route_token_pair(const float* __restrict__ lg0, const float* __restrict__ lg1,
+                                                 int E, int k, int renorm, int lane,
+                                                 int32_t* __restrict__ ids0, float* __restrict__ w0,
+                                                 int32_t* __restrict__ ids1, float* __restrict__ w1) {
+    const float* lg[2] = {lg0, lg1};
+    uint32_t key[2][EPL];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            key[n][i] = e < E ? order_key(lg[n][e]) : 0u;
+        }
+    uint32_t taken[2] = {0u, 0u}, bk[2];
+    int bi[2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n) lane_best<EPL>(key[n], 0u, bk[n], bi[n]);
+    int my_id[2] = {0, 0};
+    uint32_t my_key[2] = {0u, 0u}, top[2] = {0u, 0u};
+    for (int j = 0; j < k; ++j) {
+        uint32_t m[2], win[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) m[n] = __reduce_max_sync(0xffffffffu, bk[n]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+            win[n] = __reduce_min_sync(0xffffffffu, bk[n] == m[n] ? (uint32_t)(lane + 32 * bi[n]) : 0xffffffffu);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (j == 0) top[n] = m[n];
+            if (lane == j) {
+                my_id[n] = (int)win[n];
+                my_key[n] = m[n];
+            }
+            if ((int)(win[n] & 31u) == lane) {
+                taken[n] |= 1u << bi[n];
+                lane_best<EPL>(key[n], taken[n], bk[n], bi[n]);
+            }
+        }
+    }
+    int32_t* ids[2] = {ids0, ids1};
+    float* wo[2] = {w0, w1};
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        const float mx = key_value(top[n]);
+        const float ej = lane < k ? expf(key_value(my_key[n]) - mx) : 0.f;
+        float den = 0.f;
+        if (renorm) {
+            den = ej;
+        } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i)
+                if (key[n][i] != 0u) den += expf(key_value(key[n][i]) - mx);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (lane < k) {
+            ids[n][lane] = my_id[n];
+            wo[n][lane] = ej / den;
+        }
+    }
+}
+
 }  // namespace pmoe

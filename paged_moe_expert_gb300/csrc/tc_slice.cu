@@ -67,9 +67,9 @@ constexpr int kTabSlotExpert = kTabSlotOf + 2048;            // i16 [1024] slot 
 constexpr int kTabIds = kTabSlotExpert + 2048;               // i32 [16][16] routing ids
 constexpr int kTabW = kTabIds + 1024;                        // f32 [16][16] routing weights
 constexpr int kTabMisc = kTabW + 1024;                       // i32 [64]
-constexpr int kTabXch = kTabMisc + 256;                      // f32 [16][64] up -> gate lanes
-constexpr int kTabRed = kTabXch + BN * 64 * 4;               // f32 [8][32] combine sums
-constexpr int kTabBytes = (kTabRed + 8 * 32 * 4 + 127) / 128 * 128;
+constexpr int kTabXch = kTabMisc + 256;                      // f32 [16][64] up -> gate lanes; after
+                                                             // the barrier [4][8][32] combine sums
+constexpr int kTabBytes = (kTabXch + BN * 64 * 4 + 127) / 128 * 128;
 constexpr uint32_t kTmemCols = 512;            // gate/up accumulators 2 x 16, down <= 480 columns
 constexpr uint32_t kIdesc = idesc_bf16(128, BN);
 
@@ -157,7 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* w_s = reinterpret_cast<float*>(tab + kTabW);
     int32_t* misc = reinterpret_cast<int32_t*>(tab + kTabMisc);
     float* xch = reinterpret_cast<float*>(tab + kTabXch);
-    float* red = reinterpret_cast<float*>(tab + kTabRed);
     // misc: [0..7] scan scratch, [8] routed experts Ar, [9] abort, [10] TMEM address,
     //       [11] barrier decision, [12..13] arrival counter at entry (low, high), [14] CTAs
     //       that work (G'), [15] this CTA's tiles
@@ -424,20 +423,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = gi; e < E; e += kGroupThreads) tok_mask[e] = 0u;
         group_bar();
         if (leader) TRACE(17);   // routing starts
-        for (int t = gw; t < T; t += kGroupWarps) {
-            const float* lg = args.logits + (int64_t)t * E;
-            int32_t* io = ids_s + t * kMaxTopK;
-            float* wo = w_s + t * kMaxTopK;
-            switch (args.epl) {
-                case 1: route_token<1>(lg, E, args.k, args.renorm, lane, io, wo); break;
-                case 2: route_token<2>(lg, E, args.k, args.renorm, lane, io, wo); break;
-                case 4: route_token<4>(lg, E, args.k, args.renorm, lane, io, wo); break;
-                case 8: route_token<8>(lg, E, args.k, args.renorm, lane, io, wo); break;
-                case 16: route_token<16>(lg, E, args.k, args.renorm, lane, io, wo); break;
-                default: route_token<32>(lg, E, args.k, args.renorm, lane, io, wo); break;
+        // warp gw routes token gw, and token gw + 8 with it when there is one (T <= 16)
+        static_assert(kSliceMaxTokens <= 2 * kGroupWarps, "two tokens per routing warp at most");
+        {
+            const int t = gw, t2 = gw + kGroupWarps;
+            if (t < T) {
+                const float* lg = args.logits + (int64_t)t * E;
+                int32_t* io = ids_s + t * kMaxTopK;
+                float* wo = w_s + t * kMaxTopK;
+                if (t2 < T) {
+                    const float* lg2 = args.logits + (int64_t)t2 * E;
+                    int32_t* io2 = ids_s + t2 * kMaxTopK;
+                    float* wo2 = w_s + t2 * kMaxTopK;
+                    switch (args.epl) {
+                        case 1: route_token_pair<1>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                        case 2: route_token_pair<2>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                        case 4: route_token_pair<4>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                        case 8: route_token_pair<8>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                        case 16: route_token_pair<16>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                        default: route_token_pair<32>(lg, lg2, E, args.k, args.renorm, lane, io, wo, io2, wo2); break;
+                    }
+                } else {
+                    switch (args.epl) {
+                        case 1: route_token<1>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                        case 2: route_token<2>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                        case 4: route_token<4>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                        case 8: route_token<8>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                        case 16: route_token<16>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                        default: route_token<32>(lg, E, args.k, args.renorm, lane, io, wo); break;
+                    }
+                }
+                __syncwarp();
+                if (lane < args.k) atomicOr(&tok_mask[io[lane]], 1u << t);
+                if (t2 < T && lane < args.k) atomicOr(&tok_mask[(ids_s + t2 * kMaxTopK)[lane]], 1u << t2);
             }
-            __syncwarp();
-            if (lane < args.k) atomicOr(&tok_mask[io[lane]], 1u << t);
         }
         if (leader) TRACE(18);   // this warp's tokens routed
         group_bar();
@@ -598,32 +617,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*decision) {
             if (leader) TRACE(11);   // barrier
             // combine: out[t][r] = bf16(sum over c < G' of partial_c[t][r]); one item is a token
-            // and 32 output rows; warp w sums the partials c = w, w + 8, ... in order, then the
-            // first warp adds the eight sums in order
+            // and 32 output rows, the CTA's items cta, cta + G, ... taken four at a time; warp w
+            // sums the partials c = w, w + 8, ... of each in order, then warp j < 4 adds item j's
+            // eight sums in order.  Four items' loads in flight at once: their round trips to L2,
+            // not the bytes, set the combine's time.
             const int ch32 = (args.d + 31) / 32;
-            for (int item = cta; item < T * ch32; item += G) {
-                const int t = item / ch32, r = (item - t * ch32) * 32 + lane;
-                const int rr = r < args.d ? r : args.d - 1;
-                const float* src = args.p2 + (int64_t)t * args.d + rr;
-                const int64_t cstride = (int64_t)T * args.d;
-                // loads clamped to a written partial so that all of them issue at once; only the
-                // partials c < G' are added, in order
-                float s = 0.f;
-                int c = gw;
-                for (; c + 56 < Gw; c += 64) {
-                    float p[8];
+            const int n_items = T * ch32;
+            const int64_t cstride = (int64_t)T * args.d;
+            float* cred = xch;   // [4][8][32] warp sums (the gate/up exchange is no longer used)
+            for (int i0 = cta; i0 < n_items; i0 += 4 * G) {
+                const float* src[4];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) p[q] = __ldcg(src + (int64_t)(c + 8 * q) * cstride);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) s += p[q];
+                for (int j = 0; j < 4; ++j) {
+                    const int item = i0 + j * G < n_items ? i0 + j * G : i0;
+                    const int t = item / ch32, r = (item - t * ch32) * 32 + lane;
+                    src[j] = args.p2 + (int64_t)t * args.d + (r < args.d ? r : args.d - 1);
                 }
-                for (; c < Gw; c += 8) s += __ldcg(src + (int64_t)c * cstride);
-                red[gw * 32 + lane] = s;
+                float sj[4] = {0.f, 0.f, 0.f, 0.f};
+                int c = gw;
+                for (; c + 24 < Gw; c += 32) {
+                    float p[4][4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) p[j][q] = __ldcg(src[j] + (int64_t)(c + 8 * q) * cstride);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) sj[j] += p[j][q];
+                }
+                for (; c < Gw; c += 8) {
+                    float p[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) p[j] = __ldcg(src[j] + (int64_t)c * cstride);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sj[j] += p[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cred[(j * kGroupWarps + gw) * 32 + lane] = sj[j];
                 group_bar();
-                if (gw == 0) {
+                if (gw < 4 && i0 + gw * G < n_items) {
+                    const int item = i0 + gw * G;
+                    const int t = item / ch32, r = (item - t * ch32) * 32 + lane;
                     float o = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kGroupWarps; ++w) o += red[w * 32 + lane];
+                    for (int w = 0; w < kGroupWarps; ++w) o += cred[(gw * kGroupWarps + w) * 32 + lane];
                     if (r < args.d) args.out[(int64_t)t * args.d + r] = f32_to_bf16_bits(o);
                 }
                 group_bar();
