@@ -431,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float* lg = args.logits + (int64_t)t * E;
                 int32_t* io = ids_s + t * kMaxTopK;
                 float* wo = w_s + t * kMaxTopK;
-                if (t2 < T) {
+                // (the 8-token instance never has a second token: no pair code in it)
+                if (MT > kGroupWarps && t2 < T) {
                     const float* lg2 = args.logits + (int64_t)t2 * E;
                     int32_t* io2 = ids_s + t2 * kMaxTopK;
                     float* wo2 = w_s + t2 * kMaxTopK;
@@ -455,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 if (lane < args.k) atomicOr(&tok_mask[io[lane]], 1u << t);
-                if (t2 < T && lane < args.k) atomicOr(&tok_mask[(ids_s + t2 * kMaxTopK)[lane]], 1u << t2);
+                if (MT > kGroupWarps && t2 < T && lane < args.k)
+                    atomicOr(&tok_mask[(ids_s + t2 * kMaxTopK)[lane]], 1u << t2);
             }
         }
         if (leader) TRACE(18);   // this warp's tokens routed
