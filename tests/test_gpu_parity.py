@@ -422,3 +422,36 @@ def _weights(name):
         _WCACHE.clear()
         _WCACHE[name] = syn.make_weights(syn.CONFIGS[name])
     return _WCACHE[name]
+
+
+def spread_logits(T, E, k, seed):
+    """Logits under which token t prefers experts t*k .. t*k+k-1 (mod E): the tokens spread over
+    the most experts, so the column-slice kernel's CTAs get the most column tiles."""
+    lg = np.random.default_rng(seed).normal(size=(T, E)).astype(np.float32)
+    for t in range(T):
+        for j in range(k):
+            lg[t, (t * k + j) % E] += 20.0
+    return lg
+
+
+@pytest.mark.parametrize("name,T", [("qwen15", 16), ("qwen15", 9), ("qwen3next", 16), ("mixtral", 2)])
+def test_slice_spread_routing(name, T):
+    """The column-slice kernel with the most active experts a token count allows (Qwen1.5-shaped
+    16 tokens: 64 experts, 10 column tiles per CTA; Qwen3-Next-shaped 16 tokens: 161 experts;
+    9 tokens: a routing warp with one token beside warps with two), against the oracle on every
+    token, and the automatic path picks it for these layers at these token counts."""
+    cfg = syn.CONFIGS[name]
+    L = setup_layer(cfg, T, weights=_weights(name))
+    lg = spread_logits(T, cfg.E, cfg.k, 90 + T)
+    ws = pm.alloc_workspace(L.desc, T)
+    out = out_bits(L.plan.forward(L.hidden, torch.from_numpy(lg).cuda(), L.page_table, L.buf_slot,
+                                  workspace=ws))
+    assert L.plan.device_error() == 0
+    assert L.plan.last_run()[0] == pm.PATH_SLICE
+    st = L.plan.routing_state(ws, T)
+    rids, _ = oracle.route(lg, cfg.k, cfg.renormalize)
+    assert np.array_equal(st["ids"], rids)
+    assert len(st["active"]) == cfg.S + len(np.unique(rids)) == cfg.S + min(cfg.E, T * cfg.k)
+    ref = oracle_layer(cfg, L.w).forward(L.hidden_np, lg)
+    s = assert_close(out, ref["out_bf16"], "%s T=%d spread" % (name, T))
+    assert s["mean_rel"] <= 1e-3, s
