@@ -67,3 +67,16 @@ def test_dominant_kernel_takes_the_burst_peak_in_short_regions():
     assert long["peak"] == 1000.0 and long["peak_kind"] == "sustained"
     mem = bench.dominant_roofline({"flops": 1e9, "bytes": 1e10}, 4e-3, 5, peaks, region_s=0.1)
     assert mem["bound"] == "hbm" and mem["frac"] == pytest.approx(0.5)
+
+
+def test_kernel_names_follow_the_launch_sequence():
+    """The per-kernel timings are labelled from the launch count and the path: the routing kernel
+    and the multi-CTA sort, or the one-CTA prep; a separate row gather on the tensor-core paths
+    unless the prep copies the rows; one launch for the whole layer on the decode kernels."""
+    ids = bench.PATH_IDS
+    assert bench.kernel_names(6, ids["tc2"]) == ["route", "align", "gather", "gemm1", "gemm2", "combine"]
+    assert bench.kernel_names(5, ids["tc_decode"]) == ["prep", "gather", "gemm1", "gemm2", "combine"]
+    assert bench.kernel_names(5, ids["stream"]) == ["route", "align", "gemm1", "gemm2", "combine"]
+    assert bench.kernel_names(4, ids["tc_decode"]) == ["prep", "gemm1", "gemm2", "combine"]
+    assert bench.kernel_names(1, ids["fused"]) == ["fused"]
+    assert bench.kernel_names(1, ids["slice"]) == ["fused"]
